@@ -1,0 +1,286 @@
+/*
+ * tiles.h — C ABI of libtiles: a tile-size planner (constraints C0-C4) and
+ * the GB300 (sm_103a) kernels it drives: a tiled dense GEMM C = A x B with
+ * fp16/bf16 inputs and fp32 accumulation, optionally batched, and an NCHW
+ * conv2d run as an implicit GEMM tiled over the output height.
+ *
+ * Sources of the operations (pages of the tile-size-decision material):
+ *   - constraint procedure: page "04-tile-size-decision/tile_decision.py"
+ *     (records Device/Config/Verdict; functions evaluate, finish_parallelism,
+ *     dram_traffic, sweep) and its README ("目的": C0 with the batch term b);
+ *   - GEMM problem statement C = A x B: tiling tutorial (m.nlpx.cn/news/214310),
+ *     "案例解释 / 前提" and "Tiled 方法分块复用数据";
+ *   - H-tile rows (in_start, in_end, in_span, pt', pb', halo): the tutorial's
+ *     "H/W 维切分的通用公式" and its worked example "详细数值例子".
+ *
+ * Conventions for every call:
+ *   - Plain C types only.  Device pointers are CUDA device addresses the
+ *     caller allocated; the library allocates no device memory and never
+ *     frees caller memory.  `stream` is a cudaStream_t passed as void*
+ *     (NULL = the legacy default stream).  Launches are asynchronous.
+ *   - Every call returns TILES_OK (0) or a negative tiles_status; nothing is
+ *     printed and nothing is thrown across the ABI.  tiles_last_error()
+ *     returns a human-readable message for the calling thread's last failure.
+ *   - Matrices are row-major.  Leading dimensions (ld*) and batch strides
+ *     (stride_*) are in elements; row pitches must be multiples of 16 bytes
+ *     and base pointers 16-byte aligned (TMA requirement), else
+ *     TILES_ERR_MISALIGNED.  There is no fallback path.
+ *   - Workspace: a caller-owned device buffer of tiles_workspace_bytes()
+ *     bytes, zeroed once before first use.  Kernels record a bounded-wait
+ *     timeout in it; tiles_check() reads and clears it.  A NULL workspace
+ *     disables that report (the kernel still returns).
+ */
+#ifndef TILES_H
+#define TILES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TILES_OK = 0,
+    TILES_ERR_INVALID_ARG = -1,      /* null pointer, non-positive size, bad enum */
+    TILES_ERR_UNSUPPORTED_DTYPE = -2,
+    TILES_ERR_MISALIGNED = -3,       /* pointer or row pitch not 16-byte aligned */
+    TILES_ERR_INFEASIBLE = -4,       /* no config passes C1-C4, or the given one fails */
+    TILES_ERR_CUDA = -5,             /* a CUDA runtime/driver call failed */
+    TILES_ERR_TIMEOUT = -6,          /* a bounded device wait expired (tiles_check) */
+    TILES_ERR_TOO_LARGE = -7         /* size beyond a documented maximum */
+} tiles_status;
+
+typedef enum { TILES_F16 = 0, TILES_BF16 = 1, TILES_F32 = 2 } tiles_dtype;
+
+/* MMA families of the constraint C3.  MMA, WGMMA and SIMT are the page's
+ * instruction-shape table; TCGEN05 is the sm_100/sm_103 tensor-core MMA
+ * (kind::f16) that the GB300 kernels issue. */
+typedef enum {
+    TILES_INSTR_MMA = 0,
+    TILES_INSTR_WGMMA = 1,
+    TILES_INSTR_SIMT = 2,
+    TILES_INSTR_TCGEN05 = 3
+} tiles_instr;
+
+typedef enum { TILES_DEV_H100_PAGES = 0, TILES_DEV_GB300 = 1 } tiles_device_preset_id;
+
+/* Planner modes: PAGES reproduces the page's sweep and ranking bit for bit;
+ * GB300 ranks the configurations the sm_103a kernels implement. */
+typedef enum { TILES_MODE_PAGES = 0, TILES_MODE_GB300 = 1 } tiles_mode;
+
+/* Failure bits of a verdict (the page reports them as message prefixes). */
+#define TILES_FAIL_C3   0x1u   /* instruction shape / thread multiple / kernel layout */
+#define TILES_FAIL_C1   0x2u   /* shared-memory capacity per block */
+#define TILES_FAIL_C2   0x4u   /* registers (page) or tensor-memory columns (GB300) */
+#define TILES_FAIL_OCC  0x8u   /* no resident block fits: blocks_per_sm == 0 */
+/* Warning bits (constraint C4). */
+#define TILES_WARN_TAIL 0x1u   /* more than one wave and the last is < 50% full */
+#define TILES_WARN_IDLE 0x2u   /* fewer tiles than SMs */
+
+/* Binding resource of the occupancy computation. */
+typedef enum {
+    TILES_BIND_NONE = 0, TILES_BIND_REGS = 1, TILES_BIND_SMEM = 2,
+    TILES_BIND_THREADS = 3, TILES_BIND_TMEM = 4
+} tiles_binding;
+
+/* Hardware model (the page's Device record plus GB300 fields). */
+typedef struct {
+    int32_t smem_per_sm;              /* bytes */
+    int32_t smem_per_block_max;       /* bytes, opt-in limit of one block */
+    int32_t regs_per_sm;
+    int32_t max_threads_per_sm;
+    int32_t max_threads_per_block;
+    int32_t max_blocks_per_sm;
+    int32_t regs_per_thread_max;
+    int32_t reg_granularity_per_warp;
+    int32_t warp_size;
+    int32_t sm_count;
+    /* GB300 additions (zero on the page's device) */
+    int32_t tmem_cols;                /* tensor-memory columns per SM (512) */
+    int32_t mma_flops_per_clk;        /* dense f16/bf16 FLOP per clock per SM */
+    int32_t fill_bytes_per_clk;       /* L2 -> shared bytes per clock per SM (time model) */
+    int32_t kernel_regs_per_thread;   /* register budget of the GB300 kernels */
+    int32_t reserved[4];
+} tiles_device;
+
+/* One tile configuration (the page's Config record plus GB300 fields). */
+typedef struct {
+    int32_t bm, bn, bk;      /* output tile rows/cols and K step (elements) */
+    int32_t stages;          /* shared-memory pipeline depth */
+    int32_t threads;         /* threads per block */
+    int32_t instr;           /* tiles_instr */
+    int32_t acc_bufs;        /* GB300: TMEM accumulator buffers (0 on the page) */
+    int32_t cta_group;       /* GB300: 1 or 2 SMs per MMA (0 on the page) */
+    int32_t reserved[4];
+} tiles_config;
+
+/* Result of checking one configuration (the page's Verdict record). */
+typedef struct {
+    tiles_config cfg;
+    int64_t smem_per_stage;      /* bytes */
+    int64_t smem_total;          /* bytes (GB300: + barriers and alignment) */
+    int32_t accum_per_thread;    /* C2 accumulators per thread */
+    int32_t regs_per_thread;     /* C2, warp-rounded */
+    int32_t regs_per_block;
+    int32_t blocks_by_regs;
+    int32_t blocks_by_smem;
+    int32_t blocks_by_threads;
+    int32_t blocks_by_tmem;      /* GB300 */
+    int32_t blocks_per_sm;
+    int32_t tmem_cols_alloc;     /* GB300: power-of-two TMEM allocation */
+    int32_t binding;             /* tiles_binding */
+    uint32_t failures;           /* TILES_FAIL_* bits */
+    int32_t c3_violations;       /* how many C3 conditions failed */
+    uint32_t warnings;           /* TILES_WARN_* bits */
+    int32_t pad0;
+    int64_t grid;                /* C4: output tiles (times the batch) */
+    int64_t waves;               /* C4 */
+    double last_wave_fill;       /* C4, in [0, 1] */
+    double c0_bytes;             /* C0, float64 as on the page */
+    int64_t est_clocks;          /* GB300 time model (0 in page mode) */
+} tiles_verdict;
+
+/* A planning request. */
+typedef struct {
+    int64_t b, m, n, k;          /* batch and GEMM sizes, all >= 1 */
+    int32_t in_dtype;            /* tiles_dtype of A and B */
+    int32_t out_dtype;           /* tiles_dtype of C */
+    int32_t instr;               /* PAGES mode: the MMA family swept */
+    int32_t mode;                /* tiles_mode */
+} tiles_problem;
+
+/* Rows of one H-tile of a convolution (tutorial, "H/W 维切分的通用公式"). */
+typedef struct {
+    int32_t in_start;   /* max(0, o0*sh - pt) */
+    int32_t in_end;     /* (o1-1)*sh - pt + (kh-1)*d + 1, exclusive */
+    int32_t in_span;    /* in_end - in_start (counts pb' virtual rows) */
+    int32_t pt;         /* top pad of the sub-operator: max(0, pt - o0*sh) */
+    int32_t pb;         /* bottom pad of the sub-operator: max(0, in_end - H) */
+    int32_t halo;       /* (kh-1)*d + 1 - sh, signed */
+} tiles_htile;
+
+/* One GEMM (or a batch of equally shaped GEMMs):
+ * C[t] = A[t] x B[t] for t < batch, A[t] at a + t*stride_a, etc. */
+typedef struct {
+    int64_t m, n, k;
+    int64_t batch;                    /* >= 1; tiles_gemm requires 1 */
+    const void* a;                    /* device, M x K, row pitch lda */
+    const void* b;                    /* device, K x N, row pitch ldb */
+    void* c;                          /* device, M x N, row pitch ldc */
+    int64_t lda, ldb, ldc;            /* elements */
+    int64_t stride_a, stride_b, stride_c;   /* elements between batch items */
+    int32_t a_dtype, b_dtype, c_dtype;      /* a == b in {F16, BF16}; c in {F32, F16, BF16} */
+    int32_t pad0;
+} tiles_gemm_desc;
+
+/* An NCHW convolution with OIHW weights, NCHW output, fully packed. */
+typedef struct {
+    int32_t n, c, h, w;               /* input */
+    int32_t c_out, kh, kw;            /* weights */
+    int32_t sh, sw, ph, pw, dh, dw;   /* stride, symmetric pad, dilation */
+    int32_t in_dtype, out_dtype;      /* in: F16/BF16 (x and w); out: F16/BF16/F32 */
+    const void* x;                    /* device, [n][c][h][w] */
+    const void* wt;                   /* device, [c_out][c][kh][kw] */
+    void* y;                          /* device, [n][c_out][oh][ow] */
+} tiles_conv_desc;
+
+/* ---- status and diagnostics -------------------------------------------- */
+
+/* Static name of a status code. */
+const char* tiles_status_string(int status);
+/* Message for the calling thread's last non-OK return ("" if none). */
+const char* tiles_last_error(void);
+/* Library version string. */
+const char* tiles_version(void);
+
+/* ---- hardware model ----------------------------------------------------- */
+
+/* Fill *out with a preset: TILES_DEV_H100_PAGES is the page's Device record
+ * (132 SMs, 228 KB per SM, 227 KB per block, 65536 registers ...);
+ * TILES_DEV_GB300 is the GB300 model (148 SMs until queried, 228 KB per SM,
+ * 227 KB per block, 512 TMEM columns).  INVALID_ARG on a bad id or NULL. */
+int tiles_device_preset(int preset, tiles_device* out);
+
+/* The GB300 preset with the runtime's values for CUDA device `ordinal`
+ * (SM count, shared memory per SM and per block, registers, threads).
+ * CUDA error if no such device. */
+int tiles_device_query(int ordinal, tiles_device* out);
+
+/* ---- constraint procedure ---------------------------------------------- */
+
+/* C3, C1, C2 and occupancy for one configuration (the page's evaluate):
+ * cfg->instr selects the page's rules (MMA/WGMMA/SIMT) or the GB300 rules
+ * (TCGEN05).  elem_bytes is the input width, accum_bytes the accumulator
+ * width.  Writes *out entirely; the grid/wave/C0 fields are left zero. */
+int tiles_evaluate(const tiles_device* dev, const tiles_config* cfg, int elem_bytes,
+                   int accum_bytes, tiles_verdict* out);
+
+/* C4 (the page's finish_parallelism) for a batch of b GEMMs of M x N:
+ * grid = b*ceil(M/bm)*ceil(N/bn); waves and last-wave fill over
+ * max(blocks_per_sm * sm_count, 1) resident blocks (GB300: over resident
+ * CTA groups); sets the warning bits.  Updates *inout in place. */
+int tiles_finish_parallelism(const tiles_device* dev, int64_t b, int64_t m, int64_t n,
+                             tiles_verdict* inout);
+
+/* C0: in_bytes*b*M*N*K*(1/bn + 1/bm) + out_bytes*b*M*N, evaluated left to
+ * right in IEEE double (README "目的"; the page's dram_traffic at b=1). */
+double tiles_c0_bytes(int64_t b, int64_t m, int64_t n, int64_t k, int bm, int bn,
+                      int in_bytes, int out_bytes);
+
+/* The sweep: enumerate, keep the feasible, rank best first.  PAGES mode
+ * enumerates bm,bn in {16..256}, bk in {16..128} (<= K), stages 2..4,
+ * threads 128/256/512 and ranks by (round(C0), -blocks_per_sm, smem_total);
+ * GB300 mode enumerates the compiled sm_103a kernel variants and ranks by
+ * (est_clocks, round(C0), -blocks_per_sm, smem_total).  Ties keep the
+ * enumeration order.  Writes min(capacity, n) verdicts to out (out may be
+ * NULL when capacity is 0) and always writes *n_feasible. */
+int tiles_plan(const tiles_device* dev, const tiles_problem* prob, tiles_verdict* out,
+               int capacity, int* n_feasible);
+
+/* The H-tile rows of output rows [o0, o1) (formulas above).  INVALID_ARG if
+ * a size is non-positive, o1 <= o0 or pt < 0. */
+int tiles_htile_rows(int H, int kh, int sh, int pt, int d, int o0, int o1, tiles_htile* out);
+
+/* ---- kernels (sm_103a) --------------------------------------------------- */
+
+/* Bytes of workspace a kernel call needs (a small constant). */
+size_t tiles_workspace_bytes(void);
+
+/* C = A x B on one GPU: fp16/bf16 inputs, fp32 accumulation in tensor
+ * memory, output cast to c_dtype with round-to-nearest-even.  cfg == NULL
+ * lets the GB300 planner choose (memoised per shape); a given cfg must be a
+ * compiled variant (bm = 128*cta_group, bk = 64, acc_bufs = 2, threads 192)
+ * and pass C1-C4, else INFEASIBLE.  desc->batch must be 1.  M, N, K >= 1;
+ * ragged edges are handled (zero fill on loads, clipped stores). */
+int tiles_gemm(const tiles_gemm_desc* desc, const tiles_config* cfg, void* workspace,
+               size_t ws_bytes, void* stream);
+
+/* The batched form: desc->batch >= 1 equally shaped GEMMs with element
+ * strides stride_a/b/c between items (each a multiple of 8 elements). */
+int tiles_gemm_batched(const tiles_gemm_desc* desc, const tiles_config* cfg, void* workspace,
+                       size_t ws_bytes, void* stream);
+
+/* y = conv2d(x, w) as an implicit GEMM per output H-tile of tile_oh rows:
+ * per image and tile, M = c_out, N = tile rows x OW, K = c*kh*kw; the
+ * producer gathers the input slice [in_start, min(in_end, H)) with the
+ * sub-operator pads pt'/pb' from tiles_htile_rows.  tile_oh >= 1;
+ * c*kh*kw and OH*OW must be multiples of 8. */
+int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, read and clear the workspace's error word:
+ * TILES_OK, or TILES_ERR_TIMEOUT if a kernel's bounded wait expired. */
+int tiles_check(void* workspace, void* stream);
+
+/* Test hook for the timeout path: launches one block whose thread waits on
+ * an mbarrier that nothing arrives at, bounded by limit_ns nanoseconds; the
+ * wait expires and records a timeout in the workspace.  Returns the launch
+ * status; tiles_check then reports TILES_ERR_TIMEOUT. */
+int tiles_selftest_wait_timeout(void* workspace, int64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILES_H */

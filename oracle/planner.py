@@ -226,12 +226,15 @@ class SweepResult:
     best_fill: float        # the largest last-wave fill among them
 
 
-def sweep(m: int, n: int, k: int, dev: DeviceModel, instr: str = "wgmma") -> SweepResult:
+def sweep(m: int, n: int, k: int, dev: DeviceModel, instr: str = "wgmma", b: int = 1,
+          in_bytes: int = 2, out_bytes: int | None = None) -> SweepResult:
     """Enumerate the page's candidate grid, keep the feasible ones, rank them.
 
     Ranking: least rounded C0 first, then more resident blocks, then less
     shared memory; ties keep the enumeration order (bm, bn, bk, stages,
     threads, each ascending).  Python's round() rounds half to even.
+    b, in_bytes and out_bytes extend C0 and C4 as the README's C0 does; the
+    defaults are the page's sweep.
     """
     tmult = INSTR_MULTIPLES[instr][3]
     kept = []
@@ -244,11 +247,12 @@ def sweep(m: int, n: int, k: int, dev: DeviceModel, instr: str = "wgmma") -> Swe
                     for threads in SWEEP_THREADS:
                         if threads % tmult:
                             continue
-                        v = evaluate(TileConfig(bm, bn, bk, stages, threads, instr), dev)
+                        v = evaluate(TileConfig(bm, bn, bk, stages, threads, instr), dev,
+                                     elem_bytes=in_bytes)
                         if not v.feasible:
                             continue
-                        finish_parallelism(v, m, n, dev)
-                        v.c0_bytes = c0_bytes(m, n, k, bm, bn)
+                        finish_parallelism(v, m, n, dev, b)
+                        v.c0_bytes = c0_bytes(m, n, k, bm, bn, in_bytes, out_bytes, b)
                         kept.append(v)
     kept.sort(key=lambda v: (round(v.c0_bytes), -v.blocks_per_sm, v.smem_total))
     if kept:

@@ -1,0 +1,180 @@
+"""GB300 mode of the tile planner (oracle; test infrastructure only).
+
+Parity unpinned: no page fixes these rules.  They extend the page's
+constraint order (tile_decision.py: C3 -> C1 -> C2 -> occupancy -> C4 -> C0)
+to the sm_103a kernels of this library, and this module restates them
+independently of the C++ planner so the two can be compared bit for bit.
+The parts that reduce to the page (C0, the fill formula, the binding order)
+are pinned through the page-mode tests.
+
+Rules
+  C3   tcgen05.mma kind::f16: 128 rows per CTA (bm = 128 * cta_group,
+       cta_group 1 or 2), bn a multiple of 16 in [16, 256], bk a multiple of
+       16; the kernels' layout adds bk * in_bytes == 128 (one swizzle atom),
+       (bn / cta_group) a multiple of 64, 192 threads, 1-2 accumulators,
+       1-8 stages.  One violation count per failed condition.
+  C1   stages * ((bm/cg)*bk + bk*(bn/cg)) * in_bytes + 256 (barriers)
+       + 1024 (alignment slack) <= smem_per_block_max.
+  C2   TMEM: acc_bufs * bn fp32 columns, allocated as a power of two >= 32,
+       <= tmem_cols.
+  occupancy  least of regs (kernel_regs_per_thread * threads), smem,
+       threads, TMEM; binding order regs, smem, threads, tmem.
+  C4   grid = b * ceil(M/bm) * ceil(N/bn); resident = max(bps *
+       (sm_count // cg), 1); waves; fill as on the page.
+  C0   the page's expression with b, in_bytes, out_bytes.
+  time est_clocks = waves * ceil(K/bk) * max(mma, fill) with
+       mma = (bm/cg)*bn*bk*2 // mma_flops_per_clk and
+       fill = ceil(smem_per_stage / fill_bytes_per_clk).
+  rank (est_clocks, round(C0), -bps, smem_total), stable over the variant
+       order.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+from . import planner as page
+
+# Compiled variants (bm, bn, cta_group, stages), in enumeration order.
+VARIANTS = ((128, 64, 1, 8), (128, 128, 1, 7), (128, 192, 1, 5), (128, 256, 1, 4))
+
+THREADS = 192
+BARRIER_BYTES = 256
+ALIGN_SLACK = 1024
+MAX_STAGES = 8
+
+
+@dataclass(frozen=True)
+class GB300Device:
+    smem_per_sm: int = 228 * 1024
+    smem_per_block_max: int = 227 * 1024
+    regs_per_sm: int = 65536
+    max_threads_per_sm: int = 2048
+    max_blocks_per_sm: int = 32
+    sm_count: int = 148
+    tmem_cols: int = 512
+    mma_flops_per_clk: int = 8192
+    fill_bytes_per_clk: int = 96
+    kernel_regs_per_thread: int = 64
+
+
+@dataclass(frozen=True)
+class GB300Config:
+    bm: int
+    bn: int
+    bk: int
+    stages: int
+    threads: int = THREADS
+    acc_bufs: int = 2
+    cta_group: int = 1
+
+
+@dataclass
+class GB300Verdict:
+    cfg: GB300Config
+    c3_violations: int = 0
+    failures: list = field(default_factory=list)
+    smem_per_stage: int = 0
+    smem_total: int = 0
+    tmem_cols_alloc: int = 0
+    regs_per_thread: int = 0
+    regs_per_block: int = 0
+    blocks_by_regs: int = 0
+    blocks_by_smem: int = 0
+    blocks_by_threads: int = 0
+    blocks_by_tmem: int = 0
+    blocks_per_sm: int = 0
+    binding: str = ""
+    grid: int = 0
+    waves: int = 0
+    last_wave_fill: float = 0.0
+    warnings: list = field(default_factory=list)
+    c0_bytes: float = 0.0
+    est_clocks: int = 0
+
+
+def _tmem_alloc(cols: int) -> int:
+    p = 32
+    while p < cols:
+        p *= 2
+    return p
+
+
+def evaluate(cfg: GB300Config, dev: GB300Device, in_bytes: int = 2) -> GB300Verdict:
+    v = GB300Verdict(cfg=cfg)
+    cg = cfg.cta_group
+    bad = [cg not in (1, 2)]
+    cgs = cg if cg in (1, 2) else 1
+    bad += [
+        cfg.bm != 128 * cgs,
+        cfg.bn % 16 != 0 or cfg.bn < 16 or cfg.bn > 256,
+        cfg.bk % 16 != 0 or cfg.bk * in_bytes != 128,
+        (cfg.bn // cgs) % 64 != 0,
+        cfg.threads != THREADS,
+        not 1 <= cfg.acc_bufs <= 2,
+        not 1 <= cfg.stages <= MAX_STAGES,
+    ]
+    v.c3_violations = sum(bad)
+    if v.c3_violations:
+        v.failures.append(page.C3)
+    v.smem_per_stage = ((cfg.bm // cgs) * cfg.bk + cfg.bk * (cfg.bn // cgs)) * in_bytes
+    v.smem_total = v.smem_per_stage * cfg.stages + BARRIER_BYTES + ALIGN_SLACK
+    if v.smem_total > dev.smem_per_block_max:
+        v.failures.append(page.C1)
+    v.tmem_cols_alloc = _tmem_alloc(max(cfg.acc_bufs * cfg.bn, 1))
+    if v.tmem_cols_alloc > dev.tmem_cols:
+        v.failures.append(page.C2)
+    v.regs_per_thread = dev.kernel_regs_per_thread
+    v.regs_per_block = dev.kernel_regs_per_thread * cfg.threads
+    v.blocks_by_regs = dev.regs_per_sm // max(v.regs_per_block, 1)
+    v.blocks_by_smem = dev.smem_per_sm // max(v.smem_total, 1)
+    v.blocks_by_threads = dev.max_threads_per_sm // max(cfg.threads, 1)
+    v.blocks_by_tmem = dev.tmem_cols // max(v.tmem_cols_alloc, 1)
+    counts = (("regs", v.blocks_by_regs), ("smem", v.blocks_by_smem),
+              ("threads", v.blocks_by_threads), ("tmem", v.blocks_by_tmem))
+    least = min(c for _, c in counts)
+    v.blocks_per_sm = max(min(least, dev.max_blocks_per_sm), 0)
+    if v.blocks_per_sm == 0:
+        v.failures.append(page.OCC)
+    else:
+        v.binding = next(name for name, c in counts if c == least)
+    return v
+
+
+def finish_parallelism(v: GB300Verdict, dev: GB300Device, b: int, m: int, n: int) -> None:
+    cfg = v.cfg
+    cg = max(cfg.cta_group, 1)
+    v.grid = b * page.ceil_div(m, cfg.bm) * page.ceil_div(n, cfg.bn)
+    resident = max(v.blocks_per_sm * (dev.sm_count // cg), 1)
+    v.waves = page.ceil_div(v.grid, resident)
+    rem = v.grid % resident
+    v.last_wave_fill = rem / resident if rem else 1.0
+    v.warnings = []
+    if v.waves > 1 and v.last_wave_fill < 0.5:
+        v.warnings.append(page.W_TAIL)
+    if v.grid < dev.sm_count:
+        v.warnings.append(page.W_IDLE)
+
+
+def est_clocks(v: GB300Verdict, dev: GB300Device, k: int) -> int:
+    cfg = v.cfg
+    cg = max(cfg.cta_group, 1)
+    mma = (cfg.bm // cg) * cfg.bn * cfg.bk * 2 // dev.mma_flops_per_clk
+    fill = page.ceil_div(v.smem_per_stage, dev.fill_bytes_per_clk)
+    return v.waves * page.ceil_div(k, cfg.bk) * max(mma, fill)
+
+
+def plan(b: int, m: int, n: int, k: int, dev: GB300Device, in_bytes: int = 2,
+         out_bytes: int = 2) -> list:
+    kept = []
+    for bm, bn, cg, stages in VARIANTS:
+        cfg = GB300Config(bm, bn, 128 // in_bytes, stages, cta_group=cg)
+        v = evaluate(cfg, dev, in_bytes)
+        if v.failures:
+            continue
+        finish_parallelism(v, dev, b, m, n)
+        v.c0_bytes = page.c0_bytes(m, n, k, bm, bn, in_bytes, out_bytes, b)
+        v.est_clocks = est_clocks(v, dev, k)
+        kept.append(v)
+    kept.sort(key=lambda v: (v.est_clocks, round(v.c0_bytes), -v.blocks_per_sm, v.smem_total))
+    return kept

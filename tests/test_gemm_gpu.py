@@ -1,0 +1,200 @@
+"""GPU parity of the tcgen05 GEMM against the float64 oracle.
+
+Every case runs through the C ABI (tiles_gemm / tiles_gemm_batched via the
+binding) and compares element by element with oracle.gemm under
+|C - C_ref| <= 1e-3 * sum|A||B| + ulp_out(C_ref), or exactly where the inputs
+make the fp32 result exact.
+"""
+
+import numpy as np
+import pytest
+
+import synth_inputs as S
+from oracle import gemm as OG
+from oracle import tolerance as OT
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import tile_size_decision_gb300 as T  # noqa: E402
+from tests.gpu_util import to_cuda, to_f64, empty_out  # noqa: E402
+
+VARIANT_BN = (64, 128, 192, 256)
+STAGES = {64: 8, 128: 7, 192: 5, 256: 4}
+
+
+def variant(bn):
+    return T.make_config(128, bn, 64, STAGES[bn], 192, "tcgen05", 2, 1)
+
+
+@pytest.fixture(scope="module")
+def ws():
+    T.load()
+    return T.workspace()
+
+
+def run_gemm(a_np, b_np, in_dt, out_dt, cfg=None, ws=None, pitch_a=None, pitch_b=None,
+             pitch_c=None):
+    a = to_cuda(a_np, in_dt, pitch_a)
+    b = to_cuda(b_np, in_dt, pitch_b)
+    c = empty_out((a_np.shape[0], b_np.shape[1]), out_dt, pitch_c)
+    T.gemm(a, b, out=c, cfg=cfg, workspace=ws)
+    T.check(ws)
+    return c
+
+
+def assert_close(got, a64, b64, out_dt):
+    ref = OG.gemm(a64, b64)
+    bound = OG.gemm_bound(a64, b64)
+    ok, worst, idx = OT.check(got, ref, bound, out_dt)
+    assert ok, f"worst ratio {worst} at {idx}: got {got[idx]} want {ref[idx]}"
+
+
+@pytest.mark.parametrize("bn", VARIANT_BN)
+def test_identity_exact(ws, bn):
+    # C = I x B must return B exactly: catches swizzle, descriptor and
+    # row/column placement mistakes in every variant.
+    m, k, n = 128, 128, 2 * bn
+    a = S.quantise(np.eye(m, k), S.F16)
+    b = S.random_matrix(1, (k, n), S.F16)
+    c = run_gemm(a, b, S.F16, S.F32, variant(bn), ws)
+    assert np.array_equal(to_f64(c), S.widen(b, S.F16))
+
+
+@pytest.mark.parametrize("bn", VARIANT_BN)
+def test_permutation_exact(ws, bn):
+    rng = np.random.default_rng(3)
+    m = k = 256
+    n = bn + 64
+    perm = rng.permutation(m)
+    a = S.quantise(np.eye(m)[perm], S.BF16)
+    b = S.random_matrix(2, (k, n), S.BF16)
+    c = run_gemm(a, b, S.BF16, S.F32, variant(bn), ws)
+    assert np.array_equal(to_f64(c), S.widen(b, S.BF16)[perm])
+
+
+@pytest.mark.parametrize("bn", VARIANT_BN)
+@pytest.mark.parametrize("dt", [S.F16, S.BF16])
+def test_integer_inputs_exact(ws, bn, dt):
+    # Entries in [-2, 2] and K = 320: every partial sum is an integer below
+    # 2^24, so the fp32 accumulation is exact whatever its order.
+    m, n, k = 200, 3 * bn - 16, 320
+    a = S.integer_matrix(5, (m, k), dt)
+    b = S.integer_matrix(6, (k, n), dt)
+    c = run_gemm(a, b, dt, S.F32, variant(bn), ws)
+    assert np.array_equal(to_f64(c), OG.gemm(S.widen(a, dt), S.widen(b, dt)))
+
+
+SHAPES = [
+    (1, 1, 1), (1, 8, 8), (7, 24, 16), (16, 16, 17), (128, 64, 64), (129, 136, 80),
+    (130, 136, 80), (255, 257, 63), (256, 256, 128), (300, 200, 100), (64, 520, 1000),
+    (1000, 8, 8), (517, 611, 129),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("out_dt", [S.F32, S.F16, S.BF16])
+def test_small_shapes_planned(ws, shape, out_dt):
+    m, n, k = shape
+    in_dt = S.BF16 if out_dt == S.BF16 else S.F16
+    a = S.random_matrix(10 + m, (m, k), in_dt)
+    b = S.random_matrix(20 + n, (k, n), in_dt)
+    pa, pb = -(-k // 8) * 8, -(-n // 8) * 8
+    pc = -(-n // 8) * 8 if out_dt != S.F32 else -(-n // 4) * 4
+    c = run_gemm(a, b, in_dt, out_dt, None, ws, pa, pb, pc)
+    assert_close(to_f64(c), S.widen(a, in_dt), S.widen(b, in_dt), out_dt)
+
+
+@pytest.mark.parametrize("bn", VARIANT_BN)
+def test_ragged_every_variant_with_canaries(ws, bn):
+    # Output written into the interior of a larger buffer: rows past M and
+    # columns past N (the canary band) must stay untouched.
+    m, n, k = 333, 2 * bn + 40, 200
+    a = S.random_matrix(31, (m, k), S.F16, "normal")
+    b = S.random_matrix(32, (k, n), S.F16, "normal")
+    big = torch.full((m + 3, n + 24), 12345.0, dtype=torch.float32, device="cuda")
+    c = big[:m, :n]
+    T.gemm(to_cuda(a, S.F16, -(-k // 8) * 8), to_cuda(b, S.F16, -(-n // 8) * 8), out=c,
+           cfg=variant(bn), workspace=ws)
+    T.check(ws)
+    host = to_f64(big)
+    assert np.all(host[m:, :] == 12345.0) and np.all(host[:, n:] == 12345.0)
+    assert_close(host[:m, :n], S.widen(a, S.F16), S.widen(b, S.F16), S.F32)
+
+
+def test_batched_small(ws):
+    bsz, m, n, k = 5, 130, 200, 96
+    a = S.random_matrix(41, (bsz, m, k), S.BF16, "normal")
+    b = S.random_matrix(42, (bsz, k, n), S.BF16, "normal")
+    c = empty_out((bsz, m, n), S.BF16)
+    T.gemm_batched(to_cuda(a, S.BF16), to_cuda(b, S.BF16), out=c, workspace=ws)
+    T.check(ws)
+    assert_close(to_f64(c), S.widen(a, S.BF16), S.widen(b, S.BF16), S.BF16)
+
+
+def test_batched_rows_do_not_leak_between_items(ws):
+    # M not a multiple of the tile: a tile's rows past M must read zeros, not
+    # the next batch item's rows.  Item t of A is all (t+1), B all ones.
+    bsz, m, n, k = 3, 70, 64, 64
+    a = np.stack([np.full((m, k), t + 1.0) for t in range(bsz)])
+    a = S.quantise(a, S.F16)
+    b = S.quantise(np.ones((bsz, k, n)), S.F16)
+    c = empty_out((bsz, m, n), S.F32)
+    T.gemm_batched(to_cuda(a, S.F16), to_cuda(b, S.F16), out=c, workspace=ws)
+    T.check(ws)
+    got = to_f64(c)
+    for t in range(bsz):
+        assert np.all(got[t] == (t + 1) * k)
+
+
+def full_workload(name, ws):
+    wl = S.WORKLOADS[name]
+    a, b = S.gemm_inputs(wl)
+    ta, tb = to_cuda(a, wl.in_dtype), to_cuda(b, wl.in_dtype)
+    c = empty_out(wl.c_shape(), wl.out_dtype)
+    if wl.b > 1:
+        T.gemm_batched(ta, tb, out=c, workspace=ws)
+    else:
+        T.gemm(ta, tb, out=c, workspace=ws)
+    T.check(ws)
+    return wl, a, b, to_f64(c)
+
+
+@pytest.mark.parametrize("name", ["gemm_512", "gemm_4096", "gemm_batched", "gemm_ragged"])
+def test_workload_full_parity(ws, name):
+    wl, a, b, got = full_workload(name, ws)
+    assert_close(got, S.widen(a, wl.in_dtype), S.widen(b, wl.in_dtype), wl.out_dtype)
+
+
+def test_repeat_is_deterministic(ws):
+    wl = S.WORKLOADS["gemm_ragged"]
+    a, b = S.gemm_inputs(wl)
+    ta, tb = to_cuda(a, wl.in_dtype), to_cuda(b, wl.in_dtype)
+    c1 = T.gemm(ta, tb, out_dtype="f32", workspace=ws)
+    c2 = T.gemm(ta, tb, out_dtype="f32", workspace=ws)
+    T.check(ws)
+    assert torch.equal(c1, c2)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(ws):
+    T.selftest_wait_timeout(ws, 50_000_000)       # 50 ms
+    with pytest.raises(T.TilesError) as e:
+        T.check(ws)
+    assert e.value.status == -6
+    # The error word was cleared and the context still runs kernels.
+    T.check(ws)
+    a = S.integer_matrix(1, (128, 64), S.F16)
+    b = S.integer_matrix(2, (64, 64), S.F16)
+    c = run_gemm(a, b, S.F16, S.F32, None, ws)
+    assert np.array_equal(to_f64(c), OG.gemm(S.widen(a, S.F16), S.widen(b, S.F16)))
+
+
+def test_rejects_unaligned_pitch(ws):
+    a = torch.zeros((64, 60), dtype=torch.float16, device="cuda")
+    b = torch.zeros((60, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(T.TilesError) as e:
+        T.gemm(a, b, out_dtype="f32", workspace=ws)
+    assert e.value.status == -3

@@ -1,0 +1,245 @@
+"""tile_size_decision_gb300 — constraint-planned tiled GEMM and H-tiled
+convolution for NVIDIA GB300 (sm_103a).
+
+A thin Python binding over libtiles.so (C ABI in include/tiles.h).  The
+binding only marshals arguments: planning (C0-C4), tensor-map encoding and
+every kernel run in the native library.  PyTorch supplies device memory and
+streams.  Names follow the C ABI without the ``tiles_`` prefix.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+from . import _abi
+from ._abi import TilesError, check as _check
+
+__all__ = [
+    "TilesError", "load", "version", "device_preset", "device_query", "evaluate",
+    "finish_parallelism", "c0_bytes", "plan", "htile_rows", "workspace_bytes", "workspace",
+    "gemm", "gemm_batched", "conv2d_htiled", "check", "selftest_wait_timeout", "make_config",
+]
+
+
+def load():
+    return _abi.load()
+
+
+def version() -> str:
+    return load().tiles_version().decode()
+
+
+def device_preset(name: str = "gb300") -> _abi.Device:
+    d = _abi.Device()
+    pid = {"h100_pages": _abi.DEV_H100_PAGES, "gb300": _abi.DEV_GB300}[name]
+    _check(load().tiles_device_preset(pid, C.byref(d)), "tiles_device_preset")
+    return d
+
+
+def device_query(ordinal: int = 0) -> _abi.Device:
+    d = _abi.Device()
+    _check(load().tiles_device_query(ordinal, C.byref(d)), "tiles_device_query")
+    return d
+
+
+def make_config(bm, bn, bk, stages=3, threads=128, instr="wgmma", acc_bufs=0,
+                cta_group=0) -> _abi.Config:
+    c = _abi.Config()
+    c.bm, c.bn, c.bk, c.stages, c.threads = bm, bn, bk, stages, threads
+    c.instr = _abi.INSTR_CODES[instr] if isinstance(instr, str) else instr
+    c.acc_bufs, c.cta_group = acc_bufs, cta_group
+    return c
+
+
+def evaluate(dev: _abi.Device, cfg: _abi.Config, elem_bytes: int = 2,
+             accum_bytes: int = 4) -> _abi.Verdict:
+    v = _abi.Verdict()
+    _check(load().tiles_evaluate(C.byref(dev), C.byref(cfg), elem_bytes, accum_bytes,
+                                 C.byref(v)), "tiles_evaluate")
+    return v
+
+
+def finish_parallelism(dev: _abi.Device, v: _abi.Verdict, m: int, n: int,
+                       b: int = 1) -> _abi.Verdict:
+    _check(load().tiles_finish_parallelism(C.byref(dev), b, m, n, C.byref(v)),
+           "tiles_finish_parallelism")
+    return v
+
+
+def c0_bytes(m, n, k, bm, bn, in_bytes=2, out_bytes=None, b=1) -> float:
+    if out_bytes is None:
+        out_bytes = in_bytes
+    return load().tiles_c0_bytes(b, m, n, k, bm, bn, in_bytes, out_bytes)
+
+
+def plan(m: int, n: int, k: int, b: int = 1, in_dtype: str = "f16", out_dtype: str | None = None,
+         mode: str = "gb300", instr: str = "tcgen05", device: _abi.Device | None = None,
+         capacity: int | None = None):
+    """Ranked feasible verdicts (best first) and the count of feasible ones."""
+    lib = load()
+    if device is None:
+        device = device_preset("gb300" if mode == "gb300" else "h100_pages")
+    p = _abi.Problem()
+    p.b, p.m, p.n, p.k = b, m, n, k
+    p.in_dtype = _abi.DTYPE_CODES[in_dtype]
+    p.out_dtype = _abi.DTYPE_CODES[out_dtype or in_dtype]
+    p.instr = _abi.INSTR_CODES[instr]
+    p.mode = {"pages": _abi.MODE_PAGES, "gb300": _abi.MODE_GB300}[mode]
+    nf = C.c_int(0)
+    _check(lib.tiles_plan(C.byref(device), C.byref(p), None, 0, C.byref(nf)), "tiles_plan")
+    cap = nf.value if capacity is None else min(capacity, nf.value)
+    out = (_abi.Verdict * max(cap, 1))()
+    _check(lib.tiles_plan(C.byref(device), C.byref(p), out, cap, C.byref(nf)), "tiles_plan")
+    return list(out[:cap]), nf.value
+
+
+def htile_rows(H, kh, sh, pt, d, o0, o1) -> _abi.HTile:
+    t = _abi.HTile()
+    _check(load().tiles_htile_rows(H, kh, sh, pt, d, o0, o1, C.byref(t)), "tiles_htile_rows")
+    return t
+
+
+def workspace_bytes() -> int:
+    return int(load().tiles_workspace_bytes())
+
+
+# ---- kernels (need torch and a GPU) --------------------------------------------
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    m = {torch.float16: _abi.F16, torch.bfloat16: _abi.BF16, torch.float32: _abi.F32}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def workspace(device=None):
+    """A zeroed workspace tensor for the kernels' error word."""
+    torch = _torch()
+    return torch.zeros(workspace_bytes(), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def _cfg_ptr(cfg):
+    return C.byref(cfg) if cfg is not None else None
+
+
+def _check_operand(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name} must have unit stride in its last dimension")
+
+
+def _gemm_desc(a, b, out, batched: bool) -> _abi.GemmDesc:
+    for t, nm in ((a, "a"), (b, "b"), (out, "out")):
+        _check_operand(t, nm)
+    d = _abi.GemmDesc()
+    d.m, d.k = a.shape[-2], a.shape[-1]
+    d.n = b.shape[-1]
+    if b.shape[-2] != d.k or out.shape[-2] != d.m or out.shape[-1] != d.n:
+        raise ValueError(f"shape mismatch: {tuple(a.shape)} x {tuple(b.shape)} -> "
+                         f"{tuple(out.shape)}")
+    d.batch = a.shape[0] if batched else 1
+    d.a, d.b, d.c = a.data_ptr(), b.data_ptr(), out.data_ptr()
+    d.lda, d.ldb, d.ldc = a.stride(-2), b.stride(-2), out.stride(-2)
+    if batched:
+        if b.shape[0] != d.batch or out.shape[0] != d.batch:
+            raise ValueError("batch sizes differ")
+        d.stride_a, d.stride_b, d.stride_c = a.stride(0), b.stride(0), out.stride(0)
+    d.a_dtype, d.b_dtype, d.c_dtype = _dtype_code(a), _dtype_code(b), _dtype_code(out)
+    return d
+
+
+def _alloc_out(shape, like, out_dtype):
+    torch = _torch()
+    dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+          None: like.dtype}[out_dtype] if not isinstance(out_dtype, torch.dtype) else out_dtype
+    return torch.empty(shape, dtype=dt, device=like.device)
+
+
+def gemm(a, b, out=None, out_dtype=None, cfg=None, workspace=None, stream=None):
+    """out = a @ b for 2-D row-major CUDA tensors (fp16/bf16 in)."""
+    if out is None:
+        out = _alloc_out((a.shape[0], b.shape[1]), a, out_dtype)
+    d = _gemm_desc(a, b, out, batched=False)
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().tiles_gemm(C.byref(d), _cfg_ptr(cfg), ws, wsb, _stream_handle(stream)),
+           "tiles_gemm")
+    return out
+
+
+def gemm_batched(a, b, out=None, out_dtype=None, cfg=None, workspace=None, stream=None):
+    """out[t] = a[t] @ b[t] for 3-D CUDA tensors."""
+    if out is None:
+        out = _alloc_out((a.shape[0], a.shape[1], b.shape[2]), a, out_dtype)
+    d = _gemm_desc(a, b, out, batched=True)
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().tiles_gemm_batched(C.byref(d), _cfg_ptr(cfg), ws, wsb, _stream_handle(stream)),
+           "tiles_gemm_batched")
+    return out
+
+
+def conv_out_hw(h, w, kh, kw, stride, pad, dil):
+    oh = (h + 2 * pad[0] - (kh - 1) * dil[0] - 1) // stride[0] + 1
+    ow = (w + 2 * pad[1] - (kw - 1) * dil[1] - 1) // stride[1] + 1
+    return oh, ow
+
+
+def conv2d_htiled(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), tile_oh=16, out=None,
+                  out_dtype=None, cfg=None, workspace=None, stream=None):
+    """NCHW conv2d with OIHW weights as an implicit GEMM per output H-tile."""
+    for t, nm in ((x, "x"), (w, "w")):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous CUDA tensor")
+    n, c, h, wd = x.shape
+    co, c2, kh, kw = w.shape
+    if c2 != c:
+        raise ValueError("channel mismatch")
+    oh, ow = conv_out_hw(h, wd, kh, kw, stride, pad, dil)
+    if out is None:
+        out = _alloc_out((n, co, oh, ow), x, out_dtype)
+    if not out.is_contiguous() or tuple(out.shape) != (n, co, oh, ow):
+        raise ValueError("out must be contiguous with shape (n, c_out, oh, ow)")
+    d = _abi.ConvDesc()
+    d.n, d.c, d.h, d.w = n, c, h, wd
+    d.c_out, d.kh, d.kw = co, kh, kw
+    d.sh, d.sw = stride
+    d.ph, d.pw = pad
+    d.dh, d.dw = dil
+    d.in_dtype, d.out_dtype = _dtype_code(x), _dtype_code(out)
+    if _dtype_code(w) != d.in_dtype:
+        raise TypeError("x and w must share a dtype")
+    d.x, d.wt, d.y = x.data_ptr(), w.data_ptr(), out.data_ptr()
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().tiles_conv2d_htiled(C.byref(d), tile_oh, _cfg_ptr(cfg), ws, wsb,
+                                      _stream_handle(stream)), "tiles_conv2d_htiled")
+    return out
+
+
+def check(workspace=None, stream=None) -> None:
+    """Synchronise and raise TilesError if a kernel's bounded wait expired."""
+    ws = workspace.data_ptr() if workspace is not None else None
+    _check(load().tiles_check(ws, _stream_handle(stream)), "tiles_check")
+
+
+def selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
+    _check(load().tiles_selftest_wait_timeout(workspace.data_ptr(), limit_ns,
+                                              _stream_handle(stream)),
+           "tiles_selftest_wait_timeout")

@@ -1,0 +1,402 @@
+// C ABI of libtiles (declarations and contracts in include/tiles.h).
+//
+// Host side of the kernels: argument validation, the memoised GB300 plan,
+// TMA tensor-map encoding (through the runtime's driver entry point, so the
+// library loads without a GPU) and the launch on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "conv_sm103a.cuh"
+#include "gemm_sm103a.cuh"
+#include "tiles_internal.h"
+
+namespace tiles {
+
+namespace {
+
+thread_local std::string g_last_error;
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr size_t kWorkspaceBytes = 256;
+
+int bytes_of(int dtype) {
+    switch (dtype) {
+        case TILES_F16: case TILES_BF16: return 2;
+        case TILES_F32: return 4;
+        default: return 0;
+    }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A 3-D tensor map over a row-major [d2][d1][d0] array of 16-bit elements
+// with row pitch `pitch1` and item pitch `pitch2` (elements), box
+// {box0, box1, 1}, 128-byte swizzle, zero fill out of range.
+int encode_3d(CUtensorMap* map, int dtype, const void* base, uint64_t d0, uint64_t d1,
+              uint64_t d2, uint64_t pitch1, uint64_t pitch2, uint32_t box0, uint32_t box1) {
+    auto fn = encode_fn();
+    if (!fn) return fail(TILES_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (no CUDA driver?)");
+    const CUtensorMapDataType t =
+        dtype == TILES_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {pitch1 * 2, pitch2 * 2};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, t, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TILES_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return TILES_OK;
+}
+
+struct DeviceInfo { int ordinal; tiles_device dev; };
+
+int current_device(tiles_device* dev, int* ordinal) {
+    static std::mutex mu;
+    static std::map<int, tiles_device> cache;
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(d);
+    if (it == cache.end()) {
+        tiles_device q;
+        int s = tiles_device_query(d, &q);
+        if (s != TILES_OK) return s;
+        it = cache.emplace(d, q).first;
+    }
+    *dev = it->second;
+    if (ordinal) *ordinal = d;
+    return TILES_OK;
+}
+
+using PlanKey = std::tuple<int, int64_t, int64_t, int64_t, int64_t, int, int>;
+
+int planned_config(const tiles_device& dev, int ordinal, int64_t b, int64_t m, int64_t n,
+                   int64_t k, int in_dtype, int out_dtype, tiles_config* cfg) {
+    static std::mutex mu;
+    static std::map<PlanKey, tiles_config> cache;
+    PlanKey key{ordinal, b, m, n, k, in_dtype, out_dtype};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) { *cfg = it->second; return TILES_OK; }
+    }
+    tiles_problem p{};
+    p.b = b; p.m = m; p.n = n; p.k = k;
+    p.in_dtype = in_dtype; p.out_dtype = out_dtype;
+    p.instr = TILES_INSTR_TCGEN05; p.mode = TILES_MODE_GB300;
+    std::vector<tiles_verdict> ranked;
+    int s = plan(dev, p, &ranked);
+    if (s != TILES_OK) return s;
+    if (ranked.empty()) return fail(TILES_ERR_INFEASIBLE, "no GB300 configuration passes C1-C4");
+    *cfg = ranked.front().cfg;
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = *cfg;
+    return TILES_OK;
+}
+
+// A given configuration must be one of the compiled variants and pass C1-C4
+// on this device.
+int check_config(const tiles_device& dev, const tiles_config& cfg, int in_bytes) {
+    bool compiled = false;
+    for (int i = 0; i < kNumGemmVariants; ++i) {
+        const KernelVariant& kv = kGemmVariants[i];
+        if (kv.bm == cfg.bm && kv.bn == cfg.bn && kv.cta_group == cfg.cta_group &&
+            kv.stages == cfg.stages)
+            compiled = true;
+    }
+    tiles_verdict v;
+    evaluate(dev, cfg, in_bytes, 4, &v);
+    if (v.failures)
+        return fail(TILES_ERR_INFEASIBLE, "configuration %dx%dx%d/%d fails constraints (bits 0x%x)",
+                    cfg.bm, cfg.bn, cfg.bk, cfg.stages, v.failures);
+    if (!compiled || cfg.instr != TILES_INSTR_TCGEN05 || cfg.acc_bufs != 2)
+        return fail(TILES_ERR_INFEASIBLE, "configuration %dx%dx%d/%d is not a compiled variant",
+                    cfg.bm, cfg.bn, cfg.bk, cfg.stages);
+    return TILES_OK;
+}
+
+int launch_by_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
+                 int grid, cudaStream_t st) {
+    switch (bn) {
+        case 64: return launch_gemm_variant<64>(ta, tb, args, grid, st);
+        case 128: return launch_gemm_variant<128>(ta, tb, args, grid, st);
+        case 192: return launch_gemm_variant<192>(ta, tb, args, grid, st);
+        case 256: return launch_gemm_variant<256>(ta, tb, args, grid, st);
+        default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+}
+
+int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws, size_t ws_bytes,
+                void* stream, bool batched) {
+    if (!d) return fail(TILES_ERR_INVALID_ARG, "null descriptor");
+    if (!d->a || !d->b || !d->c) return fail(TILES_ERR_INVALID_ARG, "null matrix pointer");
+    if (d->m < 1 || d->n < 1 || d->k < 1 || d->batch < 1)
+        return fail(TILES_ERR_INVALID_ARG, "sizes must be >= 1 (m=%lld n=%lld k=%lld batch=%lld)",
+                    (long long)d->m, (long long)d->n, (long long)d->k, (long long)d->batch);
+    if (!batched && d->batch != 1)
+        return fail(TILES_ERR_INVALID_ARG, "tiles_gemm takes batch == 1; use tiles_gemm_batched");
+    if (d->m > INT32_MAX / 2 || d->n > INT32_MAX / 2 || d->k > INT32_MAX / 2 ||
+        d->batch > INT32_MAX / 2)
+        return fail(TILES_ERR_TOO_LARGE, "a size exceeds 2^30");
+    if ((d->a_dtype != TILES_F16 && d->a_dtype != TILES_BF16) || d->b_dtype != d->a_dtype)
+        return fail(TILES_ERR_UNSUPPORTED_DTYPE, "A and B must both be f16 or both bf16");
+    const int cb = bytes_of(d->c_dtype);
+    if (!cb) return fail(TILES_ERR_UNSUPPORTED_DTYPE, "C must be f32, f16 or bf16");
+    if (d->lda < d->k || d->ldb < d->n || d->ldc < d->n)
+        return fail(TILES_ERR_INVALID_ARG, "leading dimension smaller than the row length");
+    if (d->lda % 8 || d->ldb % 8 || (d->ldc * cb) % 16)
+        return fail(TILES_ERR_MISALIGNED, "row pitches must be multiples of 16 bytes");
+    if (!aligned16(d->a) || !aligned16(d->b) || !aligned16(d->c))
+        return fail(TILES_ERR_MISALIGNED, "matrix base pointers must be 16-byte aligned");
+    if (batched && d->batch > 1) {
+        if (d->stride_a % 8 || d->stride_b % 8 || (d->stride_c * cb) % 16)
+            return fail(TILES_ERR_MISALIGNED, "batch strides must be multiples of 16 bytes");
+        if (d->stride_a < d->m * d->lda || d->stride_b < d->k * d->ldb ||
+            d->stride_c < d->m * d->ldc)
+            return fail(TILES_ERR_INVALID_ARG, "batch strides overlap the items");
+    }
+    tiles_device dev;
+    int ordinal = 0;
+    int s = current_device(&dev, &ordinal);
+    if (s != TILES_OK) return s;
+    tiles_config cfg;
+    if (user_cfg) {
+        cfg = *user_cfg;
+        s = check_config(dev, cfg, 2);
+        if (s != TILES_OK) return s;
+    } else {
+        s = planned_config(dev, ordinal, d->batch, d->m, d->n, d->k, d->a_dtype, d->c_dtype, &cfg);
+        if (s != TILES_OK) return s;
+    }
+    const int64_t batch = d->batch;
+    const int64_t sa = batch > 1 ? d->stride_a : d->m * d->lda;
+    const int64_t sb = batch > 1 ? d->stride_b : d->k * d->ldb;
+    CUtensorMap ta, tb;
+    s = encode_3d(&ta, d->a_dtype, d->a, d->k, d->m, batch, d->lda, sa, 64, 128);
+    if (s != TILES_OK) return s;
+    s = encode_3d(&tb, d->b_dtype, d->b, d->n, d->k, batch, d->ldb, sb, 64, 64);
+    if (s != TILES_OK) return s;
+
+    GemmArgs args{};
+    args.m = (int32_t)d->m; args.n = (int32_t)d->n; args.k = (int32_t)d->k;
+    args.batch = (int32_t)batch;
+    args.m_blocks = (int32_t)((d->m + cfg.bm - 1) / cfg.bm);
+    args.n_blocks = (int32_t)((d->n + cfg.bn - 1) / cfg.bn);
+    args.k_blocks = (int32_t)((d->k + cfg.bk - 1) / cfg.bk);
+    const int64_t tiles = batch * args.m_blocks * args.n_blocks;
+    if (tiles > INT32_MAX) return fail(TILES_ERR_TOO_LARGE, "too many output tiles");
+    args.tiles = (int32_t)tiles;
+    args.c = d->c;
+    args.ldc = d->ldc;
+    args.stride_c = batch > 1 ? d->stride_c : 0;
+    args.c_dtype = d->c_dtype;
+    args.idesc = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, 128, cfg.bn);
+    args.err = (ws && ws_bytes >= sizeof(int32_t)) ? static_cast<int32_t*>(ws) : nullptr;
+    args.wait_limit_ns = kDefaultWaitLimitNs;
+    const int grid = (int)std::min<int64_t>(tiles, dev.sm_count);
+    int e = launch_by_bn(cfg.bn, ta, tb, args, grid, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(TILES_ERR_CUDA, "GEMM launch failed: %s",
+                    cudaGetErrorString(static_cast<cudaError_t>(e)));
+    return TILES_OK;
+}
+
+}  // namespace
+
+int fail(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+__global__ void selftest_wait_kernel(int32_t* err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on `bar`: its phase 0 never completes, so the
+    // bounded wait must give up after limit_ns and report it.
+    if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, &abort_flag, limit_ns) && err)
+        atomicOr(err, kErrSelftest);
+}
+
+}  // namespace tiles
+
+using namespace tiles;
+
+extern "C" {
+
+const char* tiles_status_string(int status) {
+    switch (status) {
+        case TILES_OK: return "TILES_OK";
+        case TILES_ERR_INVALID_ARG: return "TILES_ERR_INVALID_ARG";
+        case TILES_ERR_UNSUPPORTED_DTYPE: return "TILES_ERR_UNSUPPORTED_DTYPE";
+        case TILES_ERR_MISALIGNED: return "TILES_ERR_MISALIGNED";
+        case TILES_ERR_INFEASIBLE: return "TILES_ERR_INFEASIBLE";
+        case TILES_ERR_CUDA: return "TILES_ERR_CUDA";
+        case TILES_ERR_TIMEOUT: return "TILES_ERR_TIMEOUT";
+        case TILES_ERR_TOO_LARGE: return "TILES_ERR_TOO_LARGE";
+        default: return "TILES_ERR_UNKNOWN";
+    }
+}
+
+const char* tiles_last_error(void) { return g_last_error.c_str(); }
+
+const char* tiles_version(void) { return "tiles 0.1 (sm_103a)"; }
+
+int tiles_device_preset(int preset, tiles_device* out) {
+    if (!out) return fail(TILES_ERR_INVALID_ARG, "null output");
+    if (preset == TILES_DEV_H100_PAGES) { device_preset_h100(out); return TILES_OK; }
+    if (preset == TILES_DEV_GB300) { device_preset_gb300(out); return TILES_OK; }
+    return fail(TILES_ERR_INVALID_ARG, "unknown device preset %d", preset);
+}
+
+int tiles_device_query(int ordinal, tiles_device* out) {
+    if (!out) return fail(TILES_ERR_INVALID_ARG, "null output");
+    tiles_device d;
+    device_preset_gb300(&d);
+    struct { cudaDeviceAttr attr; int32_t* field; } q[] = {
+        {cudaDevAttrMultiProcessorCount, &d.sm_count},
+        {cudaDevAttrMaxSharedMemoryPerMultiprocessor, &d.smem_per_sm},
+        {cudaDevAttrMaxSharedMemoryPerBlockOptin, &d.smem_per_block_max},
+        {cudaDevAttrMaxRegistersPerMultiprocessor, &d.regs_per_sm},
+        {cudaDevAttrMaxThreadsPerMultiProcessor, &d.max_threads_per_sm},
+        {cudaDevAttrMaxThreadsPerBlock, &d.max_threads_per_block},
+        {cudaDevAttrMaxBlocksPerMultiprocessor, &d.max_blocks_per_sm},
+        {cudaDevAttrWarpSize, &d.warp_size},
+    };
+    for (auto& e : q) {
+        int v = 0;
+        cudaError_t r = cudaDeviceGetAttribute(&v, e.attr, ordinal);
+        if (r != cudaSuccess)
+            return fail(TILES_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(r));
+        *e.field = v;
+    }
+    int major = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, ordinal);
+    d.tmem_cols = major == 10 ? 512 : 0;
+    *out = d;
+    return TILES_OK;
+}
+
+int tiles_evaluate(const tiles_device* dev, const tiles_config* cfg, int elem_bytes,
+                   int accum_bytes, tiles_verdict* out) {
+    if (!dev || !cfg || !out) return fail(TILES_ERR_INVALID_ARG, "null argument");
+    if (elem_bytes <= 0 || accum_bytes <= 0 || cfg->bm <= 0 || cfg->bn <= 0 || cfg->bk <= 0 ||
+        cfg->stages <= 0 || cfg->threads <= 0)
+        return fail(TILES_ERR_INVALID_ARG, "sizes must be positive");
+    return evaluate(*dev, *cfg, elem_bytes, accum_bytes, out);
+}
+
+int tiles_finish_parallelism(const tiles_device* dev, int64_t b, int64_t m, int64_t n,
+                             tiles_verdict* inout) {
+    if (!dev || !inout) return fail(TILES_ERR_INVALID_ARG, "null argument");
+    if (b < 1 || m < 1 || n < 1) return fail(TILES_ERR_INVALID_ARG, "sizes must be >= 1");
+    finish_parallelism(*dev, b, m, n, inout);
+    return TILES_OK;
+}
+
+double tiles_c0_bytes(int64_t b, int64_t m, int64_t n, int64_t k, int bm, int bn, int in_bytes,
+                      int out_bytes) {
+    if (bm <= 0 || bn <= 0) return 0.0;
+    return c0_bytes(b, m, n, k, bm, bn, in_bytes, out_bytes);
+}
+
+int tiles_plan(const tiles_device* dev, const tiles_problem* prob, tiles_verdict* out,
+               int capacity, int* n_feasible) {
+    if (!dev || !prob || !n_feasible || capacity < 0 || (capacity > 0 && !out))
+        return fail(TILES_ERR_INVALID_ARG, "null argument or negative capacity");
+    *n_feasible = 0;
+    if (prob->b < 1 || prob->m < 1 || prob->n < 1 || prob->k < 1)
+        return fail(TILES_ERR_INVALID_ARG, "sizes must be >= 1");
+    std::vector<tiles_verdict> ranked;
+    int s = plan(*dev, *prob, &ranked);
+    if (s != TILES_OK) return fail(s, "planning failed");
+    *n_feasible = (int)ranked.size();
+    for (int i = 0; i < capacity && i < (int)ranked.size(); ++i) out[i] = ranked[i];
+    return TILES_OK;
+}
+
+int tiles_htile_rows(int H, int kh, int sh, int pt, int d, int o0, int o1, tiles_htile* out) {
+    if (!out) return fail(TILES_ERR_INVALID_ARG, "null output");
+    int s = htile_rows(H, kh, sh, pt, d, o0, o1, out);
+    if (s != TILES_OK) return fail(s, "invalid H-tile arguments");
+    return TILES_OK;
+}
+
+size_t tiles_workspace_bytes(void) { return kWorkspaceBytes; }
+
+int tiles_gemm(const tiles_gemm_desc* desc, const tiles_config* cfg, void* ws, size_t ws_bytes,
+               void* stream) {
+    return gemm_common(desc, cfg, ws, ws_bytes, stream, false);
+}
+
+int tiles_gemm_batched(const tiles_gemm_desc* desc, const tiles_config* cfg, void* ws,
+                       size_t ws_bytes, void* stream) {
+    return gemm_common(desc, cfg, ws, ws_bytes, stream, true);
+}
+
+int tiles_check(void* ws, void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+    if (!ws) return TILES_OK;
+    int32_t word = 0;
+    e = cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "read workspace: %s", cudaGetErrorString(e));
+    if (word == 0) return TILES_OK;
+    e = cudaMemset(ws, 0, sizeof(word));
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "clear workspace: %s", cudaGetErrorString(e));
+    return fail(TILES_ERR_TIMEOUT, "a bounded device wait expired (error bits 0x%x)", word);
+}
+
+int tiles_selftest_wait_timeout(void* ws, int64_t limit_ns, void* stream) {
+    if (limit_ns <= 0 || limit_ns > 10000000000ll)
+        return fail(TILES_ERR_INVALID_ARG, "limit_ns must be in (0, 1e10]");
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<int32_t*>(ws), (uint64_t)limit_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return TILES_OK;
+}
+
+int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
+                        void* ws, size_t ws_bytes, void* stream) {
+    return conv2d_htiled(desc, tile_oh, cfg, ws, ws_bytes, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,320 @@
+// Tile-size planner: constraints C0-C4, the sweep and the H-tile rows.
+//
+// Page mode follows the page "04-tile-size-decision/tile_decision.py"
+// (evaluate: C3 -> C1 -> C2 -> occupancy; finish_parallelism: C4;
+// dram_traffic: C0; sweep: enumerate, filter, rank) and its README (C0 with
+// the batch term b).  GB300 mode applies the same constraint order to the
+// sm_103a kernels of this library: C3 becomes the tcgen05 kind::f16 shape
+// and the kernels' tile layout, C2 becomes the tensor-memory (TMEM) column
+// budget of the accumulators, C4 counts waves of persistent CTA groups, and
+// the ranking puts a wave-quantised time estimate before C0.
+//
+// Host-only C++; no CUDA here.
+
+#include "tiles_internal.h"
+
+#include <algorithm>
+#include <cfenv>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+namespace tiles {
+
+namespace {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// (M multiple, N multiple, K multiple, thread multiple) of the page's
+// instruction-shape table: mma m16n8k16 (warp), wgmma m64nNk16 (warpgroup),
+// scalar.
+struct InstrMultiples { int m, n, k, t; };
+
+bool page_multiples(int instr, InstrMultiples* out) {
+    switch (instr) {
+        case TILES_INSTR_MMA:   *out = {16, 8, 16, 32}; return true;
+        case TILES_INSTR_WGMMA: *out = {64, 8, 16, 128}; return true;
+        case TILES_INSTR_SIMT:  *out = {1, 1, 1, 32}; return true;
+        default: return false;
+    }
+}
+
+// Occupancy shared by both modes: least of the per-resource block counts,
+// capped by the hardware limit; the binding resource is the first reaching
+// that least value in the order regs, smem, threads (then TMEM in GB300 mode).
+void occupancy(const tiles_device& dev, tiles_verdict* v, bool with_tmem) {
+    v->blocks_by_regs = dev.regs_per_sm / std::max(v->regs_per_block, 1);
+    v->blocks_by_smem = (int32_t)(dev.smem_per_sm / std::max<int64_t>(v->smem_total, 1));
+    v->blocks_by_threads = dev.max_threads_per_sm / std::max(v->cfg.threads, 1);
+    int least = std::min(v->blocks_by_regs, std::min(v->blocks_by_smem, v->blocks_by_threads));
+    if (with_tmem) least = std::min(least, v->blocks_by_tmem);
+    v->blocks_per_sm = std::max(std::min(least, dev.max_blocks_per_sm), 0);
+    v->binding = TILES_BIND_NONE;
+    if (v->blocks_per_sm == 0) {
+        v->failures |= TILES_FAIL_OCC;
+        return;
+    }
+    if (v->blocks_by_regs == least) v->binding = TILES_BIND_REGS;
+    else if (v->blocks_by_smem == least) v->binding = TILES_BIND_SMEM;
+    else if (v->blocks_by_threads == least) v->binding = TILES_BIND_THREADS;
+    else v->binding = TILES_BIND_TMEM;
+}
+
+void evaluate_page(const tiles_device& dev, const tiles_config& cfg, int elem_bytes,
+                   int accum_bytes, tiles_verdict* v) {
+    InstrMultiples im;
+    page_multiples(cfg.instr, &im);
+    // C3: instruction shape, checked first.
+    int c3 = 0;
+    if (cfg.bm % im.m) ++c3;
+    if (cfg.bn % im.n) ++c3;
+    if (cfg.bk % im.k) ++c3;
+    if (cfg.threads % im.t) ++c3;
+    if (cfg.threads > dev.max_threads_per_block) ++c3;
+    v->c3_violations = c3;
+    if (c3) v->failures |= TILES_FAIL_C3;
+    // C1: A and B slices of one stage, times the pipeline depth.
+    v->smem_per_stage = ((int64_t)cfg.bm * cfg.bk + (int64_t)cfg.bk * cfg.bn) * elem_bytes;
+    v->smem_total = v->smem_per_stage * cfg.stages;
+    if (v->smem_total > dev.smem_per_block_max) v->failures |= TILES_FAIL_C1;
+    // C2: accumulators per thread in 32-bit registers, rounded to the
+    // per-warp allocation granule.
+    v->accum_per_thread = (int32_t)ceil_div((int64_t)cfg.bm * cfg.bn, cfg.threads);
+    int64_t words = (int64_t)v->accum_per_thread * accum_bytes / 4;
+    int64_t per_warp = ceil_div(words * dev.warp_size, dev.reg_granularity_per_warp) *
+                       dev.reg_granularity_per_warp;
+    v->regs_per_thread = (int32_t)(per_warp / dev.warp_size);
+    if (v->regs_per_thread > dev.regs_per_thread_max) v->failures |= TILES_FAIL_C2;
+    v->regs_per_block = v->regs_per_thread * cfg.threads;
+    occupancy(dev, v, false);
+}
+
+}  // namespace
+
+// GB300 kernel variants compiled into this library (bm, bn, cta_group,
+// stages), in enumeration order.  bk is one 128-byte swizzle atom of the
+// input type; the stage count is the deepest pipeline that fits 227 KB.
+const KernelVariant kGemmVariants[] = {
+    {128, 64, 1, 8}, {128, 128, 1, 7}, {128, 192, 1, 5}, {128, 256, 1, 4},
+};
+const int kNumGemmVariants = sizeof(kGemmVariants) / sizeof(kGemmVariants[0]);
+
+int64_t gb300_smem_bytes(const tiles_config& cfg, int in_bytes, int64_t* per_stage) {
+    const int cg = std::max(cfg.cta_group, 1);
+    int64_t stage = ((int64_t)(cfg.bm / cg) * cfg.bk + (int64_t)cfg.bk * (cfg.bn / cg)) * in_bytes;
+    if (per_stage) *per_stage = stage;
+    return stage * cfg.stages + kSmemBarrierBytes + kSmemAlignSlack;
+}
+
+static int pow2_at_least(int x) {
+    int p = 32;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+void evaluate_gb300(const tiles_device& dev, const tiles_config& cfg, int in_bytes,
+                    tiles_verdict* v) {
+    const int cg = cfg.cta_group;
+    // C3: tcgen05.mma kind::f16 takes M = 128 rows per CTA (cta_group::1:
+    // M 128; ::2: M 256 over the pair), N a multiple of 16 in [16, 256], K 16
+    // per instruction.  The kernels add their tile layout: a K block is one
+    // 128-byte swizzle atom, B arrives in 64-column atoms per CTA, threads
+    // are the 6 warps of the warp-specialised block.
+    int c3 = 0;
+    if (cg != 1 && cg != 2) ++c3;
+    const int cgs = (cg == 1 || cg == 2) ? cg : 1;
+    if (cfg.bm != 128 * cgs) ++c3;
+    if (cfg.bn % 16 || cfg.bn < 16 || cfg.bn > 256) ++c3;
+    if (cfg.bk % 16 || cfg.bk * in_bytes != 128) ++c3;
+    if ((cfg.bn / cgs) % 64) ++c3;
+    if (cfg.threads != kGemmThreads) ++c3;
+    if (cfg.acc_bufs < 1 || cfg.acc_bufs > 2) ++c3;
+    if (cfg.stages < 1 || cfg.stages > kMaxStages) ++c3;
+    v->c3_violations = c3;
+    if (c3) v->failures |= TILES_FAIL_C3;
+    // C1: pipeline stages plus barriers and the 1 KB alignment slack of the
+    // swizzled operand tiles, within the opt-in per-block limit.
+    tiles_config c = cfg;
+    c.cta_group = cgs;
+    v->smem_total = gb300_smem_bytes(c, in_bytes, &v->smem_per_stage);
+    if (v->smem_total > dev.smem_per_block_max) v->failures |= TILES_FAIL_C1;
+    // C2: the fp32 accumulators live in TMEM, 128 lanes x bn columns per
+    // buffer per CTA; the allocation is a power of two of at least 32.
+    int cols = std::max(cfg.acc_bufs, 0) * cfg.bn;
+    v->tmem_cols_alloc = pow2_at_least(std::max(cols, 1));
+    if (v->tmem_cols_alloc > dev.tmem_cols) v->failures |= TILES_FAIL_C2;
+    v->accum_per_thread = 0;
+    v->regs_per_thread = dev.kernel_regs_per_thread;
+    v->regs_per_block = dev.kernel_regs_per_thread * cfg.threads;
+    v->blocks_by_tmem = dev.tmem_cols / std::max(v->tmem_cols_alloc, 1);
+    occupancy(dev, v, true);
+}
+
+int evaluate(const tiles_device& dev, const tiles_config& cfg, int elem_bytes, int accum_bytes,
+             tiles_verdict* v) {
+    std::memset(v, 0, sizeof(*v));
+    v->cfg = cfg;
+    if (cfg.instr == TILES_INSTR_TCGEN05) {
+        evaluate_gb300(dev, cfg, elem_bytes, v);
+        return TILES_OK;
+    }
+    InstrMultiples im;
+    if (!page_multiples(cfg.instr, &im)) return TILES_ERR_INVALID_ARG;
+    evaluate_page(dev, cfg, elem_bytes, accum_bytes, v);
+    return TILES_OK;
+}
+
+void finish_parallelism(const tiles_device& dev, int64_t b, int64_t m, int64_t n,
+                        tiles_verdict* v) {
+    const tiles_config& cfg = v->cfg;
+    v->grid = b * ceil_div(m, cfg.bm) * ceil_div(n, cfg.bn);
+    int64_t resident;
+    if (cfg.instr == TILES_INSTR_TCGEN05) {
+        // Persistent CTA groups: each group of cta_group SMs holds
+        // blocks_per_sm groups at a time.
+        const int cg = std::max(cfg.cta_group, 1);
+        resident = std::max<int64_t>((int64_t)v->blocks_per_sm * (dev.sm_count / cg), 1);
+    } else {
+        resident = std::max<int64_t>((int64_t)v->blocks_per_sm * dev.sm_count, 1);
+    }
+    v->waves = ceil_div(v->grid, resident);
+    int64_t rem = v->grid % resident;
+    v->last_wave_fill = rem ? (double)rem / (double)resident : 1.0;
+    v->warnings = 0;
+    if (v->waves > 1 && v->last_wave_fill < 0.5) v->warnings |= TILES_WARN_TAIL;
+    if (v->grid < dev.sm_count) v->warnings |= TILES_WARN_IDLE;
+}
+
+double c0_bytes(int64_t b, int64_t m, int64_t n, int64_t k, int bm, int bn, int in_bytes,
+                int out_bytes) {
+    // Left to right in double, as the page's expression: the integer product
+    // converts once, then multiplies (1/bn + 1/bm); the output term adds.
+    // The products are formed exactly in 128 bits, like Python's integers.
+    const __int128 rd = (__int128)in_bytes * b * m * n * k;
+    const __int128 wr = (__int128)out_bytes * b * m * n;
+    double reads = (double)rd * (1.0 / bn + 1.0 / bm);
+    return reads + (double)wr;
+}
+
+// Round half to even, as Python's round() on a float.
+static int64_t round_even(double x) {
+    const int saved = std::fegetround();
+    std::fesetround(FE_TONEAREST);
+    double r = std::nearbyint(x);
+    std::fesetround(saved);
+    return (int64_t)r;
+}
+
+int64_t gb300_est_clocks(const tiles_device& dev, const tiles_verdict& v, int64_t k) {
+    const tiles_config& cfg = v.cfg;
+    const int cg = std::max(cfg.cta_group, 1);
+    int64_t kblocks = ceil_div(k, cfg.bk);
+    int64_t mma = (int64_t)(cfg.bm / cg) * cfg.bn * cfg.bk * 2 / std::max(dev.mma_flops_per_clk, 1);
+    int64_t fill = ceil_div(v.smem_per_stage, std::max(dev.fill_bytes_per_clk, 1));
+    return v.waves * kblocks * std::max(mma, fill);
+}
+
+static int bytes_of(int dtype) {
+    switch (dtype) {
+        case TILES_F16: case TILES_BF16: return 2;
+        case TILES_F32: return 4;
+        default: return 0;
+    }
+}
+
+int plan(const tiles_device& dev, const tiles_problem& p, std::vector<tiles_verdict>* out) {
+    const int in_b = bytes_of(p.in_dtype), out_b = bytes_of(p.out_dtype);
+    if (!in_b || !out_b) return TILES_ERR_UNSUPPORTED_DTYPE;
+    struct Ranked { tiles_verdict v; int64_t c0r; int64_t order; };
+    std::vector<Ranked> kept;
+    int64_t order = 0;
+    if (p.mode == TILES_MODE_PAGES) {
+        InstrMultiples im;
+        if (!page_multiples(p.instr, &im)) return TILES_ERR_INVALID_ARG;
+        static const int BM[] = {16, 32, 64, 128, 256}, BK[] = {16, 32, 64, 128};
+        static const int ST[] = {2, 3, 4}, TH[] = {128, 256, 512};
+        for (int bm : BM) for (int bn : BM) for (int bk : BK) {
+            if (bk > p.k) continue;
+            for (int st : ST) for (int th : TH) {
+                if (th % im.t) continue;
+                tiles_config c{};
+                c.bm = bm; c.bn = bn; c.bk = bk; c.stages = st; c.threads = th; c.instr = p.instr;
+                tiles_verdict v;
+                evaluate(dev, c, in_b, 4, &v);
+                if (v.failures) continue;
+                finish_parallelism(dev, p.b, p.m, p.n, &v);
+                v.c0_bytes = c0_bytes(p.b, p.m, p.n, p.k, bm, bn, in_b, out_b);
+                kept.push_back({v, round_even(v.c0_bytes), order++});
+            }
+        }
+        std::stable_sort(kept.begin(), kept.end(), [](const Ranked& a, const Ranked& b) {
+            if (a.c0r != b.c0r) return a.c0r < b.c0r;
+            if (a.v.blocks_per_sm != b.v.blocks_per_sm) return a.v.blocks_per_sm > b.v.blocks_per_sm;
+            return a.v.smem_total < b.v.smem_total;
+        });
+    } else if (p.mode == TILES_MODE_GB300) {
+        if (in_b != 2) return TILES_ERR_UNSUPPORTED_DTYPE;
+        for (int i = 0; i < kNumGemmVariants; ++i) {
+            const KernelVariant& kv = kGemmVariants[i];
+            tiles_config c{};
+            c.bm = kv.bm; c.bn = kv.bn; c.bk = 128 / in_b; c.threads = kGemmThreads;
+            c.instr = TILES_INSTR_TCGEN05; c.acc_bufs = 2; c.cta_group = kv.cta_group;
+            c.stages = kv.stages;
+            tiles_verdict v;
+            evaluate(dev, c, in_b, 4, &v);
+            if (v.failures) continue;
+            finish_parallelism(dev, p.b, p.m, p.n, &v);
+            v.c0_bytes = c0_bytes(p.b, p.m, p.n, p.k, c.bm, c.bn, in_b, out_b);
+            v.est_clocks = gb300_est_clocks(dev, v, p.k);
+            kept.push_back({v, round_even(v.c0_bytes), order++});
+        }
+        std::stable_sort(kept.begin(), kept.end(), [](const Ranked& a, const Ranked& b) {
+            if (a.v.est_clocks != b.v.est_clocks) return a.v.est_clocks < b.v.est_clocks;
+            if (a.c0r != b.c0r) return a.c0r < b.c0r;
+            if (a.v.blocks_per_sm != b.v.blocks_per_sm) return a.v.blocks_per_sm > b.v.blocks_per_sm;
+            return a.v.smem_total < b.v.smem_total;
+        });
+    } else {
+        return TILES_ERR_INVALID_ARG;
+    }
+    out->clear();
+    for (auto& r : kept) out->push_back(r.v);
+    return TILES_OK;
+}
+
+void device_preset_h100(tiles_device* d) {
+    std::memset(d, 0, sizeof(*d));
+    d->smem_per_sm = 228 * 1024;
+    d->smem_per_block_max = 227 * 1024;
+    d->regs_per_sm = 65536;
+    d->max_threads_per_sm = 2048;
+    d->max_threads_per_block = 1024;
+    d->max_blocks_per_sm = 32;
+    d->regs_per_thread_max = 255;
+    d->reg_granularity_per_warp = 256;
+    d->warp_size = 32;
+    d->sm_count = 132;
+}
+
+void device_preset_gb300(tiles_device* d) {
+    device_preset_h100(d);
+    d->sm_count = 148;
+    d->tmem_cols = 512;
+    d->mma_flops_per_clk = 8192;
+    d->fill_bytes_per_clk = kDefaultFillBytesPerClk;
+    d->kernel_regs_per_thread = kGemmRegsPerThread;
+}
+
+int htile_rows(int H, int kh, int sh, int pt, int d, int o0, int o1, tiles_htile* t) {
+    if (H <= 0 || kh <= 0 || sh <= 0 || d <= 0 || pt < 0 || o0 < 0 || o1 <= o0)
+        return TILES_ERR_INVALID_ARG;
+    t->in_start = std::max(0, o0 * sh - pt);
+    t->in_end = (o1 - 1) * sh - pt + (kh - 1) * d + 1;
+    t->in_span = t->in_end - t->in_start;
+    t->pt = std::max(0, pt - o0 * sh);
+    t->pb = std::max(0, t->in_end - H);
+    t->halo = (kh - 1) * d + 1 - sh;
+    return TILES_OK;
+}
+
+}  // namespace tiles

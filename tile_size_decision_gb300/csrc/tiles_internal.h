@@ -1,0 +1,52 @@
+// Internal declarations shared by the planner, the C ABI and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "../../include/tiles.h"
+
+namespace tiles {
+
+// Threads of the warp-specialised GEMM block: warp 0 TMA producer, warp 1
+// MMA issuer and TMEM owner, warps 2-5 epilogue.
+constexpr int kGemmThreads = 192;
+// Registers per thread of the GEMM kernels as built (ptxas reports 61,
+// which the per-warp granule of 256 rounds to 64); the planner's occupancy
+// uses this figure.
+constexpr int kGemmRegsPerThread = 64;
+// Shared memory beyond the operand stages: mbarriers, the TMEM address slot,
+// an abort flag (kSmemBarrierBytes) and the slack that lets the operand
+// tiles start on a 1024-byte boundary, as the 128-byte swizzle requires.
+constexpr int kSmemBarrierBytes = 256;
+constexpr int kSmemAlignSlack = 1024;
+constexpr int kMaxStages = 8;
+// Default L2 -> shared-memory fill rate per SM per clock used by the GB300
+// time model (bytes).  A model parameter, not a measured constant.
+constexpr int kDefaultFillBytesPerClk = 96;
+
+// A compiled kernel variant: tile rows and columns, SMs per MMA, and the
+// pipeline depth it was built with.
+struct KernelVariant { int bm, bn, cta_group, stages; };
+extern const KernelVariant kGemmVariants[];
+extern const int kNumGemmVariants;
+
+int evaluate(const tiles_device& dev, const tiles_config& cfg, int elem_bytes, int accum_bytes,
+             tiles_verdict* v);
+void finish_parallelism(const tiles_device& dev, int64_t b, int64_t m, int64_t n,
+                        tiles_verdict* v);
+double c0_bytes(int64_t b, int64_t m, int64_t n, int64_t k, int bm, int bn, int in_bytes,
+                int out_bytes);
+int plan(const tiles_device& dev, const tiles_problem& p, std::vector<tiles_verdict>* out);
+int64_t gb300_smem_bytes(const tiles_config& cfg, int in_bytes, int64_t* per_stage);
+int64_t gb300_est_clocks(const tiles_device& dev, const tiles_verdict& v, int64_t k);
+void device_preset_h100(tiles_device* d);
+void device_preset_gb300(tiles_device* d);
+int htile_rows(int H, int kh, int sh, int pt, int d, int o0, int o1, tiles_htile* t);
+int conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg, void* ws,
+                  size_t ws_bytes, void* stream);
+
+// Per-thread error text (tiles_last_error).
+int fail(int status, const char* fmt, ...);
+
+}  // namespace tiles

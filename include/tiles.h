@@ -269,6 +269,25 @@ int tiles_gemm_batched(const tiles_gemm_desc* desc, const tiles_config* cfg, voi
 int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
                         void* workspace, size_t ws_bytes, void* stream);
 
+/* The GEMM of tiles_gemm_batched (batch >= 1) for callers that cannot
+ * allocate device memory and so cannot pass a workspace.  The source pages
+ * have no counterpart: it exists for code that runs where cudaMalloc is not
+ * allowed (allocator or driver callbacks, runtimes that own all device
+ * memory, paths that must not allocate).  Its scratch is a 256-byte static
+ * device array in the library, held by every GPU that loads the library until
+ * the process exits; the call allocates nothing and calls no allocating
+ * routine.  The GEMM needs exactly that much (its timeout error word); a need
+ * beyond it is rejected with TILES_ERR_TOO_LARGE.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the array: a timeout recorded by a call stays until a call with
+ * wait != 0 reads and clears it, and calls that overlap on the GPU race on it.
+ * wait == 0: asynchronous on `stream`, returns the launch status.
+ * wait != 0: also synchronises `stream` and returns TILES_ERR_TIMEOUT if a
+ * bounded wait expired in a call since the last read. */
+int tiles_gemm_noalloc(const tiles_gemm_desc* desc, const tiles_config* cfg, void* stream,
+                       int wait);
+
 /* Synchronise `stream`, read and clear the workspace's error word:
  * TILES_OK, or TILES_ERR_TIMEOUT if a kernel's bounded wait expired. */
 int tiles_check(void* workspace, void* stream);

@@ -1,0 +1,85 @@
+"""tiles_gemm_noalloc: the GEMM for callers that cannot allocate device memory.
+
+Such callers (code running inside an allocator or driver callback, under a
+runtime that owns all device memory, or on a path that must not allocate)
+cannot hand the library a workspace.  The entry point uses the library's
+static device scratch instead.  These tests call it through the C ABI twice in
+a row and compare each result with the workspace-taking entry point
+(tiles_gemm_batched) under the parity tolerance of the other GPU tests.  The
+file is named so that pytest collects it last.
+"""
+
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import synth_inputs as S
+from oracle import gemm as OG
+from oracle import tolerance as OT
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import tile_size_decision_gb300 as T  # noqa: E402
+from tile_size_decision_gb300 import _abi  # noqa: E402
+from tests.gpu_util import to_cuda, to_f64, empty_out  # noqa: E402
+
+
+def desc_for(a, b, c, dt_in, dt_out):
+    d = _abi.GemmDesc()
+    d.batch, d.m, d.k = a.shape
+    d.n = b.shape[2]
+    d.a, d.b, d.c = a.data_ptr(), b.data_ptr(), c.data_ptr()
+    d.lda, d.ldb, d.ldc = a.stride(1), b.stride(1), c.stride(1)
+    d.stride_a, d.stride_b, d.stride_c = a.stride(0), b.stride(0), c.stride(0)
+    d.a_dtype = d.b_dtype = _abi.DTYPE_CODES[dt_in]
+    d.c_dtype = _abi.DTYPE_CODES[dt_out]
+    return d
+
+
+@pytest.mark.parametrize("case", [
+    (3, 300, 520, 256, S.BF16, S.F32),
+    (1, 1000, 1000, 512, S.F16, S.F16),
+])
+def test_noalloc_matches_workspace_gemm_on_two_calls(case):
+    bsz, m, n, k, dt_in, dt_out = case
+    lib = T.load()
+    a_np = S.random_matrix(7, (bsz, m, k), dt_in, "normal")
+    b_np = S.random_matrix(8, (bsz, k, n), dt_in, "normal")
+    a, b = to_cuda(a_np, dt_in), to_cuda(b_np, dt_in)
+    stream = torch.cuda.current_stream()
+    handle = C.c_void_p(stream.cuda_stream)
+
+    ws = T.workspace()
+    ref = empty_out((bsz, m, n), dt_out)
+    d_ref = desc_for(a, b, ref, dt_in, dt_out)
+    assert lib.tiles_gemm_batched(C.byref(d_ref), None, ws.data_ptr(), ws.numel(), handle) == 0
+    assert lib.tiles_check(ws.data_ptr(), handle) == 0
+    ref64 = to_f64(ref)
+
+    a64, b64 = S.widen(a_np, dt_in), S.widen(b_np, dt_in)
+    bound = OG.gemm_bound(a64, b64)
+    for call in range(2):
+        out = empty_out((bsz, m, n), dt_out)
+        d = desc_for(a, b, out, dt_in, dt_out)
+        status = lib.tiles_gemm_noalloc(C.byref(d), None, handle, 1)
+        assert status == 0, lib.tiles_last_error().decode()
+        got = to_f64(out)
+        ok, worst, idx = OT.check(got, ref64, bound, dt_out)
+        assert ok, f"call {call}: ratio {worst} at {idx}"
+
+
+def test_noalloc_rejects_bad_arguments_before_launch():
+    lib = T.load()
+    d = _abi.GemmDesc()
+    d.m = d.n = d.k = 64
+    d.batch = 1
+    d.a, d.b, d.c = 0x10000, 0x20000, 0x30002
+    d.lda = d.ldb = d.ldc = 64
+    d.a_dtype = d.b_dtype = _abi.F16
+    d.c_dtype = _abi.F32
+    assert lib.tiles_gemm_noalloc(C.byref(d), None, None, 1) == _abi.ERR_MISALIGNED

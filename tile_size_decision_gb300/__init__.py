@@ -17,7 +17,7 @@ from ._abi import TilesError, check as _check
 __all__ = [
     "TilesError", "load", "version", "device_preset", "device_query", "evaluate",
     "finish_parallelism", "c0_bytes", "plan", "htile_rows", "workspace_bytes", "workspace",
-    "gemm", "gemm_batched", "conv2d_htiled", "check", "selftest_wait_timeout", "make_config",
+    "gemm", "gemm_batched", "gemm_noalloc", "conv2d_htiled", "check", "selftest_wait_timeout", "make_config",
 ]
 
 
@@ -230,6 +230,18 @@ def conv2d_htiled(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), tile_oh=16, out=N
     wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().tiles_conv2d_htiled(C.byref(d), tile_oh, _cfg_ptr(cfg), ws, wsb,
                                       _stream_handle(stream)), "tiles_conv2d_htiled")
+    return out
+
+
+def gemm_noalloc(a, b, out=None, out_dtype=None, cfg=None, stream=None, wait=False):
+    """out[t] = a[t] @ b[t] (3-D tensors) without a workspace: for callers
+    that cannot allocate device memory.  The library's static scratch takes
+    the workspace's place; wait=True synchronises and reports a timeout."""
+    if out is None:
+        out = _alloc_out((a.shape[0], a.shape[1], b.shape[2]), a, out_dtype)
+    d = _gemm_desc(a, b, out, batched=True)
+    _check(load().tiles_gemm_noalloc(C.byref(d), _cfg_ptr(cfg), _stream_handle(stream),
+                                     1 if wait else 0), "tiles_gemm_noalloc")
     return out
 
 

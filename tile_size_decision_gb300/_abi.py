@@ -129,6 +129,8 @@ SIGNATURES = {
                                      C.c_size_t, C.c_void_p]),
     "tiles_conv2d_htiled": (C.c_int, [C.POINTER(ConvDesc), C.c_int, C.POINTER(Config),
                                       C.c_void_p, C.c_size_t, C.c_void_p]),
+    "tiles_gemm_noalloc": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_void_p,
+                                     C.c_int]),
     "tiles_check": (C.c_int, [C.c_void_p, C.c_void_p]),
     "tiles_selftest_wait_timeout": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
 }

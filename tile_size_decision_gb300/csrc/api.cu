@@ -257,6 +257,51 @@ __global__ void selftest_wait_kernel(int32_t* err, uint64_t limit_ns) {
 
 }  // namespace tiles
 
+// ---- GEMM without caller-allocated memory ----------------------------------
+//
+// Callers that cannot call cudaMalloc (code running where device allocation
+// is forbidden or unavailable: inside an allocator or driver callback, under
+// a runtime that owns all device memory, or in a real-time path that must
+// not allocate) cannot provide the workspace that tiles_gemm takes.  For
+// them tiles_gemm_noalloc uses this file-scope device array instead.  It is
+// exactly the kernels' workspace (the error word a bounded wait writes on
+// expiry), 256 bytes, and every GPU that loads the library holds it until the
+// process exits.  It starts at zero when the module loads; the error word is
+// cleared each time a waiting call reads it.
+static __device__ __align__(256) unsigned char tiles_noalloc_scratch[256];
+
+namespace tiles {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = sizeof(tiles_noalloc_scratch);
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// The device address of the scratch array on the current device.  In host
+// code the array's name is only a host-side stand-in, so the address is
+// asked of the runtime once per device (with that device current) and kept.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(TILES_ERR_INVALID_ARG, "device ordinal %d beyond %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, tiles_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(TILES_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return TILES_OK;
+}
+
+}  // namespace
+}  // namespace tiles
+
 using namespace tiles;
 
 extern "C" {
@@ -397,6 +442,28 @@ int tiles_selftest_wait_timeout(void* ws, int64_t limit_ns, void* stream) {
 int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
                         void* ws, size_t ws_bytes, void* stream) {
     return conv2d_htiled(desc, tile_oh, cfg, ws, ws_bytes, stream);
+}
+
+int tiles_gemm_noalloc(const tiles_gemm_desc* desc, const tiles_config* cfg, void* stream,
+                       int wait) {
+    if (tiles_workspace_bytes() > kNoAllocScratchBytes)
+        return fail(TILES_ERR_TOO_LARGE, "the GEMM needs %zu bytes of scratch; the static array "
+                    "holds %zu", tiles_workspace_bytes(), kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    int s = noalloc_scratch(&scratch);
+    if (s != TILES_OK) return s;
+    s = gemm_common(desc, cfg, scratch, kNoAllocScratchBytes, stream, true);
+    if (s != TILES_OK || !wait) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+    int32_t word = 0;
+    e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "read scratch: %s", cudaGetErrorString(e));
+    if (word == 0) return TILES_OK;
+    e = cudaMemset(scratch, 0, sizeof(word));
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "clear scratch: %s", cudaGetErrorString(e));
+    return fail(TILES_ERR_TIMEOUT, "a bounded device wait expired (error bits 0x%x)", word);
 }
 
 }  // extern "C"

@@ -36,7 +36,8 @@ from dataclasses import dataclass, field
 from . import planner as page
 
 # Compiled variants (bm, bn, cta_group, stages), in enumeration order.
-VARIANTS = ((128, 64, 1, 8), (128, 128, 1, 7), (128, 192, 1, 5), (128, 256, 1, 4))
+VARIANTS = ((128, 64, 1, 8), (128, 128, 1, 7), (128, 192, 1, 5), (128, 256, 1, 4),
+            (256, 128, 2, 8), (256, 256, 2, 7))
 
 THREADS = 192
 BARRIER_BYTES = 256
@@ -54,7 +55,7 @@ class GB300Device:
     sm_count: int = 148
     tmem_cols: int = 512
     mma_flops_per_clk: int = 8192
-    fill_bytes_per_clk: int = 96
+    fill_bytes_per_clk: int = 64
     kernel_regs_per_thread: int = 64
 
 

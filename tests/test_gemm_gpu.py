@@ -22,12 +22,14 @@ if not torch.cuda.is_available():
 import tile_size_decision_gb300 as T  # noqa: E402
 from tests.gpu_util import to_cuda, to_f64, empty_out  # noqa: E402
 
-VARIANT_BN = (64, 128, 192, 256)
-STAGES = {64: 8, 128: 7, 192: 5, 256: 4}
+# Compiled variants: (bn, cta_group) -> stages.
+VARIANTS = {(64, 1): 8, (128, 1): 7, (192, 1): 5, (256, 1): 4, (128, 2): 8, (256, 2): 7}
+VARIANT_IDS = [f"bn{bn}_cg{cg}" for bn, cg in VARIANTS]
 
 
-def variant(bn):
-    return T.make_config(128, bn, 64, STAGES[bn], 192, "tcgen05", 2, 1)
+def variant(v):
+    bn, cg = v
+    return T.make_config(128 * cg, bn, 64, VARIANTS[v], 192, "tcgen05", 2, cg)
 
 
 @pytest.fixture(scope="module")
@@ -53,38 +55,42 @@ def assert_close(got, a64, b64, out_dt):
     assert ok, f"worst ratio {worst} at {idx}: got {got[idx]} want {ref[idx]}"
 
 
-@pytest.mark.parametrize("bn", VARIANT_BN)
-def test_identity_exact(ws, bn):
+@pytest.mark.parametrize("v", list(VARIANTS), ids=VARIANT_IDS)
+def test_identity_exact(ws, v):
     # C = I x B must return B exactly: catches swizzle, descriptor and
     # row/column placement mistakes in every variant.
-    m, k, n = 128, 128, 2 * bn
+    bn, cg = v
+    m = k = 128 * cg
+    n = 2 * bn
     a = S.quantise(np.eye(m, k), S.F16)
     b = S.random_matrix(1, (k, n), S.F16)
-    c = run_gemm(a, b, S.F16, S.F32, variant(bn), ws)
+    c = run_gemm(a, b, S.F16, S.F32, variant(v), ws)
     assert np.array_equal(to_f64(c), S.widen(b, S.F16))
 
 
-@pytest.mark.parametrize("bn", VARIANT_BN)
-def test_permutation_exact(ws, bn):
+@pytest.mark.parametrize("v", list(VARIANTS), ids=VARIANT_IDS)
+def test_permutation_exact(ws, v):
+    bn, cg = v
     rng = np.random.default_rng(3)
-    m = k = 256
+    m = k = 512
     n = bn + 64
     perm = rng.permutation(m)
     a = S.quantise(np.eye(m)[perm], S.BF16)
     b = S.random_matrix(2, (k, n), S.BF16)
-    c = run_gemm(a, b, S.BF16, S.F32, variant(bn), ws)
+    c = run_gemm(a, b, S.BF16, S.F32, variant(v), ws)
     assert np.array_equal(to_f64(c), S.widen(b, S.BF16)[perm])
 
 
-@pytest.mark.parametrize("bn", VARIANT_BN)
+@pytest.mark.parametrize("v", list(VARIANTS), ids=VARIANT_IDS)
 @pytest.mark.parametrize("dt", [S.F16, S.BF16])
-def test_integer_inputs_exact(ws, bn, dt):
+def test_integer_inputs_exact(ws, v, dt):
     # Entries in [-2, 2] and K = 320: every partial sum is an integer below
     # 2^24, so the fp32 accumulation is exact whatever its order.
-    m, n, k = 200, 3 * bn - 16, 320
+    bn, cg = v
+    m, n, k = 200 * cg + 57, 3 * bn - 16, 320
     a = S.integer_matrix(5, (m, k), dt)
     b = S.integer_matrix(6, (k, n), dt)
-    c = run_gemm(a, b, dt, S.F32, variant(bn), ws)
+    c = run_gemm(a, b, dt, S.F32, variant(v), ws)
     assert np.array_equal(to_f64(c), OG.gemm(S.widen(a, dt), S.widen(b, dt)))
 
 
@@ -108,42 +114,46 @@ def test_small_shapes_planned(ws, shape, out_dt):
     assert_close(to_f64(c), S.widen(a, in_dt), S.widen(b, in_dt), out_dt)
 
 
-@pytest.mark.parametrize("bn", VARIANT_BN)
-def test_ragged_every_variant_with_canaries(ws, bn):
+@pytest.mark.parametrize("v", list(VARIANTS), ids=VARIANT_IDS)
+def test_ragged_every_variant_with_canaries(ws, v):
     # Output written into the interior of a larger buffer: rows past M and
     # columns past N (the canary band) must stay untouched.
-    m, n, k = 333, 2 * bn + 40, 200
+    bn, cg = v
+    m, n, k = 333 * cg, 2 * bn + 40, 200
     a = S.random_matrix(31, (m, k), S.F16, "normal")
     b = S.random_matrix(32, (k, n), S.F16, "normal")
     big = torch.full((m + 3, n + 24), 12345.0, dtype=torch.float32, device="cuda")
     c = big[:m, :n]
     T.gemm(to_cuda(a, S.F16, -(-k // 8) * 8), to_cuda(b, S.F16, -(-n // 8) * 8), out=c,
-           cfg=variant(bn), workspace=ws)
+           cfg=variant(v), workspace=ws)
     T.check(ws)
     host = to_f64(big)
     assert np.all(host[m:, :] == 12345.0) and np.all(host[:, n:] == 12345.0)
     assert_close(host[:m, :n], S.widen(a, S.F16), S.widen(b, S.F16), S.F32)
 
 
-def test_batched_small(ws):
-    bsz, m, n, k = 5, 130, 200, 96
+@pytest.mark.parametrize("v", [None] + list(VARIANTS), ids=["planned"] + VARIANT_IDS)
+def test_batched_small(ws, v):
+    bsz, m, n, k = 5, 300, 200, 96
     a = S.random_matrix(41, (bsz, m, k), S.BF16, "normal")
     b = S.random_matrix(42, (bsz, k, n), S.BF16, "normal")
     c = empty_out((bsz, m, n), S.BF16)
-    T.gemm_batched(to_cuda(a, S.BF16), to_cuda(b, S.BF16), out=c, workspace=ws)
+    T.gemm_batched(to_cuda(a, S.BF16), to_cuda(b, S.BF16), out=c,
+                   cfg=variant(v) if v else None, workspace=ws)
     T.check(ws)
     assert_close(to_f64(c), S.widen(a, S.BF16), S.widen(b, S.BF16), S.BF16)
 
 
-def test_batched_rows_do_not_leak_between_items(ws):
+@pytest.mark.parametrize("v", [(128, 1), (256, 2)], ids=["bn128_cg1", "bn256_cg2"])
+def test_batched_rows_do_not_leak_between_items(ws, v):
     # M not a multiple of the tile: a tile's rows past M must read zeros, not
     # the next batch item's rows.  Item t of A is all (t+1), B all ones.
-    bsz, m, n, k = 3, 70, 64, 64
+    bsz, m, n, k = 3, 70, 256, 64
     a = np.stack([np.full((m, k), t + 1.0) for t in range(bsz)])
     a = S.quantise(a, S.F16)
     b = S.quantise(np.ones((bsz, k, n)), S.F16)
     c = empty_out((bsz, m, n), S.F32)
-    T.gemm_batched(to_cuda(a, S.F16), to_cuda(b, S.F16), out=c, workspace=ws)
+    T.gemm_batched(to_cuda(a, S.F16), to_cuda(b, S.F16), out=c, cfg=variant(v), workspace=ws)
     T.check(ws)
     got = to_f64(c)
     for t in range(bsz):

@@ -3,7 +3,7 @@
     python -m tile_size_decision_gb300.build [-v] [--force]
 
 Each translation unit compiles in parallel into ``_build/``; the GEMM source
-compiles once per tile width.  Objects newer than every source and header
+compiles once per (tile width, CTAs per MMA).  Objects newer than every source and header
 are reused.  The shared library links the CUDA runtime statically and looks
 up the driver at run time, so it loads on machines without a GPU.
 """
@@ -28,7 +28,7 @@ LIB = os.path.join(HERE, "libtiles.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--expt-relaxed-constexpr"]
-GEMM_WIDTHS = (64, 128, 192, 256)
+GEMM_VARIANTS = ((64, 1), (128, 1), (192, 1), (256, 1), (128, 2), (256, 2))
 
 
 def nvcc() -> str:
@@ -45,8 +45,9 @@ def units():
         ("api.cu", "api.o", []),
         ("conv_sm103a.cu", "conv_sm103a.o", []),
     ]
-    for bn in GEMM_WIDTHS:
-        out.append(("gemm_sm103a.cu", f"gemm_bn{bn}.o", [f"-DTILES_GEMM_BN={bn}"]))
+    for bn, cg in GEMM_VARIANTS:
+        out.append(("gemm_sm103a.cu", f"gemm_bn{bn}_cg{cg}.o",
+                    [f"-DTILES_GEMM_BN={bn}", f"-DTILES_GEMM_CG={cg}"]))
     return out
 
 

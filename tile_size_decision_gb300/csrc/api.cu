@@ -142,15 +142,40 @@ int check_config(const tiles_device& dev, const tiles_config& cfg, int in_bytes)
     return TILES_OK;
 }
 
-int launch_by_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                 int grid, cudaStream_t st) {
-    switch (bn) {
-        case 64: return launch_gemm_variant<64>(ta, tb, args, grid, st);
-        case 128: return launch_gemm_variant<128>(ta, tb, args, grid, st);
-        case 192: return launch_gemm_variant<192>(ta, tb, args, grid, st);
-        case 256: return launch_gemm_variant<256>(ta, tb, args, grid, st);
-        default: return static_cast<int>(cudaErrorInvalidValue);
+// Persistent CTA groups that fit at once for a compiled variant (cached per
+// device and variant).
+int max_groups(int ordinal, int bn, int cg, int sm_count) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_tuple(ordinal, bn, cg);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int g = sm_count / cg;
+    if (cg == 2 && bn == 256) g = gemm_variant_max_groups<256, 2>(sm_count);
+    if (cg == 2 && bn == 128) g = gemm_variant_max_groups<128, 2>(sm_count);
+    cache[key] = g;
+    return g;
+}
+
+int launch_variant(int bn, int cg, const CUtensorMap& ta, const CUtensorMap& tb,
+                   const GemmArgs& args, int groups, cudaStream_t st) {
+    if (cg == 1) {
+        switch (bn) {
+            case 64: return launch_gemm_variant<64, 1>(ta, tb, args, groups, st);
+            case 128: return launch_gemm_variant<128, 1>(ta, tb, args, groups, st);
+            case 192: return launch_gemm_variant<192, 1>(ta, tb, args, groups, st);
+            case 256: return launch_gemm_variant<256, 1>(ta, tb, args, groups, st);
+            default: break;
+        }
+    } else if (cg == 2) {
+        switch (bn) {
+            case 128: return launch_gemm_variant<128, 2>(ta, tb, args, groups, st);
+            case 256: return launch_gemm_variant<256, 2>(ta, tb, args, groups, st);
+            default: break;
+        }
     }
+    return static_cast<int>(cudaErrorInvalidValue);
 }
 
 int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws, size_t ws_bytes,
@@ -199,6 +224,7 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
     const int64_t sa = batch > 1 ? d->stride_a : d->m * d->lda;
     const int64_t sb = batch > 1 ? d->stride_b : d->k * d->ldb;
     CUtensorMap ta, tb;
+    // Each CTA loads 128 rows of A and 64-column atoms of B per K block.
     s = encode_3d(&ta, d->a_dtype, d->a, d->k, d->m, batch, d->lda, sa, 64, 128);
     if (s != TILES_OK) return s;
     s = encode_3d(&tb, d->b_dtype, d->b, d->n, d->k, batch, d->ldb, sb, 64, 64);
@@ -217,11 +243,13 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
     args.ldc = d->ldc;
     args.stride_c = batch > 1 ? d->stride_c : 0;
     args.c_dtype = d->c_dtype;
-    args.idesc = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, 128, cfg.bn);
+    args.idesc = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, cfg.bm, cfg.bn);
     args.err = (ws && ws_bytes >= sizeof(int32_t)) ? static_cast<int32_t*>(ws) : nullptr;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int grid = (int)std::min<int64_t>(tiles, dev.sm_count);
-    int e = launch_by_bn(cfg.bn, ta, tb, args, grid, static_cast<cudaStream_t>(stream));
+    const int groups = (int)std::min<int64_t>(
+        tiles, max_groups(ordinal, cfg.bn, cfg.cta_group, dev.sm_count));
+    int e = launch_variant(cfg.bn, cfg.cta_group, ta, tb, args, groups,
+                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(TILES_ERR_CUDA, "GEMM launch failed: %s",
                     cudaGetErrorString(static_cast<cudaError_t>(e)));

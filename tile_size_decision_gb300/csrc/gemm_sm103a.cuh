@@ -7,21 +7,29 @@
 // output tile per block, A and B slices staged on chip and reused by the
 // whole tile) with its multi-stage pipeline ("Double Buffering /
 // Multi-Stage Pipelining") and 128-byte swizzle ("Bank Conflict 与
-// Swizzling"), rebuilt on Blackwell's TMA, mbarriers and tensor memory:
+// Swizzling"), rebuilt on Blackwell's TMA, mbarriers and tensor memory.
 //
-//   warp 0      TMA producer: per K block, one 128 x 64 box of A and BN/64
-//               boxes of 64 x 64 of B into the stage's swizzled tiles.
-//   warp 1      owns TMEM (2 accumulators of 128 lanes x BN fp32 columns);
-//               one lane issues 4 tcgen05.mma (K = 16 each) per stage and
-//               commits the stage back to the producer.
+// CG = 1: one CTA per 128 x BN output tile.
+// CG = 2: a CTA pair (cluster of 2) per 256 x BN tile.  Each CTA loads its
+//         own 128 rows of A and BN/2 columns of B; both CTAs' loads complete
+//         on the leader's (rank 0) full barrier; one thread of the leader
+//         issues tcgen05.mma.cta_group::2 (M = 256), whose commits multicast
+//         to both CTAs; each CTA's TMEM holds its 128 rows of the tile.
+//         Per SM this halves B's share of the L2 -> shared traffic.
+//
+// Roles in each CTA (192 threads):
+//   warp 0      TMA producer (one lane).
+//   warp 1      TMEM owner; in the leader one lane issues the MMAs: 4 per
+//               stage (K = 16 each), commits the stage back to the
+//               producers, and commits a finished tile to the epilogues.
 //   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, cast, store the
 //               rows they own (warp w reads TMEM lanes 32*(w%4)..+31).
 //
-// Tiles are scheduled persistently: CTA i takes tiles i, i+grid, ...; with
-// two accumulators the epilogue of one tile overlaps the next tile's
-// mainloop.  Every wait is bounded (see mbar_wait); on expiry the kernel
-// records the role in the workspace error word, drains its own
-// asynchronous work and returns.
+// Tiles are scheduled persistently: CTA group g takes tiles g, g+groups, ...
+// Two TMEM accumulators let one tile's epilogue overlap the next tile's
+// mainloop.  Every wait is bounded (mbar_wait); on expiry the kernel records
+// the role in the workspace error word, lets the other roles stop, waits
+// for its own asynchronous work and returns.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -62,19 +70,24 @@ struct PipeBarriers {
 };
 static_assert(sizeof(PipeBarriers) <= kSmemBarrierBytes, "barrier block too large");
 
-template <int BN_, int STAGES_>
+template <int BN_, int STAGES_, int CG_>
 struct GemmLayout {
-    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
-    static constexpr int A_BYTES = BM * BK * 2;       // 16 KB: 128 rows x 128 B
-    static constexpr int B_CHUNK = BK * 64 * 2;       // 8 KB: 64 K-rows x 64 columns
-    static constexpr int B_BYTES = B_CHUNK * (BN / 64);
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int CG = CG_;
+    static constexpr int BM = 128 * CG;                // output rows per tile
+    static constexpr int BN = BN_, BK = 64, STAGES = STAGES_;
+    static constexpr int B_COLS = BN / CG;            // B columns each CTA loads
+    static constexpr int A_BYTES = 128 * BK * 2;       // 16 KB: 128 rows x 128 B
+    static constexpr int B_CHUNK = BK * 64 * 2;        // 8 KB: 64 K-rows x 64 columns
+    static constexpr int B_BYTES = B_CHUNK * (B_COLS / 64);
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;          // per CTA
+    static constexpr int TX_BYTES = STAGE_BYTES * CG;              // on the leader's barrier
     static constexpr int OPERAND_BYTES = STAGES * STAGE_BYTES;
     static constexpr int SMEM_BYTES = OPERAND_BYTES + kSmemBarrierBytes + kSmemAlignSlack;
     static constexpr int ACC_COLS = 2 * BN;
     static constexpr int TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64
                                    : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
-    static_assert(BN % 64 == 0 && BN <= 256, "BN must be a multiple of 64 up to 256");
+    static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
+    static_assert(B_COLS % 64 == 0 && BN <= 256, "B columns per CTA must be whole 64-column atoms");
     static_assert(STAGES >= 2 && STAGES <= kMaxStages, "stage count");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per block");
 };
@@ -94,6 +107,14 @@ __device__ __forceinline__ TileCoord decode_tile(int t, int m_blocks, int n_bloc
 __device__ __forceinline__ void raise_error(int32_t* err, volatile int* abort, int bit) {
     *abort = 1;
     if (err) atomicOr(err, bit);
+}
+
+// After an abort, loads or commits this CTA issued may still be in flight:
+// hold the block for a fixed, short interval before it may exit.
+__device__ __forceinline__ void settle_after_abort() {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 100000ull) {
+    }
 }
 
 // Store 32 consecutive fp32 accumulators of one row, cast to the output type,
@@ -151,14 +172,16 @@ __device__ __forceinline__ void store_row_chunk(void* row, int64_t col0, int64_t
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-    using L = GemmLayout<BN, STAGES>;
+    using L = GemmLayout<BN, STAGES, CG>;
     extern __shared__ uint8_t smem_raw[];
     // Operand tiles start on a 1024-byte boundary: the 128-byte swizzle is a
     // function of address bits 4-9 and the descriptors assume base offset 0.
+    // The offset is the same in both CTAs of a pair (same kernel, same
+    // dynamic shared memory), as the pair MMA requires.
     const uint32_t raw = ptx::smem_addr(smem_raw);
     uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* smA = base;
@@ -167,6 +190,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int group = CG == 2 ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+    const int groups = CG == 2 ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -175,7 +202,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&bar->acc_full[a], 1);
-            ptx::mbar_init(&bar->acc_empty[a], 4);   // one arrive per epilogue warp
+            ptx::mbar_init(&bar->acc_empty[a], 4 * CG);   // every epilogue warp of the group
         }
         ptx::mbar_init(&bar->drain, 1);
         bar->abort = 0;
@@ -186,11 +213,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ptx::tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(&bar->tmem_base, L::TMEM_COLS);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc<CG>(&bar->tmem_base, L::TMEM_COLS);
+        ptx::tmem_relinquish<CG>();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
 
     const uint32_t tmem = bar->tmem_base;
@@ -202,37 +229,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // ---------------- TMA producer ----------------
             uint32_t stage = 0, phase = 0;
             int issued = 0;
-            for (int t = blockIdx.x; t < args.tiles; t += gridDim.x) {
+            bool aborted = false;
+            for (int t = group; t < args.tiles && !aborted; t += groups) {
                 const TileCoord tc = decode_tile(t, args.m_blocks, args.n_blocks);
+                const int row0 = tc.mi * L::BM + static_cast<int>(rank) * 128;
+                const int col0 = tc.ni * BN + static_cast<int>(rank) * L::B_COLS;
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(&bar->empty[stage], phase ^ 1u, abort, limit)) {
                         raise_error(args.err, abort, kErrProducer);
-                        goto producer_done;
+                        aborted = true;
+                        break;
                     }
-                    ptx::mbar_arrive_expect_tx(&bar->full[stage], L::STAGE_BYTES);
-                    ptx::tma_load_3d(smA + stage * L::A_BYTES, &tmA, &bar->full[stage],
-                                     kb * L::BK, tc.mi * L::BM, tc.b);
+                    if (leader) ptx::mbar_arrive_expect_tx(&bar->full[stage], L::TX_BYTES);
+                    uint8_t* a_dst = smA + stage * L::A_BYTES;
+                    uint8_t* b_dst = smB + stage * L::B_BYTES;
+                    if constexpr (CG == 1) {
+                        ptx::tma_load_3d(a_dst, &tmA, &bar->full[stage], kb * L::BK, row0, tc.b);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        ptx::tma_load_3d(smB + stage * L::B_BYTES + j * L::B_CHUNK, &tmB,
-                                         &bar->full[stage], tc.ni * BN + j * 64, kb * L::BK, tc.b);
+                        for (int j = 0; j < L::B_COLS / 64; ++j)
+                            ptx::tma_load_3d(b_dst + j * L::B_CHUNK, &tmB, &bar->full[stage],
+                                             col0 + j * 64, kb * L::BK, tc.b);
+                    } else {
+                        const uint32_t fb = ptx::map_to_cta(ptx::smem_addr(&bar->full[stage]), 0);
+                        ptx::tma_load_3d_pair(a_dst, &tmA, fb, kb * L::BK, row0, tc.b);
+#pragma unroll
+                        for (int j = 0; j < L::B_COLS / 64; ++j)
+                            ptx::tma_load_3d_pair(b_dst + j * L::B_CHUNK, &tmB, fb, col0 + j * 64,
+                                                  kb * L::BK, tc.b);
+                    }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-        producer_done:
-            // Loads still in flight land before the block may exit: wait on
-            // the full barrier of each of the last (up to STAGES) issues.
-            for (int i = 0; i < (issued < STAGES ? issued : STAGES); ++i) {
-                if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
-                ptx::mbar_wait(&bar->full[stage], phase, nullptr, limit);
+            if (aborted) {
+                settle_after_abort();
+            } else if (CG == 1) {
+                // Every load landed before its stage was consumed; waiting on
+                // the last (up to STAGES) full barriers is then immediate.
+                for (int i = 0; i < (issued < STAGES ? issued : STAGES); ++i) {
+                    if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+                    ptx::mbar_wait(&bar->full[stage], phase, nullptr, limit);
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (leader CTA) ----------------
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            for (int t = blockIdx.x; t < args.tiles; t += gridDim.x) {
+            for (int t = group; t < args.tiles; t += groups) {
                 if (!ptx::mbar_wait(&bar->acc_empty[acc], acc_phase ^ 1u, abort, limit)) {
                     raise_error(args.err, abort, kErrMma);
                     break;
@@ -257,18 +301,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         // B, MN-major: 16 K rows = two 8-row groups of
                         // 1024 B; 64-column atoms B_CHUNK apart.
                         const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 2048, L::B_CHUNK, 1024);
-                        ptx::mma_f16(d, ad, bd, args.idesc, (kb | kk) != 0);
+                        ptx::mma_f16<CG>(d, ad, bd, args.idesc, (kb | kk) != 0);
                     }
-                    ptx::mma_commit(&bar->empty[stage]);
+                    ptx::mma_commit<CG>(&bar->empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::mma_commit(&bar->acc_full[acc]);
+                ptx::mma_commit<CG>(&bar->acc_full[acc]);
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            // Every MMA issued here completes before the block tears down.
-            ptx::mma_commit(&bar->drain);
+            // Every MMA issued here completes before the group tears down.
+            ptx::mma_commit_local<CG>(&bar->drain);
             ptx::mbar_wait(&bar->drain, 0, nullptr, limit);
         }
     } else {
@@ -277,7 +321,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row_in_tile = quarter * 32 + lane;
         const int out_bytes = args.c_dtype == TILES_F32 ? 4 : 2;
         uint32_t acc = 0, acc_phase = 0;
-        for (int t = blockIdx.x; t < args.tiles; t += gridDim.x) {
+        for (int t = group; t < args.tiles; t += groups) {
             const TileCoord tc = decode_tile(t, args.m_blocks, args.n_blocks);
             bool ok = ptx::mbar_wait(&bar->acc_full[acc], acc_phase, abort, limit);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -285,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            const int64_t row = static_cast<int64_t>(tc.mi) * L::BM + row_in_tile;
+            const int64_t row = static_cast<int64_t>(tc.mi) * L::BM + rank * 128 + row_in_tile;
             const bool row_ok = row < args.m;
             char* crow = static_cast<char*>(args.c) +
                          (static_cast<int64_t>(tc.b) * args.stride_c + row * args.ldc) * out_bytes;
@@ -300,33 +344,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bar->acc_empty[acc]);
+            if (lane == 0) {
+                if constexpr (CG == 1)
+                    ptx::mbar_arrive(&bar->acc_empty[acc]);
+                else
+                    ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_addr(&bar->acc_empty[acc]), 0));
+            }
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, L::TMEM_COLS);
+        ptx::tmem_dealloc<CG>(tmem, L::TMEM_COLS);
     }
 }
 
-// Host-side launch of one compiled variant (defined per BN in
-// gemm_sm103a.cu).  Returns a cudaError_t value.
-template <int BN>
+// Host-side launch of one compiled variant (defined per (BN, CG) in
+// gemm_sm103a.cu).  `groups` is the number of persistent CTA groups.
+// Returns a cudaError_t value.
+template <int BN, int CG>
 int launch_gemm_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                        int grid, cudaStream_t stream);
+                        int groups, cudaStream_t stream);
 
-// Stages compiled for each BN (the planner's kGemmVariants agree).
-template <int BN> struct GemmStages;
-template <> struct GemmStages<64>  { static constexpr int value = 8; };
-template <> struct GemmStages<128> { static constexpr int value = 7; };
-template <> struct GemmStages<192> { static constexpr int value = 5; };
-template <> struct GemmStages<256> { static constexpr int value = 4; };
+// Persistent CTA groups that fit on the device at once for a variant.
+template <int BN, int CG>
+int gemm_variant_max_groups(int sm_count);
+
+// Stages compiled for each (BN, CG) (the planner's kGemmVariants agree).
+template <int BN, int CG> struct GemmStages;
+template <> struct GemmStages<64, 1>  { static constexpr int value = 8; };
+template <> struct GemmStages<128, 1> { static constexpr int value = 7; };
+template <> struct GemmStages<192, 1> { static constexpr int value = 5; };
+template <> struct GemmStages<256, 1> { static constexpr int value = 4; };
+template <> struct GemmStages<128, 2> { static constexpr int value = 8; };
+template <> struct GemmStages<256, 2> { static constexpr int value = 7; };
 
 __global__ void selftest_wait_kernel(int32_t* err, uint64_t limit_ns);
 

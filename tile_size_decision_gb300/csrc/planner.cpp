@@ -96,6 +96,7 @@ void evaluate_page(const tiles_device& dev, const tiles_config& cfg, int elem_by
 // input type; the stage count is the deepest pipeline that fits 227 KB.
 const KernelVariant kGemmVariants[] = {
     {128, 64, 1, 8}, {128, 128, 1, 7}, {128, 192, 1, 5}, {128, 256, 1, 4},
+    {256, 128, 2, 8}, {256, 256, 2, 7},
 };
 const int kNumGemmVariants = sizeof(kGemmVariants) / sizeof(kGemmVariants[0]);
 

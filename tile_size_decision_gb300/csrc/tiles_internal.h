@@ -22,8 +22,10 @@ constexpr int kSmemBarrierBytes = 256;
 constexpr int kSmemAlignSlack = 1024;
 constexpr int kMaxStages = 8;
 // Default L2 -> shared-memory fill rate per SM per clock used by the GB300
-// time model (bytes).  A model parameter, not a measured constant.
-constexpr int kDefaultFillBytesPerClk = 96;
+// time model (bytes).  A model parameter calibrated on the 128x256 one-CTA
+// kernel at 4096^3, whose TMA loads averaged 58 B/clk/SM over the launch
+// (ncu: 1.61 GB in 96.9 us at 1.877 GHz on 152 SMs).
+constexpr int kDefaultFillBytesPerClk = 64;
 
 // A compiled kernel variant: tile rows and columns, SMs per MMA, and the
 // pipeline depth it was built with.

@@ -1,0 +1,136 @@
+"""GPU parity of the H-tiled implicit-GEMM convolution against the oracle.
+
+The kernel consumes the H-tile rows (in_start, pt', real rows) that the
+library's htile_rows computes on the host, i.e. the tiling tutorial's
+"H/W 维切分的通用公式".  Cases: brute force on tiny shapes, integer inputs
+(exact in fp32), tile heights from 1 row to more than OH (results must be
+bit-identical: the K order per output never changes), more than one launch
+of H-tiles, c_out above and below one 128-row block, canary guards around
+the output, and the full convolution workload.
+"""
+
+import numpy as np
+import pytest
+
+import synth_inputs as S
+from oracle import conv as OC
+from oracle import tolerance as OT
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import tile_size_decision_gb300 as T  # noqa: E402
+from tests.gpu_util import to_cuda, to_f64, TORCH_DT  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def ws():
+    T.load()
+    return T.workspace()
+
+
+def run_conv(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, ws, guard=0):
+    x = to_cuda(x_np, in_dt)
+    w = to_cuda(w_np, in_dt)
+    n, c, h, wd = x_np.shape
+    co, _, kh, kw = w_np.shape
+    oh = OC.out_size(h, kh, stride[0], pad[0], pad[0], dil[0])
+    ow = OC.out_size(wd, kw, stride[1], pad[1], pad[1], dil[1])
+    total = n * co * oh * ow
+    flat = torch.full((total + 2 * guard,), 2048.0, dtype=TORCH_DT[out_dt], device="cuda")
+    y = flat[guard:guard + total].view(n, co, oh, ow)
+    T.conv2d_htiled(x, w, stride, pad, dil, tile_oh, out=y, workspace=ws)
+    T.check(ws)
+    host = to_f64(flat)
+    if guard:
+        assert np.all(host[:guard] == 2048.0) and np.all(host[guard + total:] == 2048.0)
+    return host[guard:guard + total].reshape(n, co, oh, ow)
+
+
+def check_against_oracle(got, x64, w64, stride, pad, dil, out_dt):
+    ref = OC.conv2d(x64, w64, stride, (pad[0], pad[0]), (pad[1], pad[1]), dil)
+    bound = OC.conv2d(np.abs(x64), np.abs(w64), stride, (pad[0], pad[0]), (pad[1], pad[1]), dil)
+    ok, worst, idx = OT.check(got, ref, bound, out_dt)
+    assert ok, f"worst ratio {worst} at {idx}: got {got[idx]} want {ref[idx]}"
+
+
+TINY = [
+    # (n, c, h, w, co, kh, kw, stride, pad, dil, tile_oh)
+    (1, 8, 9, 9, 4, 3, 3, (2, 2), (1, 1), (1, 1), 2),     # the tutorial's H=9 example rows
+    (2, 8, 7, 10, 16, 3, 3, (1, 1), (1, 1), (1, 1), 3),
+    (1, 16, 12, 12, 8, 1, 1, (1, 1), (0, 0), (1, 1), 5),
+    (1, 8, 11, 13, 5, 5, 3, (2, 1), (2, 1), (1, 2), 1),
+    (3, 24, 16, 16, 130, 3, 3, (2, 2), (1, 1), (2, 2), 4),
+    (1, 8, 20, 6, 8, 2, 2, (3, 3), (0, 1), (1, 1), 7),
+]
+
+
+@pytest.mark.parametrize("case", TINY, ids=lambda c: "_".join(str(v) for v in c[:7]))
+def test_tiny_against_loops(ws, case):
+    n, c, h, wd, co, kh, kw, st, pad, dil, tile = case
+    x = S.random_matrix(1, (n, c, h, wd), S.F16)
+    w = S.random_matrix(2, (co, c, kh, kw), S.F16)
+    got = run_conv(x, w, S.F16, S.F32, st, pad, dil, tile, ws, guard=64)
+    x64, w64 = S.widen(x, S.F16), S.widen(w, S.F16)
+    ref = OC.conv2d_loops(x64, w64, st, pad, dil) if n * co * c * h * wd < 200000 else None
+    if ref is not None:
+        bound = OC.conv2d_loops(np.abs(x64), np.abs(w64), st, pad, dil)
+        ok, worst, idx = OT.check(got, ref, bound, S.F32)
+        assert ok, f"worst ratio {worst} at {idx}"
+    check_against_oracle(got, x64, w64, st, pad, dil, S.F32)
+
+
+@pytest.mark.parametrize("dt", [S.F16, S.BF16])
+def test_integer_inputs_exact(ws, dt):
+    x = S.integer_matrix(3, (2, 16, 30, 28), dt)
+    w = S.integer_matrix(4, (40, 16, 3, 3), dt)
+    got = run_conv(x, w, dt, S.F32, (2, 2), (1, 1), (1, 1), 4, ws)
+    ref = OC.conv2d(S.widen(x, dt), S.widen(w, dt), (2, 2), (1, 1), (1, 1))
+    assert np.array_equal(got, ref)
+
+
+def test_tile_height_does_not_change_bits(ws):
+    x = S.random_matrix(5, (2, 16, 37, 33), S.BF16, "normal")
+    w = S.random_matrix(6, (64, 16, 3, 3), S.BF16, "normal")
+    outs = [run_conv(x, w, S.BF16, S.F32, (2, 1), (1, 1), (1, 1), t, ws) for t in (1, 2, 3, 7, 19, 40)]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    check_against_oracle(outs[0], S.widen(x, S.BF16), S.widen(w, S.BF16), (2, 1), (1, 1), (1, 1),
+                         S.F32)
+
+
+def test_more_h_tiles_than_one_launch(ws):
+    # 300 output rows at tile height 1: three launches of at most 128 H-tiles.
+    x = S.random_matrix(7, (1, 8, 300, 20), S.F16)
+    w = S.random_matrix(8, (12, 8, 3, 3), S.F16)
+    got = run_conv(x, w, S.F16, S.F16, (1, 1), (1, 1), (1, 1), 1, ws, guard=32)
+    check_against_oracle(got, S.widen(x, S.F16), S.widen(w, S.F16), (1, 1), (1, 1), (1, 1), S.F16)
+
+
+def test_many_output_channels_bf16_out(ws):
+    x = S.random_matrix(9, (2, 32, 20, 20), S.BF16, "normal")
+    w = S.random_matrix(10, (300, 32, 3, 3), S.BF16, "normal")
+    got = run_conv(x, w, S.BF16, S.BF16, (1, 1), (1, 1), (1, 1), 6, ws, guard=16)
+    check_against_oracle(got, S.widen(x, S.BF16), S.widen(w, S.BF16), (1, 1), (1, 1), (1, 1),
+                         S.BF16)
+
+
+def test_conv_workload_full(ws):
+    wl = S.WORKLOADS["conv_htiled"]
+    x, w = S.conv_inputs(wl)
+    got = run_conv(x, w, wl.in_dtype, wl.out_dtype, (wl.sh, wl.sw), (wl.ph, wl.pw),
+                   (wl.dh, wl.dw), wl.tile_oh, ws)
+    assert got.shape == (wl.n, wl.c_out, wl.oh, wl.ow)
+    check_against_oracle(got, S.widen(x, wl.in_dtype), S.widen(w, wl.in_dtype), (wl.sh, wl.sw),
+                         (wl.ph, wl.pw), (wl.dh, wl.dw), wl.out_dtype)
+
+
+def test_rejects_unaligned_weights(ws):
+    x = torch.zeros((1, 3, 8, 8), dtype=torch.float16, device="cuda")
+    w = torch.zeros((4, 3, 3, 3), dtype=torch.float16, device="cuda")   # K = 27
+    with pytest.raises(T.TilesError) as e:
+        T.conv2d_htiled(x, w, (1, 1), (1, 1), (1, 1), 4, workspace=ws)
+    assert e.value.status == -3

@@ -1,3 +1,54 @@
 // H-tiled implicit-GEMM convolution for sm_103a (declarations).
+//
+// An NCHW convolution with OIHW weights is, per image and per output H-tile
+// of rows [o0, o1), a GEMM with
+//     M = c_out,  N = (o1 - o0) * OW,  K = c * kh * kw,
+//     A = W viewed as [c_out][c*kh*kw]  (already the K-major operand),
+//     B = the tile's im2col matrix, gathered from the input slice
+//         [in_start, min(in_end, H)) with the sub-operator pads pt', pb'
+//         (tiling tutorial, "H/W 维切分的通用公式"),
+//     C = y[n][c_out][o0:o1][:], row pitch OH*OW.
 #pragma once
+
+#include <cstdint>
+
 #include "tiles_internal.h"
+
+namespace tiles {
+
+// Rows of one output H-tile as the kernel consumes them (computed on the
+// host by htile_rows).
+struct ConvHTile {
+    int32_t o0;         // first output row
+    int16_t rows;       // o1 - o0
+    int16_t pt;         // top pad of the sub-operator, pt'
+    int32_t in_start;   // first input row of the slice
+    int32_t real_rows;  // min(in_end, H) - in_start: rows of the slice inside the image
+};
+static_assert(sizeof(ConvHTile) == 16, "H-tile record");
+
+// H-tiles handled by one launch (the table travels in the kernel parameters).
+constexpr int kConvMaxHTiles = 128;
+// Threads of the convolution block: the GEMM's six warps plus four warps
+// that gather the im2col operand.
+constexpr int kConvThreads = 320;
+constexpr int kConvGatherThreads = 128;
+
+struct ConvArgs {
+    const void* x;
+    void* y;
+    int32_t n, c, h, w, c_out, kh, kw, sh, sw, pw, dh, dw;
+    int32_t oh, ow;
+    int32_t k;                  // c * kh * kw
+    int32_t n_htiles;           // H-tiles in this launch
+    int32_t m_blocks, n_blocks, k_blocks;
+    int32_t tiles;              // n * n_htiles * m_blocks * n_blocks
+    int32_t out_dtype;
+    uint32_t idesc;
+    int32_t vec_ok;             // 16-byte vector stores are aligned for every tile
+    int32_t* err;
+    uint64_t wait_limit_ns;
+    ConvHTile ht[kConvMaxHTiles];
+};
+
+}  // namespace tiles

@@ -118,12 +118,14 @@ __device__ __forceinline__ void settle_after_abort() {
 }
 
 // Store 32 consecutive fp32 accumulators of one row, cast to the output type,
-// clipped at column n.  `row` points at the row's first element.
+// clipped at column n.  `row` points at the row's first element.  With
+// vec, full chunks use 16-byte stores (the caller guarantees alignment).
 __device__ __forceinline__ void store_row_chunk(void* row, int64_t col0, int64_t n,
-                                                const uint32_t (&v)[32], int dtype) {
+                                                const uint32_t (&v)[32], int dtype,
+                                                bool vec = true) {
     if (dtype == TILES_F32) {
         float* p = static_cast<float*>(row) + col0;
-        if (col0 + 32 <= n) {
+        if (vec && col0 + 32 <= n) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
                 float4 q = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
@@ -142,7 +144,7 @@ __device__ __forceinline__ void store_row_chunk(void* row, int64_t col0, int64_t
             __half2 t = __floats2half2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
             h[i] = *reinterpret_cast<uint32_t*>(&t);
         }
-        if (col0 + 32 <= n) {
+        if (vec && col0 + 32 <= n) {
 #pragma unroll
             for (int i = 0; i < 16; i += 4)
                 *reinterpret_cast<uint4*>(p + 2 * i) = make_uint4(h[i], h[i + 1], h[i + 2], h[i + 3]);
@@ -160,7 +162,7 @@ __device__ __forceinline__ void store_row_chunk(void* row, int64_t col0, int64_t
                 __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
             h[i] = *reinterpret_cast<uint32_t*>(&t);
         }
-        if (col0 + 32 <= n) {
+        if (vec && col0 + 32 <= n) {
 #pragma unroll
             for (int i = 0; i < 16; i += 4)
                 *reinterpret_cast<uint4*>(p + 2 * i) = make_uint4(h[i], h[i + 1], h[i + 2], h[i + 3]);

@@ -25,10 +25,13 @@
  *     (stride_*) are in elements; row pitches must be multiples of 16 bytes
  *     and base pointers 16-byte aligned (TMA requirement), else
  *     TILES_ERR_MISALIGNED.  There is no fallback path.
- *   - Workspace: a caller-owned device buffer of tiles_workspace_bytes()
- *     bytes, zeroed once before first use.  Kernels record a bounded-wait
- *     timeout in it; tiles_check() reads and clears it.  A NULL workspace
- *     disables that report (the kernel still returns).
+ *   - Workspace: a caller-owned device buffer, zeroed once before first
+ *     use, of at least tiles_workspace_bytes() bytes.  Kernels record a
+ *     bounded-wait timeout in its first word; tiles_check() reads and clears
+ *     it.  A GEMM given tiles_gemm_workspace_bytes() bytes also uses it for
+ *     the partial tiles of a last round split along K.  A NULL workspace
+ *     disables the timeout report (the kernel still returns).  One
+ *     workspace serves one launch at a time.
  */
 #ifndef TILES_H
 #define TILES_H
@@ -101,7 +104,9 @@ typedef struct {
     int32_t mma_flops_per_clk;        /* dense f16/bf16 FLOP per clock per SM */
     int32_t fill_bytes_per_clk;       /* L2 -> shared bytes per clock per SM (time model) */
     int32_t kernel_regs_per_thread;   /* register budget of the GB300 kernels */
-    int32_t reserved[4];
+    int32_t cta_pairs;                /* GB300: CTA pairs (2-CTA clusters) resident at once;
+                                         0 = sm_count / 2 */
+    int32_t reserved[3];
 } tiles_device;
 
 /* One tile configuration (the page's Config record plus GB300 fields). */
@@ -133,12 +138,15 @@ typedef struct {
     uint32_t failures;           /* TILES_FAIL_* bits */
     int32_t c3_violations;       /* how many C3 conditions failed */
     uint32_t warnings;           /* TILES_WARN_* bits */
-    int32_t pad0;
+    int32_t tail_split;          /* GB300: K parts of each last-round tile (0: none) */
     int64_t grid;                /* C4: output tiles (times the batch) */
     int64_t waves;               /* C4 */
     double last_wave_fill;       /* C4, in [0, 1] */
     double c0_bytes;             /* C0, float64 as on the page */
-    int64_t est_clocks;          /* GB300 time model (0 in page mode) */
+    int64_t est_clocks;          /* GB300 time model (0 in page mode): rounds of
+                                    ceil(K/bk) K blocks of max(MMA clocks, fill
+                                    clocks); with tail_split the last round runs
+                                    ceil(ceil(K/bk) / tail_split) K blocks */
 } tiles_verdict;
 
 /* A planning request. */
@@ -184,6 +192,20 @@ typedef struct {
     const void* wt;                   /* device, [c_out][c][kh][kw] */
     void* y;                          /* device, [n][c_out][oh][ow] */
 } tiles_conv_desc;
+
+/* The launch geometry tiles_gemm would use for a descriptor. */
+typedef struct {
+    tiles_config cfg;            /* the configuration (planned or given) */
+    int64_t tiles;               /* output tiles, b * ceil(M/bm) * ceil(N/bn) */
+    int64_t resident_groups;     /* CTA groups (CTAs or CTA pairs) resident at once */
+    int64_t full_units;          /* units run as whole tiles */
+    int64_t units;               /* whole tiles plus the last round's split units */
+    int64_t groups;              /* persistent CTA groups launched */
+    int32_t tail_mode;           /* 0: last round as whole tiles; 1: as N-halves;
+                                    2: split along K into ksplit parts */
+    int32_t ksplit;              /* K parts per last-round tile (tail_mode 2) */
+    int64_t workspace_bytes;     /* workspace this schedule uses (>= 256) */
+} tiles_schedule;
 
 /* ---- status and diagnostics -------------------------------------------- */
 
@@ -255,6 +277,24 @@ size_t tiles_workspace_bytes(void);
  * ragged edges are handled (zero fill on loads, clipped stores). */
 int tiles_gemm(const tiles_gemm_desc* desc, const tiles_config* cfg, void* workspace,
                size_t ws_bytes, void* stream);
+
+/* The schedule a tiles_gemm_batched call with these arguments and a
+ * workspace of ws_bytes would launch: the planned (or given, checked)
+ * configuration and rounds of the resident CTA groups.  A last round that
+ * would fill at most half of them (constraint C4, last-wave fill) is split:
+ * along K into resident/rest parts (at most 8) when the workspace holds the
+ * fp32 partial tiles -- the leading parts hand their partials to the last
+ * part, which adds them in part order (deterministic) and stores C -- else
+ * into N-halves when a half is whole 64-column B atoms.  Validates like
+ * tiles_gemm_batched; launches nothing. */
+int tiles_gemm_schedule(const tiles_gemm_desc* desc, const tiles_config* cfg, size_t ws_bytes,
+                        tiles_schedule* out);
+
+/* Workspace bytes that let this GEMM split its last round along K (256 when
+ * it needs no split; 0 on invalid arguments, see tiles_last_error).  A
+ * smaller workspace is accepted by the GEMM calls and changes only the
+ * schedule.  A workspace serves one launch at a time. */
+size_t tiles_gemm_workspace_bytes(const tiles_gemm_desc* desc, const tiles_config* cfg);
 
 /* The batched form: desc->batch >= 1 equally shaped GEMMs with element
  * strides stride_a/b/c between items (each a multiple of 8 elements). */

@@ -19,12 +19,20 @@ Rules
        <= tmem_cols.
   occupancy  least of regs (kernel_regs_per_thread * threads), smem,
        threads, TMEM; binding order regs, smem, threads, tmem.
-  C4   grid = b * ceil(M/bm) * ceil(N/bn); resident = max(bps *
-       (sm_count // cg), 1); waves; fill as on the page.
+  C4   grid = b * ceil(M/bm) * ceil(N/bn); resident = max(bps * slots, 1)
+       with slots = sm_count for one CTA per tile and the co-resident CTA
+       pairs (cta_pairs, else sm_count // 2) for pairs; waves; fill as on the
+       page.
   C0   the page's expression with b, in_bytes, out_bytes.
-  time est_clocks = waves * ceil(K/bk) * max(mma, fill) with
+  time est_clocks = waves * ceil(K/bk) * unit with unit = max(mma, fill),
        mma = (bm/cg)*bn*bk*2 // mma_flops_per_clk and
-       fill = ceil(smem_per_stage / fill_bytes_per_clk).
+       fill = ceil(smem_per_stage / fill_bytes_per_clk).  When the last round
+       would leave groups idle its tiles split along K into tail_split = s
+       parts, s in 2..min(resident // rest, 8, K blocks) minimising
+       ceil(K/bk / s) * unit + (s-1) * reduce with reduce =
+       ceil((bm/cg)*bn*4 / fill_bytes_per_clk) (reading one partial back):
+       est_clocks = (grid // resident) * ceil(K/bk) * unit
+                    + ceil(ceil(K/bk) / s) * unit + (s-1) * reduce.
   rank (est_clocks, round(C0), -bps, smem_total), stable over the variant
        order.
 """
@@ -56,7 +64,8 @@ class GB300Device:
     tmem_cols: int = 512
     mma_flops_per_clk: int = 8192
     fill_bytes_per_clk: int = 64
-    kernel_regs_per_thread: int = 64
+    kernel_regs_per_thread: int = 112
+    cta_pairs: int = 0          # co-resident 2-CTA clusters; 0 = sm_count // 2
 
 
 @dataclass(frozen=True)
@@ -92,6 +101,7 @@ class GB300Verdict:
     warnings: list = field(default_factory=list)
     c0_bytes: float = 0.0
     est_clocks: int = 0
+    tail_split: int = 0
 
 
 def _tmem_alloc(cols: int) -> int:
@@ -142,11 +152,16 @@ def evaluate(cfg: GB300Config, dev: GB300Device, in_bytes: int = 2) -> GB300Verd
     return v
 
 
+def resident_groups(v: GB300Verdict, dev: GB300Device) -> int:
+    cg = max(v.cfg.cta_group, 1)
+    slots = dev.cta_pairs if (cg == 2 and dev.cta_pairs > 0) else dev.sm_count // cg
+    return max(v.blocks_per_sm * slots, 1)
+
+
 def finish_parallelism(v: GB300Verdict, dev: GB300Device, b: int, m: int, n: int) -> None:
     cfg = v.cfg
-    cg = max(cfg.cta_group, 1)
     v.grid = b * page.ceil_div(m, cfg.bm) * page.ceil_div(n, cfg.bn)
-    resident = max(v.blocks_per_sm * (dev.sm_count // cg), 1)
+    resident = resident_groups(v, dev)
     v.waves = page.ceil_div(v.grid, resident)
     rem = v.grid % resident
     v.last_wave_fill = rem / resident if rem else 1.0
@@ -157,12 +172,39 @@ def finish_parallelism(v: GB300Verdict, dev: GB300Device, b: int, m: int, n: int
         v.warnings.append(page.W_IDLE)
 
 
+MAX_TAIL_PARTS = 8
+
+
+def tail_parts(grid: int, resident: int, kblocks: int, unit: int, reduce: int) -> int:
+    """K parts of each tile of a last round: the count s in 2 .. min(resident
+    // rest, 8, K blocks) minimising ceil(K blocks / s) * unit + (s-1) *
+    reduce, if it beats no split; 0 for no split."""
+    rest = grid % resident
+    if rest == 0:
+        return 0
+    smax = min(resident // rest, MAX_TAIL_PARTS, kblocks)
+    best, best_t = 0, kblocks * unit
+    for s in range(2, smax + 1):
+        t = page.ceil_div(kblocks, s) * unit + (s - 1) * reduce
+        if t < best_t:
+            best, best_t = s, t
+    return best
+
+
 def est_clocks(v: GB300Verdict, dev: GB300Device, k: int) -> int:
     cfg = v.cfg
     cg = max(cfg.cta_group, 1)
+    kblocks = page.ceil_div(k, cfg.bk)
     mma = (cfg.bm // cg) * cfg.bn * cfg.bk * 2 // dev.mma_flops_per_clk
     fill = page.ceil_div(v.smem_per_stage, dev.fill_bytes_per_clk)
-    return v.waves * page.ceil_div(k, cfg.bk) * max(mma, fill)
+    unit = max(mma, fill)
+    reduce = page.ceil_div((cfg.bm // cg) * cfg.bn * 4, dev.fill_bytes_per_clk)
+    resident = resident_groups(v, dev)
+    v.tail_split = tail_parts(v.grid, resident, kblocks, unit, reduce)
+    if not v.tail_split:
+        return v.waves * kblocks * unit
+    return ((v.grid // resident) * kblocks * unit + page.ceil_div(kblocks, v.tail_split) * unit
+            + (v.tail_split - 1) * reduce)
 
 
 def plan(b: int, m: int, n: int, k: int, dev: GB300Device, in_bytes: int = 2,

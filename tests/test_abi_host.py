@@ -180,7 +180,7 @@ def gb300_fields_native(v):
             v.smem_total, v.tmem_cols_alloc, v.regs_per_thread, v.regs_per_block,
             v.blocks_by_regs, v.blocks_by_smem, v.blocks_by_threads, v.blocks_by_tmem,
             v.blocks_per_sm, v.binding, v.failures, v.c3_violations, v.grid, v.waves,
-            fhex(v.last_wave_fill), v.warnings, fhex(v.c0_bytes), v.est_clocks)
+            fhex(v.last_wave_fill), v.warnings, fhex(v.c0_bytes), v.est_clocks, v.tail_split)
 
 
 def gb300_fields_oracle(v):
@@ -195,7 +195,7 @@ def gb300_fields_oracle(v):
             v.smem_total, v.tmem_cols_alloc, v.regs_per_thread, v.regs_per_block,
             v.blocks_by_regs, v.blocks_by_smem, v.blocks_by_threads, v.blocks_by_tmem,
             v.blocks_per_sm, BIND[v.binding], fails, v.c3_violations, v.grid, v.waves,
-            fhex(v.last_wave_fill), warns, fhex(v.c0_bytes), v.est_clocks)
+            fhex(v.last_wave_fill), warns, fhex(v.c0_bytes), v.est_clocks, v.tail_split)
 
 
 GB300_PLANS = [
@@ -209,6 +209,18 @@ GB300_PLANS = [
 ]
 
 
+@pytest.mark.parametrize("pairs", [0, 72, 74, 76])
+def test_gb300_plan_with_measured_pairs(lib, pairs):
+    dev = T.device_preset("gb300")
+    dev.sm_count = 152
+    dev.cta_pairs = pairs
+    native, nf = T.plan(4096, 4096, 4096, in_dtype="f16", device=dev)
+    odev = OG.GB300Device(sm_count=152, fill_bytes_per_clk=dev.fill_bytes_per_clk,
+                          kernel_regs_per_thread=dev.kernel_regs_per_thread, cta_pairs=pairs)
+    ref = OG.plan(1, 4096, 4096, 4096, odev, 2, 2)
+    assert [gb300_fields_native(v) for v in native] == [gb300_fields_oracle(v) for v in ref]
+
+
 @pytest.mark.parametrize("case", GB300_PLANS, ids=lambda c: "_".join(map(str, c)))
 def test_gb300_plan_matches_oracle(lib, case):
     b, m, n, k, di, do, sm = case
@@ -216,7 +228,8 @@ def test_gb300_plan_matches_oracle(lib, case):
     dev.sm_count = sm
     native, nf = T.plan(m, n, k, b=b, in_dtype=di, out_dtype=do, mode="gb300", device=dev)
     odev = OG.GB300Device(sm_count=sm, fill_bytes_per_clk=dev.fill_bytes_per_clk,
-                          kernel_regs_per_thread=dev.kernel_regs_per_thread)
+                          kernel_regs_per_thread=dev.kernel_regs_per_thread,
+                          cta_pairs=dev.cta_pairs)
     ref = OG.plan(b, m, n, k, odev, 2, 4 if do == "f32" else 2)
     assert nf == len(ref) == len(OG.VARIANTS)
     assert [gb300_fields_native(v) for v in native] == [gb300_fields_oracle(v) for v in ref]
@@ -241,7 +254,7 @@ def test_gb300_evaluate_random_configs(lib):
         v = T.evaluate(dev, T.make_config(cfg.bm, cfg.bn, cfg.bk, cfg.stages, cfg.threads,
                                           "tcgen05", cfg.acc_bufs, cfg.cta_group), ib, 4)
         T.finish_parallelism(dev, v, m, n, b)
-        assert gb300_fields_native(v)[:-2] == gb300_fields_oracle(ref)[:-2], cfg
+        assert gb300_fields_native(v)[:-3] == gb300_fields_oracle(ref)[:-3], cfg
 
 
 def test_gb300_choice_at_the_bench_shape(lib):
@@ -251,6 +264,9 @@ def test_gb300_choice_at_the_bench_shape(lib):
     # a third less operand traffic per SM, and the least C0.
     assert (best.cfg.bm, best.cfg.bn, best.cfg.stages, best.cfg.cta_group) == (256, 256, 7, 2)
     assert best.grid == 256 and best.waves == 4
+    # 256 tiles on 74 pairs: 3 whole rounds and 34 tiles left, each split
+    # along K into 74 // 34 = 2 parts.
+    assert best.tail_split == 2
 
 
 # --------------------------------------------------------------------------- #

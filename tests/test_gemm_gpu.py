@@ -160,11 +160,14 @@ def test_batched_rows_do_not_leak_between_items(ws, v):
         assert np.all(got[t] == (t + 1) * k)
 
 
-def full_workload(name, ws):
+def full_workload(name, small_ws=None):
+    # The launch configuration bench.py times: the planned tile and a
+    # workspace sized for the K-split last round (unless small_ws is given).
     wl = S.WORKLOADS[name]
     a, b = S.gemm_inputs(wl)
     ta, tb = to_cuda(a, wl.in_dtype), to_cuda(b, wl.in_dtype)
     c = empty_out(wl.c_shape(), wl.out_dtype)
+    ws = small_ws if small_ws is not None else T.gemm_workspace(ta, tb, c)
     if wl.b > 1:
         T.gemm_batched(ta, tb, out=c, workspace=ws)
     else:
@@ -175,7 +178,15 @@ def full_workload(name, ws):
 
 @pytest.mark.parametrize("name", ["gemm_512", "gemm_4096", "gemm_batched", "gemm_ragged"])
 def test_workload_full_parity(ws, name):
-    wl, a, b, got = full_workload(name, ws)
+    wl, a, b, got = full_workload(name)
+    assert_close(got, S.widen(a, wl.in_dtype), S.widen(b, wl.in_dtype), wl.out_dtype)
+
+
+@pytest.mark.parametrize("name", ["gemm_4096", "gemm_ragged"])
+def test_workload_parity_without_workspace_room(ws, name):
+    # With only the 256-byte workspace the last round falls back to N-halves
+    # (or whole tiles); the result must be the same within tolerance.
+    wl, a, b, got = full_workload(name, small_ws=ws)
     assert_close(got, S.widen(a, wl.in_dtype), S.widen(b, wl.in_dtype), wl.out_dtype)
 
 
@@ -208,3 +219,69 @@ def test_rejects_unaligned_pitch(ws):
     with pytest.raises(T.TilesError) as e:
         T.gemm(a, b, out_dtype="f32", workspace=ws)
     assert e.value.status == -3
+
+
+def _groups(cg):
+    return torch.cuda.get_device_properties(0).multi_processor_count // cg
+
+
+@pytest.mark.parametrize("v", [(256, 2), (256, 1), (128, 1)], ids=["bn256_cg2", "bn256_cg1",
+                                                                   "bn128_cg1"])
+@pytest.mark.parametrize("rest", ["one", "half_round", "all_halves"])
+@pytest.mark.parametrize("room", ["small", "full"])
+def test_tail_rounds_split(ws, v, rest, room):
+    # Tile counts around the resident group count, so the last round is
+    # split: along K when the workspace holds the partial tiles (room
+    # "full"), else into N-halves (room "small"): one extra tile, half a
+    # round extra, or a problem smaller than one round; N and M are ragged.
+    bn, cg = v
+    g = _groups(cg)
+    tiles = {"one": g + 1, "half_round": g + g // 2, "all_halves": 5}[rest]
+    m, n, k = 128 * cg * tiles - 37, bn - 40, 1000
+    a_np = S.random_matrix(51, (m, k), S.F16, "normal")
+    b_np = S.random_matrix(52, (k, n), S.F16, "normal")
+    a = to_cuda(a_np, S.F16, -(-k // 8) * 8)
+    b = to_cuda(b_np, S.F16, -(-n // 8) * 8)
+    c = empty_out((m, n), S.F32, -(-n // 4) * 4)
+    w = T.gemm_workspace(a, b, c, variant(v)) if room == "full" else ws
+    sch = T.gemm_schedule(a, b, c, variant(v), w)
+    if room == "full":
+        assert sch.tail_mode == 2 and sch.ksplit >= 2
+        assert sch.units == sch.full_units + (sch.tiles - sch.full_units) * sch.ksplit
+    for _ in range(3):          # reuse of the workspace across launches
+        c.fill_(float("nan"))
+        T.gemm(a, b, out=c, cfg=variant(v), workspace=w)
+        T.check(w)
+        assert_close(to_f64(c), S.widen(a_np, S.F16), S.widen(b_np, S.F16), S.F32)
+
+
+def test_ksplit_tail_is_deterministic(ws):
+    wl = S.WORKLOADS["gemm_ragged"]
+    a, b = S.gemm_inputs(wl)
+    ta, tb = to_cuda(a, wl.in_dtype), to_cuda(b, wl.in_dtype)
+    c1 = empty_out(wl.c_shape(), wl.out_dtype)
+    w = T.gemm_workspace(ta, tb, c1)
+    assert T.gemm_schedule(ta, tb, c1, workspace=w).tail_mode == 2
+    T.gemm(ta, tb, out=c1, workspace=w)
+    c2 = T.gemm(ta, tb, out_dtype="f32", workspace=w)
+    T.check(w)
+    assert torch.equal(c1, c2)
+
+
+def test_schedule_of_the_bench_shape():
+    # The 4096^3 fp16 GEMM plans the CTA-pair 256x256 tile; its 256 tiles run
+    # in rounds of the co-resident pairs the device reports, and a last round
+    # filling at most half of them runs as N-half tiles.
+    a = torch.zeros((4096, 4096), dtype=torch.float16, device="cuda")
+    c = torch.empty((4096, 4096), dtype=torch.float16, device="cuda")
+    sch = T.gemm_schedule(a, a, c)
+    dev = T.device_query(0)
+    assert (sch.cfg.bm, sch.cfg.bn, sch.cfg.cta_group) == (256, 256, 2)
+    assert sch.tiles == 256
+    assert sch.resident_groups == dev.cta_pairs > 0
+    rem = sch.tiles % sch.resident_groups
+    if 0 < rem and 2 * rem <= sch.resident_groups:
+        assert sch.full_units == sch.tiles - rem and sch.units == sch.full_units + 2 * rem
+    else:
+        assert sch.full_units == sch.units == sch.tiles
+    assert sch.groups == min(sch.units, sch.resident_groups)

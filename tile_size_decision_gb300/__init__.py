@@ -17,7 +17,7 @@ from ._abi import TilesError, check as _check
 __all__ = [
     "TilesError", "load", "version", "device_preset", "device_query", "evaluate",
     "finish_parallelism", "c0_bytes", "plan", "htile_rows", "workspace_bytes", "workspace",
-    "gemm", "gemm_batched", "gemm_noalloc", "conv2d_htiled", "check", "selftest_wait_timeout", "make_config",
+    "gemm", "gemm_batched", "gemm_schedule", "gemm_workspace", "gemm_noalloc", "conv2d_htiled", "check", "selftest_wait_timeout", "make_config",
 ]
 
 
@@ -231,6 +231,33 @@ def conv2d_htiled(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), tile_oh=16, out=N
     _check(load().tiles_conv2d_htiled(C.byref(d), tile_oh, _cfg_ptr(cfg), ws, wsb,
                                       _stream_handle(stream)), "tiles_conv2d_htiled")
     return out
+
+
+def _batched3(a, b, out):
+    if a.dim() == 2:
+        return a.unsqueeze(0), b.unsqueeze(0), out.unsqueeze(0)
+    return a, b, out
+
+
+def gemm_schedule(a, b, out, cfg=None, workspace=None):
+    """The launch geometry a GEMM call with this workspace would use (2-D
+    tensors count as a batch of one)."""
+    d = _gemm_desc(*_batched3(a, b, out), batched=True)
+    sch = _abi.Schedule()
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().tiles_gemm_schedule(C.byref(d), _cfg_ptr(cfg), wsb, C.byref(sch)),
+           "tiles_gemm_schedule")
+    return sch
+
+
+def gemm_workspace(a, b, out, cfg=None):
+    """A zeroed workspace large enough for this GEMM's K-split last round."""
+    torch = _torch()
+    d = _gemm_desc(*_batched3(a, b, out), batched=True)
+    n = int(load().tiles_gemm_workspace_bytes(C.byref(d), _cfg_ptr(cfg)))
+    if n == 0:
+        raise TilesError(load().tiles_status_string(-1) and -1, "tiles_gemm_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=a.device)
 
 
 def gemm_noalloc(a, b, out=None, out_dtype=None, cfg=None, stream=None, wait=False):

@@ -45,7 +45,8 @@ class Device(C.Structure):
         "smem_per_sm", "smem_per_block_max", "regs_per_sm", "max_threads_per_sm",
         "max_threads_per_block", "max_blocks_per_sm", "regs_per_thread_max",
         "reg_granularity_per_warp", "warp_size", "sm_count", "tmem_cols", "mma_flops_per_clk",
-        "fill_bytes_per_clk", "kernel_regs_per_thread")] + [("reserved", C.c_int32 * 4)]
+        "fill_bytes_per_clk", "kernel_regs_per_thread", "cta_pairs")] + \
+        [("reserved", C.c_int32 * 3)]
 
 
 class Config(C.Structure):
@@ -72,7 +73,7 @@ class Verdict(C.Structure):
         ("failures", C.c_uint32),
         ("c3_violations", C.c_int32),
         ("warnings", C.c_uint32),
-        ("pad0", C.c_int32),
+        ("tail_split", C.c_int32),
         ("grid", C.c_int64),
         ("waves", C.c_int64),
         ("last_wave_fill", C.c_double),
@@ -98,6 +99,12 @@ class GemmDesc(C.Structure):
                 ("stride_a", C.c_int64), ("stride_b", C.c_int64), ("stride_c", C.c_int64),
                 ("a_dtype", C.c_int32), ("b_dtype", C.c_int32), ("c_dtype", C.c_int32),
                 ("pad0", C.c_int32)]
+
+
+class Schedule(C.Structure):
+    _fields_ = [("cfg", Config), ("tiles", C.c_int64), ("resident_groups", C.c_int64),
+                ("full_units", C.c_int64), ("units", C.c_int64), ("groups", C.c_int64),
+                ("tail_mode", C.c_int32), ("ksplit", C.c_int32), ("workspace_bytes", C.c_int64)]
 
 
 class ConvDesc(C.Structure):
@@ -127,6 +134,9 @@ SIGNATURES = {
                              C.c_void_p]),
     "tiles_gemm_batched": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_void_p,
                                      C.c_size_t, C.c_void_p]),
+    "tiles_gemm_schedule": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_size_t,
+                                      C.POINTER(Schedule)]),
+    "tiles_gemm_workspace_bytes": (C.c_size_t, [C.POINTER(GemmDesc), C.POINTER(Config)]),
     "tiles_conv2d_htiled": (C.c_int, [C.POINTER(ConvDesc), C.c_int, C.POINTER(Config),
                                       C.c_void_p, C.c_size_t, C.c_void_p]),
     "tiles_gemm_noalloc": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_void_p,

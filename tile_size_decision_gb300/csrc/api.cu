@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -178,8 +179,33 @@ int launch_variant(int bn, int cg, const CUtensorMap& ta, const CUtensorMap& tb,
     return static_cast<int>(cudaErrorInvalidValue);
 }
 
-int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws, size_t ws_bytes,
-                void* stream, bool batched) {
+// Everything a GEMM launch decides before touching the GPU's queues:
+// validated arguments, the configuration and the wave-aware schedule.
+struct GemmPlan {
+    tiles_device dev;
+    int ordinal;
+    tiles_config cfg;
+    int64_t tiles, resident, full_units, units, groups;
+    int tail_mode, ksplit;
+    int64_t flags_offset, partials_offset, ws_needed;   // bytes, K-split layout
+};
+
+constexpr size_t kHeaderBytes = 256;
+
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+// Workspace layout of a K-split tail: the 256-byte header (error word),
+// the readiness flags, then the fp32 partial tiles.
+void ksplit_layout(GemmPlan* gp, int64_t rest) {
+    const int64_t flags = rest * gp->cfg.cta_group * (gp->ksplit - 1) * 4;
+    gp->flags_offset = kHeaderBytes;
+    gp->partials_offset = align256(gp->flags_offset + flags * 4);
+    gp->ws_needed = gp->partials_offset +
+                    rest * (gp->ksplit - 1) * (int64_t)gp->cfg.bm * gp->cfg.bn * 4;
+}
+
+int gemm_prepare(const tiles_gemm_desc* d, const tiles_config* user_cfg, bool batched,
+                 size_t ws_bytes, GemmPlan* gp) {
     if (!d) return fail(TILES_ERR_INVALID_ARG, "null descriptor");
     if (!d->a || !d->b || !d->c) return fail(TILES_ERR_INVALID_ARG, "null matrix pointer");
     if (d->m < 1 || d->n < 1 || d->k < 1 || d->batch < 1)
@@ -207,19 +233,75 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
             d->stride_c < d->m * d->ldc)
             return fail(TILES_ERR_INVALID_ARG, "batch strides overlap the items");
     }
-    tiles_device dev;
-    int ordinal = 0;
-    int s = current_device(&dev, &ordinal);
+    int s = current_device(&gp->dev, &gp->ordinal);
     if (s != TILES_OK) return s;
-    tiles_config cfg;
     if (user_cfg) {
-        cfg = *user_cfg;
-        s = check_config(dev, cfg, 2);
+        gp->cfg = *user_cfg;
+        s = check_config(gp->dev, gp->cfg, 2);
         if (s != TILES_OK) return s;
     } else {
-        s = planned_config(dev, ordinal, d->batch, d->m, d->n, d->k, d->a_dtype, d->c_dtype, &cfg);
+        s = planned_config(gp->dev, gp->ordinal, d->batch, d->m, d->n, d->k, d->a_dtype,
+                           d->c_dtype, &gp->cfg);
         if (s != TILES_OK) return s;
     }
+    const tiles_config& cfg = gp->cfg;
+    gp->tiles = d->batch * ((d->m + cfg.bm - 1) / cfg.bm) * ((d->n + cfg.bn - 1) / cfg.bn);
+    if (gp->tiles > INT32_MAX / 2) return fail(TILES_ERR_TOO_LARGE, "too many output tiles");
+    // Wave-aware schedule (C4): rounds of the resident groups.  A last round
+    // that would fill at most half of them is split: along K into
+    // ksplit = resident / rest parts when the workspace holds the partial
+    // tiles, else into N-halves when those are whole B atoms.
+    gp->resident = max_groups(gp->ordinal, cfg.bn, cfg.cta_group, gp->dev.sm_count);
+    gp->full_units = gp->units = gp->tiles;
+    gp->tail_mode = kTailNone;
+    gp->ksplit = 1;
+    gp->flags_offset = gp->partials_offset = 0;
+    gp->ws_needed = kHeaderBytes;
+    const int64_t k_blocks = (d->k + cfg.bk - 1) / cfg.bk;
+    const int64_t rest = gp->tiles % gp->resident;
+    const int64_t full = gp->tiles - rest;
+    int64_t stage_bytes = 0;
+    gb300_smem_bytes(cfg, 2, &stage_bytes);
+    const int64_t parts = gb300_tail_parts(gp->tiles, gp->resident, k_blocks,
+                                           gb300_unit_clocks(gp->dev, cfg, stage_bytes),
+                                           gb300_reduce_clocks(gp->dev, cfg));
+    if (parts >= 2) {
+        GemmPlan k = *gp;
+        k.ksplit = (int)parts;
+        ksplit_layout(&k, rest);
+        if (static_cast<uint64_t>(ws_bytes) >= static_cast<uint64_t>(k.ws_needed)) {
+            *gp = k;
+            gp->tail_mode = kTailKSplit;
+            gp->full_units = full;
+            gp->units = full + rest * parts;
+        }
+    }
+    if (gp->tail_mode == kTailNone &&
+        tail_split_applies(cfg.bn, cfg.cta_group, gp->tiles, gp->resident)) {
+        gp->tail_mode = kTailNHalf;
+        gp->full_units = full;
+        gp->units = full + 2 * rest;
+    }
+    gp->groups = std::min<int64_t>(gp->units, gp->resident);
+    return TILES_OK;
+}
+
+// Bytes of workspace a K-split tail of this GEMM would use (the header alone
+// when its last round needs no split).
+int64_t gemm_ws_bytes(const tiles_gemm_desc* d, const tiles_config* user_cfg, int* status) {
+    GemmPlan gp;
+    *status = gemm_prepare(d, user_cfg, true, SIZE_MAX, &gp);
+    return *status == TILES_OK ? gp.ws_needed : 0;
+}
+
+std::atomic<uint32_t> g_epoch{0};
+
+int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws, size_t ws_bytes,
+                void* stream, bool batched) {
+    GemmPlan gp;
+    int s = gemm_prepare(d, user_cfg, batched, ws ? ws_bytes : 0, &gp);
+    if (s != TILES_OK) return s;
+    const tiles_config& cfg = gp.cfg;
     const int64_t batch = d->batch;
     const int64_t sa = batch > 1 ? d->stride_a : d->m * d->lda;
     const int64_t sb = batch > 1 ? d->stride_b : d->k * d->ldb;
@@ -236,19 +318,28 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
     args.m_blocks = (int32_t)((d->m + cfg.bm - 1) / cfg.bm);
     args.n_blocks = (int32_t)((d->n + cfg.bn - 1) / cfg.bn);
     args.k_blocks = (int32_t)((d->k + cfg.bk - 1) / cfg.bk);
-    const int64_t tiles = batch * args.m_blocks * args.n_blocks;
-    if (tiles > INT32_MAX) return fail(TILES_ERR_TOO_LARGE, "too many output tiles");
-    args.tiles = (int32_t)tiles;
+    args.tiles = (int32_t)gp.tiles;
+    args.full_units = (int32_t)gp.full_units;
+    args.units = (int32_t)gp.units;
+    args.tail_mode = gp.tail_mode;
+    args.ksplit = gp.ksplit;
+    if (gp.tail_mode == kTailKSplit) {
+        char* base = static_cast<char*>(ws);
+        args.flags = reinterpret_cast<uint32_t*>(base + gp.flags_offset);
+        args.partials = reinterpret_cast<float*>(base + gp.partials_offset);
+        uint32_t e = g_epoch.fetch_add(1) + 1;
+        if (e == 0) e = g_epoch.fetch_add(1) + 1;      // 0 marks "never written"
+        args.epoch = e;
+    }
     args.c = d->c;
     args.ldc = d->ldc;
     args.stride_c = batch > 1 ? d->stride_c : 0;
     args.c_dtype = d->c_dtype;
     args.idesc = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, cfg.bm, cfg.bn);
+    args.idesc_half = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, cfg.bm, cfg.bn / 2);
     args.err = (ws && ws_bytes >= sizeof(int32_t)) ? static_cast<int32_t*>(ws) : nullptr;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    const int groups = (int)std::min<int64_t>(
-        tiles, max_groups(ordinal, cfg.bn, cfg.cta_group, dev.sm_count));
-    int e = launch_variant(cfg.bn, cfg.cta_group, ta, tb, args, groups,
+    int e = launch_variant(cfg.bn, cfg.cta_group, ta, tb, args, (int)gp.groups,
                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(TILES_ERR_CUDA, "GEMM launch failed: %s",
@@ -383,6 +474,11 @@ int tiles_device_query(int ordinal, tiles_device* out) {
     int major = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, ordinal);
     d.tmem_cols = major == 10 ? 512 : 0;
+    if (major == 10) {
+        int current = 0;
+        cudaGetDevice(&current);
+        if (current == ordinal) d.cta_pairs = max_groups(ordinal, 256, 2, d.sm_count);
+    }
     *out = d;
     return TILES_OK;
 }
@@ -442,6 +538,30 @@ int tiles_gemm(const tiles_gemm_desc* desc, const tiles_config* cfg, void* ws, s
 int tiles_gemm_batched(const tiles_gemm_desc* desc, const tiles_config* cfg, void* ws,
                        size_t ws_bytes, void* stream) {
     return gemm_common(desc, cfg, ws, ws_bytes, stream, true);
+}
+
+size_t tiles_gemm_workspace_bytes(const tiles_gemm_desc* desc, const tiles_config* cfg) {
+    int status = TILES_OK;
+    const int64_t n = gemm_ws_bytes(desc, cfg, &status);
+    return status == TILES_OK ? (size_t)n : 0;
+}
+
+int tiles_gemm_schedule(const tiles_gemm_desc* desc, const tiles_config* cfg, size_t ws_bytes,
+                        tiles_schedule* out) {
+    if (!out) return fail(TILES_ERR_INVALID_ARG, "null output");
+    GemmPlan gp;
+    int s = gemm_prepare(desc, cfg, true, ws_bytes, &gp);
+    if (s != TILES_OK) return s;
+    out->tail_mode = gp.tail_mode;
+    out->ksplit = gp.ksplit;
+    out->workspace_bytes = gp.ws_needed;
+    out->cfg = gp.cfg;
+    out->tiles = gp.tiles;
+    out->resident_groups = gp.resident;
+    out->full_units = gp.full_units;
+    out->units = gp.units;
+    out->groups = gp.groups;
+    return TILES_OK;
 }
 
 int tiles_check(void* ws, void* stream) {

@@ -25,9 +25,12 @@
 //   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, cast, store the
 //               rows they own (warp w reads TMEM lanes 32*(w%4)..+31).
 //
-// Tiles are scheduled persistently: CTA group g takes tiles g, g+groups, ...
-// Two TMEM accumulators let one tile's epilogue overlap the next tile's
-// mainloop.  Every wait is bounded (mbar_wait); on expiry the kernel records
+// Work is scheduled persistently: CTA group g takes units g, g+groups, ...
+// The units are the output tiles, except that when the last round would
+// leave more than half the groups idle, its tiles are split into two
+// N-halves each (the planner's C4 last-wave fill), which all run in that
+// round.  Two TMEM accumulators let one unit's epilogue overlap the next
+// unit's mainloop.  Every wait is bounded (mbar_wait); on expiry the kernel records
 // the role in the workspace error word, lets the other roles stop, waits
 // for its own asynchronous work and returns.
 #pragma once
@@ -51,10 +54,24 @@ struct GemmArgs {
     int32_t m, n, k, batch;
     int32_t m_blocks, n_blocks, k_blocks;
     int32_t tiles;             // batch * m_blocks * n_blocks
+    // Work units: units [0, full_units) are whole tiles.  The tiles after
+    // them (the last, partly filled round) run by tail_mode:
+    //   kTailNone   as whole tiles (units = tiles);
+    //   kTailNHalf  as two N-halves each (units = full + 2 * rest);
+    //   kTailKSplit as ksplit parts along K each (units = full + ksplit *
+    //               rest): parts 0..ksplit-2 write fp32 partial tiles to
+    //               `partials` and raise their flags; the last part adds them
+    //               to its own accumulator in part order and stores C.
+    int32_t full_units, units;
+    int32_t tail_mode, ksplit;
+    float* partials;           // kTailKSplit: [rest * (ksplit-1)][BN][BM] fp32
+    uint32_t* flags;           // kTailKSplit: one per (tail tile, CTA, part, warp)
+    uint32_t epoch;            // kTailKSplit: the flag value that means "ready"
     void* c;
     int64_t ldc, stride_c;     // elements
     int32_t c_dtype;           // tiles_dtype
-    uint32_t idesc;            // tcgen05 instruction descriptor
+    uint32_t idesc;            // tcgen05 instruction descriptor, N = BN
+    uint32_t idesc_half;       // the same with N = BN / 2
     int32_t* err;              // workspace error word, may be null
     uint64_t wait_limit_ns;
 };
@@ -90,6 +107,9 @@ struct GemmLayout {
     static_assert(B_COLS % 64 == 0 && BN <= 256, "B columns per CTA must be whole 64-column atoms");
     static_assert(STAGES >= 2 && STAGES <= kMaxStages, "stage count");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per block");
+    // The last K part of a split tile stages one partial per epilogue warp
+    // (32 rows x BN fp32) in the idle operand stages.
+    static_assert(4 * 32 * BN * 4 <= OPERAND_BYTES, "partial staging must fit the stages");
 };
 
 struct TileCoord { int b, mi, ni; };
@@ -102,6 +122,70 @@ __device__ __forceinline__ TileCoord decode_tile(int t, int m_blocks, int n_bloc
     c.mi = r % m_blocks;        // M fastest: concurrent CTAs share B panels
     c.ni = r / m_blocks;
     return c;
+}
+
+constexpr int kTailNone = 0;
+constexpr int kTailNHalf = 1;
+constexpr int kTailKSplit = 2;
+
+// One work unit: a whole tile, one N-half of a last-round tile, or one K
+// part of a last-round tile.
+struct UnitCoord {
+    int b, mi;
+    int n0;        // first output column
+    int width;     // columns: BN or BN / 2
+    int kb0, kb1;  // K blocks [kb0, kb1)
+    int part;      // K part (-1 unless split along K)
+    int tail;      // index of the tile among the last round's tiles
+};
+
+template <int BN>
+__device__ __forceinline__ UnitCoord decode_unit(int u, const GemmArgs& a) {
+    int t = u, off = 0, width = BN, kb0 = 0, kb1 = a.k_blocks, part = -1, tail = -1;
+    if (u >= a.full_units) {
+        const int h = u - a.full_units;
+        if (a.tail_mode == kTailNHalf) {
+            t = a.full_units + (h >> 1);
+            off = (h & 1) * (BN / 2);
+            width = BN / 2;
+        } else if (a.tail_mode == kTailKSplit) {
+            tail = h / a.ksplit;
+            part = h - tail * a.ksplit;
+            t = a.full_units + tail;
+            kb0 = part * a.k_blocks / a.ksplit;
+            kb1 = (part + 1) * a.k_blocks / a.ksplit;
+        }
+    }
+    const TileCoord tc = decode_tile(t, a.m_blocks, a.n_blocks);
+    return UnitCoord{tc.b, tc.mi, tc.ni * BN + off, width, kb0, kb1, part, tail};
+}
+
+__device__ __forceinline__ void store_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t load_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (bounded) until *flag == epoch; every lane polls with acquire
+// semantics, and the warp agrees on the outcome.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
+                                          const volatile int* abort, uint64_t limit_ns) {
+    bool ok = load_acquire_gpu(flag) == epoch;
+    if (!__all_sync(0xffffffffu, ok)) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        for (;;) {
+            ok = load_acquire_gpu(flag) == epoch;
+            if (__all_sync(0xffffffffu, ok)) break;
+            if (__any_sync(0xffffffffu, *abort != 0 || ptx::globaltimer_ns() - t0 > limit_ns))
+                return false;
+            __nanosleep(256);
+        }
+    }
+    return true;
 }
 
 __device__ __forceinline__ void raise_error(int32_t* err, volatile int* abort, int bit) {
@@ -232,32 +316,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool aborted = false;
-            for (int t = group; t < args.tiles && !aborted; t += groups) {
-                const TileCoord tc = decode_tile(t, args.m_blocks, args.n_blocks);
-                const int row0 = tc.mi * L::BM + static_cast<int>(rank) * 128;
-                const int col0 = tc.ni * BN + static_cast<int>(rank) * L::B_COLS;
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+            for (int u = group; u < args.units && !aborted; u += groups) {
+                const UnitCoord uc = decode_unit<BN>(u, args);
+                const int row0 = uc.mi * L::BM + static_cast<int>(rank) * 128;
+                const int bcols = uc.width / CG;             // B columns this CTA loads
+                const int col0 = uc.n0 + static_cast<int>(rank) * bcols;
+                const int atoms = bcols / 64;
+                const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + atoms * L::B_CHUNK) * CG;
+                for (int kb = uc.kb0; kb < uc.kb1; ++kb) {
                     if (!ptx::mbar_wait(&bar->empty[stage], phase ^ 1u, abort, limit)) {
                         raise_error(args.err, abort, kErrProducer);
                         aborted = true;
                         break;
                     }
-                    if (leader) ptx::mbar_arrive_expect_tx(&bar->full[stage], L::TX_BYTES);
+                    if (leader) ptx::mbar_arrive_expect_tx(&bar->full[stage], tx);
                     uint8_t* a_dst = smA + stage * L::A_BYTES;
                     uint8_t* b_dst = smB + stage * L::B_BYTES;
                     if constexpr (CG == 1) {
-                        ptx::tma_load_3d(a_dst, &tmA, &bar->full[stage], kb * L::BK, row0, tc.b);
-#pragma unroll
-                        for (int j = 0; j < L::B_COLS / 64; ++j)
+                        ptx::tma_load_3d(a_dst, &tmA, &bar->full[stage], kb * L::BK, row0, uc.b);
+                        for (int j = 0; j < atoms; ++j)
                             ptx::tma_load_3d(b_dst + j * L::B_CHUNK, &tmB, &bar->full[stage],
-                                             col0 + j * 64, kb * L::BK, tc.b);
+                                             col0 + j * 64, kb * L::BK, uc.b);
                     } else {
                         const uint32_t fb = ptx::map_to_cta(ptx::smem_addr(&bar->full[stage]), 0);
-                        ptx::tma_load_3d_pair(a_dst, &tmA, fb, kb * L::BK, row0, tc.b);
-#pragma unroll
-                        for (int j = 0; j < L::B_COLS / 64; ++j)
+                        ptx::tma_load_3d_pair(a_dst, &tmA, fb, kb * L::BK, row0, uc.b);
+                        for (int j = 0; j < atoms; ++j)
                             ptx::tma_load_3d_pair(b_dst + j * L::B_CHUNK, &tmB, fb, col0 + j * 64,
-                                                  kb * L::BK, tc.b);
+                                                  kb * L::BK, uc.b);
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -278,7 +363,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (leader CTA) ----------------
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            for (int t = group; t < args.tiles; t += groups) {
+            for (int u = group; u < args.units; u += groups) {
+                const UnitCoord uc = decode_unit<BN>(u, args);
+                const uint32_t idesc = uc.width == BN ? args.idesc : args.idesc_half;
                 if (!ptx::mbar_wait(&bar->acc_empty[acc], acc_phase ^ 1u, abort, limit)) {
                     raise_error(args.err, abort, kErrMma);
                     break;
@@ -286,7 +373,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + acc * BN;
                 bool ok = true;
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                for (int kb = uc.kb0; kb < uc.kb1; ++kb) {
                     if (!ptx::mbar_wait(&bar->full[stage], phase, abort, limit)) {
                         raise_error(args.err, abort, kErrMma);
                         ok = false;
@@ -303,7 +390,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         // B, MN-major: 16 K rows = two 8-row groups of
                         // 1024 B; 64-column atoms B_CHUNK apart.
                         const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 2048, L::B_CHUNK, 1024);
-                        ptx::mma_f16<CG>(d, ad, bd, args.idesc, (kb | kk) != 0);
+                        ptx::mma_f16<CG>(d, ad, bd, idesc, (kb != uc.kb0 || kk != 0) ? 1u : 0u);
                     }
                     ptx::mma_commit<CG>(&bar->empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -323,26 +410,104 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row_in_tile = quarter * 32 + lane;
         const int out_bytes = args.c_dtype == TILES_F32 ? 4 : 2;
         uint32_t acc = 0, acc_phase = 0;
-        for (int t = group; t < args.tiles; t += groups) {
-            const TileCoord tc = decode_tile(t, args.m_blocks, args.n_blocks);
+        for (int u = group; u < args.units; u += groups) {
+            const UnitCoord uc = decode_unit<BN>(u, args);
             bool ok = ptx::mbar_wait(&bar->acc_full[acc], acc_phase, abort, limit);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) raise_error(args.err, abort, kErrEpilogue);
                 break;
             }
             ptx::tc_fence_after();
-            const int64_t row = static_cast<int64_t>(tc.mi) * L::BM + rank * 128 + row_in_tile;
+            const int64_t row = static_cast<int64_t>(uc.mi) * L::BM + rank * 128 + row_in_tile;
             const bool row_ok = row < args.m;
             char* crow = static_cast<char*>(args.c) +
-                         (static_cast<int64_t>(tc.b) * args.stride_c + row * args.ldc) * out_bytes;
+                         (static_cast<int64_t>(uc.b) * args.stride_c + row * args.ldc) * out_bytes;
+            const uint32_t tacc = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+            // Partial tiles are column-major [BN][BM] so that a warp's 32
+            // rows of one column are 128 contiguous bytes.
+            const int64_t tile_elems = static_cast<int64_t>(L::BM) * BN;
+            const int prow = static_cast<int>(rank) * 128 + row_in_tile;
+            if (uc.part >= 0 && uc.part < args.ksplit - 1) {
+                // A leading K part: hand the fp32 partial tile to the last part.
+                float* dst = args.partials +
+                             (static_cast<int64_t>(uc.tail) * (args.ksplit - 1) + uc.part) * tile_elems;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld_32cols(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + c * 32, v);
-                ptx::tmem_ld_wait();
-                if (row_ok)
-                    store_row_chunk(crow, static_cast<int64_t>(tc.ni) * BN + c * 32, args.n, v,
-                                    args.c_dtype);
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32cols(tacc + c * 32, v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        dst[static_cast<int64_t>(c * 32 + i) * L::BM + prow] = __uint_as_float(v[i]);
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    uint32_t* f = args.flags +
+                                  ((static_cast<int64_t>(uc.tail) * CG + rank) * (args.ksplit - 1) +
+                                   uc.part) * 4 + quarter;
+                    store_release_gpu(f, args.epoch);
+                }
+            } else if (uc.part >= 0) {
+                // The last K part: wait for the leading parts, then add each
+                // partial into the accumulator.  This is the group's last
+                // unit, so its operand shared memory is idle: each warp
+                // stages its 32 rows of one partial there (32 KB, all copies
+                // in flight at once) as [column][32 rows] -- conflict-free
+                // reads -- and adds them into TMEM; after the last partial it
+                // casts and stores C.
+                bool ready = true;
+                for (int j = 0; j < args.ksplit - 1 && ready; ++j) {
+                    const uint32_t* f = args.flags +
+                        ((static_cast<int64_t>(uc.tail) * CG + rank) * (args.ksplit - 1) + j) * 4 +
+                        quarter;
+                    ready = wait_flag(f, args.epoch, abort, limit);
+                }
+                if (!ready && lane == 0) raise_error(args.err, abort, kErrEpilogue);
+                float* stage_buf = reinterpret_cast<float*>(base) + quarter * (BN * 32);
+                for (int j = 0; j < args.ksplit - 1 && ready; ++j) {
+                    const float* src = args.partials +
+                        (static_cast<int64_t>(uc.tail) * (args.ksplit - 1) + j) * tile_elems +
+                        static_cast<int64_t>(rank) * 128 + quarter * 32;
+#pragma unroll 4
+                    for (int i = 0; i < BN * 8 / 32; ++i) {
+                        const int piece = i * 32 + lane;          // 16-byte piece of the slice
+                        const int col = piece >> 3, seg = piece & 7;
+                        ptx::cp_async_16(stage_buf + col * 32 + seg * 4,
+                                         src + static_cast<int64_t>(col) * L::BM + seg * 4);
+                    }
+                    ptx::cp_async_wait_all();
+                    __syncwarp();
+                    const bool last = j == args.ksplit - 2;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t v[32];
+                        ptx::tmem_ld_32cols(tacc + c * 32, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) +
+                                                   stage_buf[(c * 32 + i) * 32 + lane]);
+                        if (!last) {
+                            ptx::tmem_st_32cols(tacc + c * 32, v);
+                            ptx::tmem_st_wait();
+                        } else if (row_ok) {
+                            store_row_chunk(crow, static_cast<int64_t>(uc.n0) + c * 32, args.n, v,
+                                            args.c_dtype);
+                        }
+                    }
+                    __syncwarp();
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < uc.width / 32; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32cols(tacc + c * 32, v);
+                    ptx::tmem_ld_wait();
+                    if (row_ok)
+                        store_row_chunk(crow, static_cast<int64_t>(uc.n0) + c * 32, args.n, v,
+                                        args.c_dtype);
+                }
             }
             ptx::tc_fence_before();
             __syncwarp();

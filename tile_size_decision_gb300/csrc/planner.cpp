@@ -171,10 +171,7 @@ void finish_parallelism(const tiles_device& dev, int64_t b, int64_t m, int64_t n
     v->grid = b * ceil_div(m, cfg.bm) * ceil_div(n, cfg.bn);
     int64_t resident;
     if (cfg.instr == TILES_INSTR_TCGEN05) {
-        // Persistent CTA groups: each group of cta_group SMs holds
-        // blocks_per_sm groups at a time.
-        const int cg = std::max(cfg.cta_group, 1);
-        resident = std::max<int64_t>((int64_t)v->blocks_per_sm * (dev.sm_count / cg), 1);
+        resident = gb300_resident_groups(dev, *v);
     } else {
         resident = std::max<int64_t>((int64_t)v->blocks_per_sm * dev.sm_count, 1);
     }
@@ -206,13 +203,64 @@ static int64_t round_even(double x) {
     return (int64_t)r;
 }
 
-int64_t gb300_est_clocks(const tiles_device& dev, const tiles_verdict& v, int64_t k) {
-    const tiles_config& cfg = v.cfg;
+int64_t gb300_resident_groups(const tiles_device& dev, const tiles_verdict& v) {
+    // Persistent CTA groups at once: blocks_per_sm per SM, or per CTA pair
+    // (the device's count of co-resident 2-CTA clusters when known).
+    const int cg = std::max(v.cfg.cta_group, 1);
+    const int64_t slots = (cg == 2 && dev.cta_pairs > 0) ? dev.cta_pairs : dev.sm_count / cg;
+    return std::max<int64_t>((int64_t)v.blocks_per_sm * slots, 1);
+}
+
+bool tail_split_applies(int bn, int cta_group, int64_t tiles, int64_t resident) {
+    const int cg = std::max(cta_group, 1);
+    if ((bn / 2) % cg || ((bn / 2) / cg) % 64) return false;   // a half must be whole B atoms
+    if (resident < 1) return false;
+    const int64_t rem = tiles % resident;
+    return rem > 0 && 2 * rem <= resident;
+}
+
+int64_t gb300_unit_clocks(const tiles_device& dev, const tiles_config& cfg, int64_t smem_per_stage) {
     const int cg = std::max(cfg.cta_group, 1);
-    int64_t kblocks = ceil_div(k, cfg.bk);
-    int64_t mma = (int64_t)(cfg.bm / cg) * cfg.bn * cfg.bk * 2 / std::max(dev.mma_flops_per_clk, 1);
-    int64_t fill = ceil_div(v.smem_per_stage, std::max(dev.fill_bytes_per_clk, 1));
-    return v.waves * kblocks * std::max(mma, fill);
+    const int64_t mma =
+        (int64_t)(cfg.bm / cg) * cfg.bn * cfg.bk * 2 / std::max(dev.mma_flops_per_clk, 1);
+    const int64_t fill = ceil_div(smem_per_stage, std::max(dev.fill_bytes_per_clk, 1));
+    return std::max(mma, fill);
+}
+
+int64_t gb300_reduce_clocks(const tiles_device& dev, const tiles_config& cfg) {
+    // One fp32 partial tile per CTA, read back by the last K part.
+    const int cg = std::max(cfg.cta_group, 1);
+    return ceil_div((int64_t)(cfg.bm / cg) * cfg.bn * 4, std::max(dev.fill_bytes_per_clk, 1));
+}
+
+int gb300_tail_parts(int64_t tiles, int64_t resident, int64_t k_blocks, int64_t unit,
+                     int64_t reduce) {
+    const int64_t rest = resident > 0 ? tiles % resident : 0;
+    if (rest == 0) return 0;
+    const int64_t smax = std::min<int64_t>(std::min<int64_t>(resident / rest, kMaxTailParts),
+                                           k_blocks);
+    int best = 0;
+    int64_t best_t = k_blocks * unit;
+    for (int64_t s = 2; s <= smax; ++s) {
+        const int64_t t = ceil_div(k_blocks, s) * unit + (s - 1) * reduce;
+        if (t < best_t) { best = (int)s; best_t = t; }
+    }
+    return best;
+}
+
+int64_t gb300_est_clocks(const tiles_device& dev, tiles_verdict* v, int64_t k) {
+    const tiles_config& cfg = v->cfg;
+    const int64_t kblocks = ceil_div(k, cfg.bk);
+    const int64_t unit = gb300_unit_clocks(dev, cfg, v->smem_per_stage);
+    const int64_t reduce = gb300_reduce_clocks(dev, cfg);
+    const int64_t resident = gb300_resident_groups(dev, *v);
+    // The last round, when it would fill at most half of the resident
+    // groups, runs split along K into tail_split parts; the last part reads
+    // back the others' partial tiles.
+    v->tail_split = gb300_tail_parts(v->grid, resident, kblocks, unit, reduce);
+    if (!v->tail_split) return v->waves * kblocks * unit;
+    return (v->grid / resident) * kblocks * unit + ceil_div(kblocks, v->tail_split) * unit +
+           (v->tail_split - 1) * reduce;
 }
 
 static int bytes_of(int dtype) {
@@ -266,7 +314,7 @@ int plan(const tiles_device& dev, const tiles_problem& p, std::vector<tiles_verd
             if (v.failures) continue;
             finish_parallelism(dev, p.b, p.m, p.n, &v);
             v.c0_bytes = c0_bytes(p.b, p.m, p.n, p.k, c.bm, c.bn, in_b, out_b);
-            v.est_clocks = gb300_est_clocks(dev, v, p.k);
+            v.est_clocks = gb300_est_clocks(dev, &v, p.k);
             kept.push_back({v, round_even(v.c0_bytes), order++});
         }
         std::stable_sort(kept.begin(), kept.end(), [](const Ranked& a, const Ranked& b) {

@@ -11,10 +11,10 @@ namespace tiles {
 // Threads of the warp-specialised GEMM block: warp 0 TMA producer, warp 1
 // MMA issuer and TMEM owner, warps 2-5 epilogue.
 constexpr int kGemmThreads = 192;
-// Registers per thread of the GEMM kernels as built (ptxas reports 61,
-// which the per-warp granule of 256 rounds to 64); the planner's occupancy
-// uses this figure.
-constexpr int kGemmRegsPerThread = 64;
+// Registers per thread of the GEMM kernels as built (ptxas reports up to
+// 110, which the per-warp granule of 256 rounds to 112); the planner's
+// occupancy uses this figure.
+constexpr int kGemmRegsPerThread = 112;
 // Shared memory beyond the operand stages: mbarriers, the TMEM address slot,
 // an abort flag (kSmemBarrierBytes) and the slack that lets the operand
 // tiles start on a 1024-byte boundary, as the 128-byte swizzle requires.
@@ -41,7 +41,21 @@ double c0_bytes(int64_t b, int64_t m, int64_t n, int64_t k, int bm, int bn, int 
                 int out_bytes);
 int plan(const tiles_device& dev, const tiles_problem& p, std::vector<tiles_verdict>* out);
 int64_t gb300_smem_bytes(const tiles_config& cfg, int in_bytes, int64_t* per_stage);
-int64_t gb300_est_clocks(const tiles_device& dev, const tiles_verdict& v, int64_t k);
+int64_t gb300_est_clocks(const tiles_device& dev, tiles_verdict* v, int64_t k);
+// Whether the last round of `tiles` over `resident` CTA groups runs as
+// N-half tiles (it would otherwise fill at most half of the groups).
+bool tail_split_applies(int bn, int cta_group, int64_t tiles, int64_t resident);
+int64_t gb300_resident_groups(const tiles_device& dev, const tiles_verdict& v);
+// Clocks per K block of one tile (max of MMA and operand fill) and of
+// reading back one partial tile per CTA.
+int64_t gb300_unit_clocks(const tiles_device& dev, const tiles_config& cfg, int64_t smem_per_stage);
+int64_t gb300_reduce_clocks(const tiles_device& dev, const tiles_config& cfg);
+// K parts of each last-round tile (0: no split): among 2 .. min(resident /
+// rest, kMaxTailParts, K blocks) the count minimising ceil(K blocks / s) *
+// unit + (s - 1) * reduce, if that beats the unsplit K blocks * unit.
+int gb300_tail_parts(int64_t tiles, int64_t resident, int64_t k_blocks, int64_t unit,
+                     int64_t reduce);
+constexpr int kMaxTailParts = 8;
 void device_preset_h100(tiles_device* d);
 void device_preset_gb300(tiles_device* d);
 int htile_rows(int H, int kh, int sh, int pt, int d, int o0, int o1, tiles_htile* t);

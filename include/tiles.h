@@ -117,8 +117,16 @@ typedef struct {
     int32_t instr;           /* tiles_instr */
     int32_t acc_bufs;        /* GB300: TMEM accumulator buffers (0 on the page) */
     int32_t cta_group;       /* GB300: 1 or 2 SMs per MMA (0 on the page) */
-    int32_t reserved[4];
+    int32_t tail;            /* GB300 last-round schedule, tiles_tail (0 = planner's choice) */
+    int32_t reserved[3];
 } tiles_config;
+
+/* Schedules of a last round of tiles that would leave resident CTA groups
+ * idle (constraint C4): as whole tiles, as N-half tiles, or split along K
+ * into parts whose fp32 partials the last part adds (needs workspace). */
+typedef enum {
+    TILES_TAIL_AUTO = 0, TILES_TAIL_WHOLE = 1, TILES_TAIL_NHALF = 2, TILES_TAIL_KSPLIT = 3
+} tiles_tail;
 
 /* Result of checking one configuration (the page's Verdict record). */
 typedef struct {
@@ -138,15 +146,14 @@ typedef struct {
     uint32_t failures;           /* TILES_FAIL_* bits */
     int32_t c3_violations;       /* how many C3 conditions failed */
     uint32_t warnings;           /* TILES_WARN_* bits */
-    int32_t tail_split;          /* GB300: K parts of each last-round tile (0: none) */
+    int32_t tail_split;          /* GB300 last round: K parts (>= 2), -1 N-halves, 0 whole */
     int64_t grid;                /* C4: output tiles (times the batch) */
     int64_t waves;               /* C4 */
     double last_wave_fill;       /* C4, in [0, 1] */
     double c0_bytes;             /* C0, float64 as on the page */
-    int64_t est_clocks;          /* GB300 time model (0 in page mode): rounds of
-                                    ceil(K/bk) K blocks of max(MMA clocks, fill
-                                    clocks); with tail_split the last round runs
-                                    ceil(ceil(K/bk) / tail_split) K blocks */
+    int64_t est_clocks;          /* GB300 time model (0 in page mode): whole rounds of
+                                    ceil(K/bk) K blocks of max(MMA, fill) clocks,
+                                    then the last round in its cheapest schedule */
 } tiles_verdict;
 
 /* A planning request. */

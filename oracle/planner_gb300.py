@@ -24,15 +24,16 @@ Rules
        pairs (cta_pairs, else sm_count // 2) for pairs; waves; fill as on the
        page.
   C0   the page's expression with b, in_bytes, out_bytes.
-  time est_clocks = waves * ceil(K/bk) * unit with unit = max(mma, fill),
-       mma = (bm/cg)*bn*bk*2 // mma_flops_per_clk and
-       fill = ceil(smem_per_stage / fill_bytes_per_clk).  When the last round
-       would leave groups idle its tiles split along K into tail_split = s
-       parts, s in 2..min(resident // rest, 8, K blocks) minimising
+  time est_clocks = (grid // resident) * ceil(K/bk) * unit + the last
+       round's cost, unit = max(mma, fill), mma = (bm/cg)*bn*bk*2 //
+       mma_flops_per_clk, fill = ceil(smem_per_stage / fill_bytes_per_clk).
+       The last round (when grid % resident > 0) takes the cheapest of:
+       whole tiles ceil(K/bk) * unit; N-halves (if whole B atoms and the rest
+       fills at most half the groups) ceil(K/bk) * unit of the half-width
+       tile; K parts s in 2..min(resident // rest, 8, K blocks):
        ceil(K/bk / s) * unit + (s-1) * reduce with reduce =
-       ceil((bm/cg)*bn*4 / fill_bytes_per_clk) (reading one partial back):
-       est_clocks = (grid // resident) * ceil(K/bk) * unit
-                    + ceil(ceil(K/bk) / s) * unit + (s-1) * reduce.
+       2 * ceil((bm/cg)*bn*4 / fill_bytes_per_clk) + 2048.  tail_split
+       reports s, -1 for N-halves, 0 for whole tiles.
   rank (est_clocks, round(C0), -bps, smem_total), stable over the variant
        order.
 """
@@ -175,19 +176,50 @@ def finish_parallelism(v: GB300Verdict, dev: GB300Device, b: int, m: int, n: int
 MAX_TAIL_PARTS = 8
 
 
-def tail_parts(grid: int, resident: int, kblocks: int, unit: int, reduce: int) -> int:
-    """K parts of each tile of a last round: the count s in 2 .. min(resident
-    // rest, 8, K blocks) minimising ceil(K blocks / s) * unit + (s-1) *
-    reduce, if it beats no split; 0 for no split."""
+HANDOFF_CLOCKS = 2048
+
+
+def _stage_bytes(bm: int, bn: int, bk: int, cg: int, in_bytes: int = 2) -> int:
+    return ((bm // cg) * bk + bk * (bn // cg)) * in_bytes
+
+
+def _unit(dev: GB300Device, bm: int, bn: int, bk: int, cg: int) -> int:
+    mma = (bm // cg) * bn * bk * 2 // dev.mma_flops_per_clk
+    fill = page.ceil_div(_stage_bytes(bm, bn, bk, cg), dev.fill_bytes_per_clk)
+    return max(mma, fill)
+
+
+def nhalf_applies(cfg: GB300Config, grid: int, resident: int) -> bool:
+    """A last round filling at most half the groups, with N-halves that are
+    whole 64-column B atoms per CTA."""
+    cg = max(cfg.cta_group, 1)
+    half = cfg.bn // 2
+    if half % cg or (half // cg) % 64:
+        return False
     rest = grid % resident
+    return 0 < rest and 2 * rest <= resident
+
+
+def tail_choice(v: GB300Verdict, dev: GB300Device, kblocks: int, resident: int):
+    """(mode, parts, clocks) of the last round: whole tiles, N-halves or K
+    parts, whichever the model makes cheapest (ties keep that order and the
+    fewer parts)."""
+    cfg = v.cfg
+    cg = max(cfg.cta_group, 1)
+    unit = _unit(dev, cfg.bm, cfg.bn, cfg.bk, cg)
+    best = ("whole", 0, kblocks * unit)
+    rest = v.grid % resident
     if rest == 0:
-        return 0
-    smax = min(resident // rest, MAX_TAIL_PARTS, kblocks)
-    best, best_t = 0, kblocks * unit
-    for s in range(2, smax + 1):
+        return best
+    if nhalf_applies(cfg, v.grid, resident):
+        t = kblocks * _unit(dev, cfg.bm, cfg.bn // 2, cfg.bk, cg)
+        if t < best[2]:
+            best = ("nhalf", 0, t)
+    reduce = 2 * page.ceil_div((cfg.bm // cg) * cfg.bn * 4, dev.fill_bytes_per_clk) + HANDOFF_CLOCKS
+    for s in range(2, min(resident // rest, MAX_TAIL_PARTS, kblocks) + 1):
         t = page.ceil_div(kblocks, s) * unit + (s - 1) * reduce
-        if t < best_t:
-            best, best_t = s, t
+        if t < best[2]:
+            best = ("ksplit", s, t)
     return best
 
 
@@ -195,16 +227,12 @@ def est_clocks(v: GB300Verdict, dev: GB300Device, k: int) -> int:
     cfg = v.cfg
     cg = max(cfg.cta_group, 1)
     kblocks = page.ceil_div(k, cfg.bk)
-    mma = (cfg.bm // cg) * cfg.bn * cfg.bk * 2 // dev.mma_flops_per_clk
-    fill = page.ceil_div(v.smem_per_stage, dev.fill_bytes_per_clk)
-    unit = max(mma, fill)
-    reduce = page.ceil_div((cfg.bm // cg) * cfg.bn * 4, dev.fill_bytes_per_clk)
+    unit = _unit(dev, cfg.bm, cfg.bn, cfg.bk, cg)
     resident = resident_groups(v, dev)
-    v.tail_split = tail_parts(v.grid, resident, kblocks, unit, reduce)
-    if not v.tail_split:
-        return v.waves * kblocks * unit
-    return ((v.grid // resident) * kblocks * unit + page.ceil_div(kblocks, v.tail_split) * unit
-            + (v.tail_split - 1) * reduce)
+    mode, parts, clocks = tail_choice(v, dev, kblocks, resident)
+    v.tail_split = parts if mode == "ksplit" else (-1 if mode == "nhalf" else 0)
+    rest = v.grid % resident
+    return (v.grid // resident) * kblocks * unit + (clocks if rest else 0)
 
 
 def plan(b: int, m: int, n: int, k: int, dev: GB300Device, in_bytes: int = 2,

@@ -228,12 +228,13 @@ def _groups(cg):
 @pytest.mark.parametrize("v", [(256, 2), (256, 1), (128, 1)], ids=["bn256_cg2", "bn256_cg1",
                                                                    "bn128_cg1"])
 @pytest.mark.parametrize("rest", ["one", "half_round", "all_halves"])
-@pytest.mark.parametrize("room", ["small", "full"])
-def test_tail_rounds_split(ws, v, rest, room):
+@pytest.mark.parametrize("tail", ["auto_small_ws", "nhalf", "ksplit"])
+def test_tail_rounds_split(ws, v, rest, tail):
     # Tile counts around the resident group count, so the last round is
-    # split: along K when the workspace holds the partial tiles (room
-    # "full"), else into N-halves (room "small"): one extra tile, half a
-    # round extra, or a problem smaller than one round; N and M are ragged.
+    # split: into N-halves, along K (the workspace holds the partial tiles),
+    # or as the planner picks with only the 256-byte workspace; one extra
+    # tile, half a round extra, or a problem smaller than one round; N and M
+    # are ragged.
     bn, cg = v
     g = _groups(cg)
     tiles = {"one": g + 1, "half_round": g + g // 2, "all_halves": 5}[rest]
@@ -243,14 +244,19 @@ def test_tail_rounds_split(ws, v, rest, room):
     a = to_cuda(a_np, S.F16, -(-k // 8) * 8)
     b = to_cuda(b_np, S.F16, -(-n // 8) * 8)
     c = empty_out((m, n), S.F32, -(-n // 4) * 4)
-    w = T.gemm_workspace(a, b, c, variant(v)) if room == "full" else ws
-    sch = T.gemm_schedule(a, b, c, variant(v), w)
-    if room == "full":
+    bn_, cg_ = v
+    cfg = T.make_config(128 * cg_, bn_, 64, VARIANTS[v], 192, "tcgen05", 2, cg_,
+                        tail="auto" if tail == "auto_small_ws" else tail)
+    w = ws if tail == "auto_small_ws" else T.gemm_workspace(a, b, c, cfg)
+    sch = T.gemm_schedule(a, b, c, cfg, w)
+    if tail == "ksplit":
         assert sch.tail_mode == 2 and sch.ksplit >= 2
         assert sch.units == sch.full_units + (sch.tiles - sch.full_units) * sch.ksplit
+    if tail == "nhalf":
+        assert sch.tail_mode == 1 and sch.units == sch.full_units + 2 * (sch.tiles - sch.full_units)
     for _ in range(3):          # reuse of the workspace across launches
         c.fill_(float("nan"))
-        T.gemm(a, b, out=c, cfg=variant(v), workspace=w)
+        T.gemm(a, b, out=c, cfg=cfg, workspace=w)
         T.check(w)
         assert_close(to_f64(c), S.widen(a_np, S.F16), S.widen(b_np, S.F16), S.F32)
 
@@ -285,3 +291,22 @@ def test_schedule_of_the_bench_shape():
     else:
         assert sch.full_units == sch.units == sch.tiles
     assert sch.groups == min(sch.units, sch.resident_groups)
+
+
+@pytest.mark.parametrize("tail", ["whole", "nhalf", "ksplit"])
+def test_forced_tail_schedules(tail):
+    # 256x256 pair tiles with one tile more than a round: each forced last-
+    # round schedule runs as asked and gives the same result within tolerance.
+    g = _groups(2)
+    m, n, k = 256 * (g + 3) - 11, 256, 640
+    a_np = S.random_matrix(61, (m, k), S.BF16, "normal")
+    b_np = S.random_matrix(62, (k, n), S.BF16, "normal")
+    a, b = to_cuda(a_np, S.BF16), to_cuda(b_np, S.BF16)
+    c = empty_out((m, n), S.BF16)
+    cfg = T.make_config(256, 256, 64, 7, 192, "tcgen05", 2, 2, tail=tail)
+    w = T.gemm_workspace(a, b, c, cfg)
+    sch = T.gemm_schedule(a, b, c, cfg, w)
+    assert sch.tail_mode == {"whole": 0, "nhalf": 1, "ksplit": 2}[tail]
+    T.gemm(a, b, out=c, cfg=cfg, workspace=w)
+    T.check(w)
+    assert_close(to_f64(c), S.widen(a_np, S.BF16), S.widen(b_np, S.BF16), S.BF16)

@@ -51,8 +51,11 @@ class Device(C.Structure):
 
 class Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
-        "bm", "bn", "bk", "stages", "threads", "instr", "acc_bufs", "cta_group")] + \
-        [("reserved", C.c_int32 * 4)]
+        "bm", "bn", "bk", "stages", "threads", "instr", "acc_bufs", "cta_group", "tail")] + \
+        [("reserved", C.c_int32 * 3)]
+
+
+TAIL_AUTO, TAIL_WHOLE, TAIL_NHALF, TAIL_KSPLIT = 0, 1, 2, 3
 
 
 class Verdict(C.Structure):

@@ -260,24 +260,34 @@ int gemm_prepare(const tiles_gemm_desc* d, const tiles_config* user_cfg, bool ba
     const int64_t k_blocks = (d->k + cfg.bk - 1) / cfg.bk;
     const int64_t rest = gp->tiles % gp->resident;
     const int64_t full = gp->tiles - rest;
-    int64_t stage_bytes = 0;
-    gb300_smem_bytes(cfg, 2, &stage_bytes);
-    const int64_t parts = gb300_tail_parts(gp->tiles, gp->resident, k_blocks,
-                                           gb300_unit_clocks(gp->dev, cfg, stage_bytes),
-                                           gb300_reduce_clocks(gp->dev, cfg));
-    if (parts >= 2) {
+    const int forced = user_cfg ? user_cfg->tail : TILES_TAIL_AUTO;
+    if (forced < TILES_TAIL_AUTO || forced > TILES_TAIL_KSPLIT)
+        return fail(TILES_ERR_INVALID_ARG, "unknown tail schedule %d", forced);
+    TailChoice tc = gb300_tail_choice(gp->dev, cfg, gp->tiles, gp->resident, k_blocks, 2, forced);
+    if (rest && tc.mode == TILES_TAIL_KSPLIT) {
         GemmPlan k = *gp;
-        k.ksplit = (int)parts;
+        k.ksplit = tc.parts;
         ksplit_layout(&k, rest);
         if (static_cast<uint64_t>(ws_bytes) >= static_cast<uint64_t>(k.ws_needed)) {
             *gp = k;
             gp->tail_mode = kTailKSplit;
             gp->full_units = full;
-            gp->units = full + rest * parts;
+            gp->units = full + rest * tc.parts;
+        } else if (forced == TILES_TAIL_KSPLIT) {
+            return fail(TILES_ERR_INVALID_ARG, "a K-split last round needs %lld workspace bytes",
+                        (long long)k.ws_needed);
+        } else {
+            // Not enough workspace: the cheaper of whole tiles and N-halves.
+            const TailChoice nh = gb300_tail_choice(gp->dev, cfg, gp->tiles, gp->resident,
+                                                    k_blocks, 2, TILES_TAIL_NHALF);
+            const TailChoice wh = gb300_tail_choice(gp->dev, cfg, gp->tiles, gp->resident,
+                                                    k_blocks, 2, TILES_TAIL_WHOLE);
+            tc = (nh.mode == TILES_TAIL_NHALF && nh.clocks < wh.clocks) ? nh : wh;
         }
     }
-    if (gp->tail_mode == kTailNone &&
-        tail_split_applies(cfg.bn, cfg.cta_group, gp->tiles, gp->resident)) {
+    if (rest && gp->tail_mode == kTailNone && tc.mode == TILES_TAIL_NHALF) {
+        if (!tail_split_applies(cfg.bn, cfg.cta_group, gp->tiles, gp->resident))
+            return fail(TILES_ERR_INVALID_ARG, "this tile cannot split into N-halves");
         gp->tail_mode = kTailNHalf;
         gp->full_units = full;
         gp->units = full + 2 * rest;

@@ -228,39 +228,59 @@ int64_t gb300_unit_clocks(const tiles_device& dev, const tiles_config& cfg, int6
 }
 
 int64_t gb300_reduce_clocks(const tiles_device& dev, const tiles_config& cfg) {
-    // One fp32 partial tile per CTA, read back by the last K part.
+    // One fp32 partial tile per CTA written by a leading part and read back
+    // by the last part, plus the hand-off's fixed latency.
     const int cg = std::max(cfg.cta_group, 1);
-    return ceil_div((int64_t)(cfg.bm / cg) * cfg.bn * 4, std::max(dev.fill_bytes_per_clk, 1));
+    return 2 * ceil_div((int64_t)(cfg.bm / cg) * cfg.bn * 4, std::max(dev.fill_bytes_per_clk, 1)) +
+           kTailHandoffClocks;
 }
 
-int gb300_tail_parts(int64_t tiles, int64_t resident, int64_t k_blocks, int64_t unit,
-                     int64_t reduce) {
+TailChoice gb300_tail_choice(const tiles_device& dev, const tiles_config& cfg, int64_t tiles,
+                             int64_t resident, int64_t k_blocks, int in_bytes, int forced) {
+    TailChoice tc{TILES_TAIL_WHOLE, 0, 0};
+    int64_t stage = 0;
+    gb300_smem_bytes(cfg, in_bytes, &stage);
+    const int64_t unit = gb300_unit_clocks(dev, cfg, stage);
+    tc.clocks = k_blocks * unit;
     const int64_t rest = resident > 0 ? tiles % resident : 0;
-    if (rest == 0) return 0;
-    const int64_t smax = std::min<int64_t>(std::min<int64_t>(resident / rest, kMaxTailParts),
-                                           k_blocks);
-    int best = 0;
-    int64_t best_t = k_blocks * unit;
-    for (int64_t s = 2; s <= smax; ++s) {
-        const int64_t t = ceil_div(k_blocks, s) * unit + (s - 1) * reduce;
-        if (t < best_t) { best = (int)s; best_t = t; }
+    if (rest == 0) return tc;
+    const int cg = std::max(cfg.cta_group, 1);
+    // N-halves: each half loads all of A and half of B per K block.
+    if ((forced == TILES_TAIL_AUTO || forced == TILES_TAIL_NHALF) &&
+        tail_split_applies(cfg.bn, cg, tiles, resident)) {
+        tiles_config h = cfg;
+        h.bn = cfg.bn / 2;
+        int64_t half_stage = 0;
+        gb300_smem_bytes(h, in_bytes, &half_stage);
+        const int64_t t = k_blocks * gb300_unit_clocks(dev, h, half_stage);
+        if (forced == TILES_TAIL_NHALF || t < tc.clocks) tc = TailChoice{TILES_TAIL_NHALF, 0, t};
     }
-    return best;
+    // K parts: each part runs ceil(K blocks / s) K blocks; the last reads
+    // back s - 1 partial tiles.
+    if (forced == TILES_TAIL_AUTO || forced == TILES_TAIL_KSPLIT) {
+        const int64_t smax = std::min<int64_t>(std::min<int64_t>(resident / rest, kMaxTailParts),
+                                               k_blocks);
+        const int64_t reduce = gb300_reduce_clocks(dev, cfg);
+        bool first = forced == TILES_TAIL_KSPLIT;
+        for (int64_t s = 2; s <= smax; ++s) {
+            const int64_t t = ceil_div(k_blocks, s) * unit + (s - 1) * reduce;
+            if (first || t < tc.clocks) { tc = TailChoice{TILES_TAIL_KSPLIT, (int)s, t}; first = false; }
+        }
+    }
+    return tc;
 }
 
 int64_t gb300_est_clocks(const tiles_device& dev, tiles_verdict* v, int64_t k) {
     const tiles_config& cfg = v->cfg;
     const int64_t kblocks = ceil_div(k, cfg.bk);
-    const int64_t unit = gb300_unit_clocks(dev, cfg, v->smem_per_stage);
-    const int64_t reduce = gb300_reduce_clocks(dev, cfg);
+    int64_t stage = 0;
+    gb300_smem_bytes(cfg, 2, &stage);
+    const int64_t unit = gb300_unit_clocks(dev, cfg, stage);
     const int64_t resident = gb300_resident_groups(dev, *v);
-    // The last round, when it would fill at most half of the resident
-    // groups, runs split along K into tail_split parts; the last part reads
-    // back the others' partial tiles.
-    v->tail_split = gb300_tail_parts(v->grid, resident, kblocks, unit, reduce);
-    if (!v->tail_split) return v->waves * kblocks * unit;
-    return (v->grid / resident) * kblocks * unit + ceil_div(kblocks, v->tail_split) * unit +
-           (v->tail_split - 1) * reduce;
+    const int64_t rest = v->grid % resident;
+    const TailChoice tc = gb300_tail_choice(dev, cfg, v->grid, resident, kblocks, 2, TILES_TAIL_AUTO);
+    v->tail_split = tc.mode == TILES_TAIL_KSPLIT ? tc.parts : tc.mode == TILES_TAIL_NHALF ? -1 : 0;
+    return (v->grid / resident) * kblocks * unit + (rest ? tc.clocks : 0);
 }
 
 static int bytes_of(int dtype) {

@@ -50,11 +50,15 @@ int64_t gb300_resident_groups(const tiles_device& dev, const tiles_verdict& v);
 // reading back one partial tile per CTA.
 int64_t gb300_unit_clocks(const tiles_device& dev, const tiles_config& cfg, int64_t smem_per_stage);
 int64_t gb300_reduce_clocks(const tiles_device& dev, const tiles_config& cfg);
-// K parts of each last-round tile (0: no split): among 2 .. min(resident /
-// rest, kMaxTailParts, K blocks) the count minimising ceil(K blocks / s) *
-// unit + (s - 1) * reduce, if that beats the unsplit K blocks * unit.
-int gb300_tail_parts(int64_t tiles, int64_t resident, int64_t k_blocks, int64_t unit,
-                     int64_t reduce);
+// Schedule of a last round that leaves resident groups idle: the cheapest
+// (or the forced) of whole tiles (K blocks * unit), N-halves (K blocks *
+// half-tile unit) and K parts s in 2 .. min(resident / rest, kMaxTailParts,
+// K blocks) (ceil(K blocks / s) * unit + (s - 1) * reduce).
+struct TailChoice { int mode; int parts; int64_t clocks; };
+TailChoice gb300_tail_choice(const tiles_device& dev, const tiles_config& cfg, int64_t tiles,
+                             int64_t resident, int64_t k_blocks, int in_bytes, int forced);
+// Fixed clocks of a K-part hand-off (flag release, acquire, copy latency).
+constexpr int64_t kTailHandoffClocks = 2048;
 constexpr int kMaxTailParts = 8;
 void device_preset_h100(tiles_device* d);
 void device_preset_gb300(tiles_device* d);

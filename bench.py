@@ -286,10 +286,13 @@ def conv_job(wl, dev, tiles, torch):
     j.out = torch.empty(shape, dtype=TORCH_DT(torch)[wl.out_dtype], device=dev)
     j.host_out = torch.empty(shape, dtype=j.out.dtype).pin_memory()
     x_d, w_d = j.dev_in
+    # A workspace sized for the TMA im2col producer (the default path).
+    j.ws = tiles.conv_workspace(x_d, w_d, (wl.sh, wl.sw), (wl.ph, wl.pw), (wl.dh, wl.dw),
+                                wl.tile_oh)
 
     def step(ws, stream):
         tiles.conv2d_htiled(x_d, w_d, (wl.sh, wl.sw), (wl.ph, wl.pw), (wl.dh, wl.dw), wl.tile_oh,
-                            out=j.out, workspace=ws, stream=stream)
+                            out=j.out, workspace=j.ws, stream=stream)
 
     j.step = step
     j.flops = wl.flops
@@ -307,6 +310,8 @@ def conv_job(wl, dev, tiles, torch):
         "distribution": wl.dist, "seed": wl.seed,
         "gemm_per_tile": {"m": wl.c_out, "n": wl.tile_oh * wl.ow, "k": wl.c * wl.kh * wl.kw},
         "input_bytes_with_halo": halo_bytes,
+        "producer": "tma (NCHW input transposed to NHWC in the workspace, then strided TMA boxes)",
+        "workspace_bytes": int(j.ws.numel()),
     }
     j.dtype = "f16" if wl.in_dtype == S.F16 else "bf16"
     j.oracle = lambda budget: oracle_conv_sample(wl, budget, x_np, w_np)

@@ -189,13 +189,18 @@ typedef struct {
     int32_t pad0;
 } tiles_gemm_desc;
 
-/* An NCHW convolution with OIHW weights, NCHW output, fully packed. */
+/* Memory order of the convolution input. */
+typedef enum { TILES_LAYOUT_NCHW = 0, TILES_LAYOUT_NHWC = 1 } tiles_layout;
+
+/* A convolution with OIHW weights and NCHW output, fully packed; the input
+ * is NCHW or NHWC (x_layout). */
 typedef struct {
     int32_t n, c, h, w;               /* input */
     int32_t c_out, kh, kw;            /* weights */
     int32_t sh, sw, ph, pw, dh, dw;   /* stride, symmetric pad, dilation */
     int32_t in_dtype, out_dtype;      /* in: F16/BF16 (x and w); out: F16/BF16/F32 */
-    const void* x;                    /* device, [n][c][h][w] */
+    int32_t x_layout;                 /* tiles_layout of x */
+    const void* x;                    /* device, [n][c][h][w] or [n][h][w][c] */
     const void* wt;                   /* device, [c_out][c][kh][kw] */
     void* y;                          /* device, [n][c_out][oh][ow] */
 } tiles_conv_desc;
@@ -309,12 +314,27 @@ int tiles_gemm_batched(const tiles_gemm_desc* desc, const tiles_config* cfg, voi
                        size_t ws_bytes, void* stream);
 
 /* y = conv2d(x, w) as an implicit GEMM per output H-tile of tile_oh rows:
- * per image and tile, M = c_out, N = tile rows x OW, K = c*kh*kw; the
- * producer gathers the input slice [in_start, min(in_end, H)) with the
- * sub-operator pads pt'/pb' from tiles_htile_rows.  tile_oh >= 1;
- * c*kh*kw and OH*OW must be multiples of 8. */
+ * per image and tile, M = c_out, N = the tile's output pixels, K =
+ * c*kh*kw, and each tile reads only its input slice [in_start, min(in_end,
+ * H)) with the sub-operator pads pt'/pb' from tiles_htile_rows.
+ *
+ * Two producers build the im2col operand:
+ *  - TMA (default when it applies: c % 8 == 0 and strides <= 8; needs
+ *    tiles_conv_workspace_bytes() of workspace): the
+ *    weights are reordered to [c_out][r][s][c padded to 64] and an NCHW
+ *    input is transposed to NHWC in the workspace, then per filter tap and
+ *    64 channels the operand is one strided TMA box of the NHWC input, the
+ *    pads arriving as zero fill;
+ *  - gather (NCHW input only; c*kh*kw a multiple of 8): four warps gather
+ *    the operand from global memory into shared memory.
+ * cfg == NULL picks the TMA producer when the workspace allows; a cfg with
+ * threads 192 forces it, threads 320 forces the gather.  tile_oh >= 1. */
 int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
                         void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes the TMA producer needs for this convolution (256 when it
+ * does not apply; 0 on invalid arguments). */
+size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh);
 
 /* The GEMM of tiles_gemm_batched (batch >= 1) for callers that cannot
  * allocate device memory and so cannot pass a workspace.  The source pages

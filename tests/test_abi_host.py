@@ -315,3 +315,8 @@ def test_plan_validation(lib):
     assert lib.tiles_plan(C.byref(dev), C.byref(p), None, 0, C.byref(nf)) != _abi.OK
     t = _abi.HTile()
     assert lib.tiles_htile_rows(9, 3, 2, 1, 1, 2, 2, C.byref(t)) == _abi.ERR_INVALID_ARG
+
+
+def test_binding_exports_every_listed_name():
+    for name in T.__all__:
+        assert hasattr(T, name), name

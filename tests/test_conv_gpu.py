@@ -32,8 +32,13 @@ def ws():
     return T.workspace()
 
 
-def run_conv(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, ws, guard=0):
+def run_conv(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, ws, guard=0, producer="gather",
+             layout="nchw"):
+    # producer "gather": the small workspace (threads gather the operand);
+    # "tma": a workspace sized for the TMA producer.
     x = to_cuda(x_np, in_dt)
+    if layout == "nhwc":
+        x = x.permute(0, 2, 3, 1).contiguous()
     w = to_cuda(w_np, in_dt)
     n, c, h, wd = x_np.shape
     co, _, kh, kw = w_np.shape
@@ -42,7 +47,12 @@ def run_conv(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, ws, guard=0):
     total = n * co * oh * ow
     flat = torch.full((total + 2 * guard,), 2048.0, dtype=TORCH_DT[out_dt], device="cuda")
     y = flat[guard:guard + total].view(n, co, oh, ow)
-    T.conv2d_htiled(x, w, stride, pad, dil, tile_oh, out=y, workspace=ws)
+    if producer == "tma":
+        ws = T.conv_workspace(x, w, stride, pad, dil, tile_oh, layout=layout)
+        cfg = T.make_config(128, 256, 64, 4, 192, "tcgen05", 2, 1)
+    else:
+        cfg = None
+    T.conv2d_htiled(x, w, stride, pad, dil, tile_oh, out=y, workspace=ws, cfg=cfg, layout=layout)
     T.check(ws)
     host = to_f64(flat)
     if guard:
@@ -134,3 +144,95 @@ def test_rejects_unaligned_weights(ws):
     with pytest.raises(T.TilesError) as e:
         T.conv2d_htiled(x, w, (1, 1), (1, 1), (1, 1), 4, workspace=ws)
     assert e.value.status == -3
+
+
+# --------------------------------------------------------------------------- #
+# The TMA im2col producer
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("case", TINY, ids=lambda c: "_".join(str(v) for v in c[:7]))
+@pytest.mark.parametrize("layout", ["nchw", "nhwc"])
+def test_tma_tiny_against_loops(ws, case, layout):
+    n, c, h, wd, co, kh, kw, st, pad, dil, tile = case
+    x = S.random_matrix(1, (n, c, h, wd), S.F16)
+    w = S.random_matrix(2, (co, c, kh, kw), S.F16)
+    got = run_conv(x, w, S.F16, S.F32, st, pad, dil, tile, ws, guard=64, producer="tma",
+                   layout=layout)
+    x64, w64 = S.widen(x, S.F16), S.widen(w, S.F16)
+    if n * co * c * h * wd < 200000:
+        ref = OC.conv2d_loops(x64, w64, st, pad, dil)
+        bound = OC.conv2d_loops(np.abs(x64), np.abs(w64), st, pad, dil)
+        ok, worst, idx = OT.check(got, ref, bound, S.F32)
+        assert ok, f"worst ratio {worst} at {idx}"
+    check_against_oracle(got, x64, w64, st, pad, dil, S.F32)
+
+
+@pytest.mark.parametrize("dt", [S.F16, S.BF16])
+def test_tma_integer_inputs_exact(ws, dt):
+    x = S.integer_matrix(3, (2, 72, 30, 28), dt)
+    w = S.integer_matrix(4, (40, 72, 3, 3), dt)
+    got = run_conv(x, w, dt, S.F32, (2, 2), (1, 1), (1, 1), 4, ws, producer="tma")
+    ref = OC.conv2d(S.widen(x, dt), S.widen(w, dt), (2, 2), (1, 1), (1, 1))
+    assert np.array_equal(got, ref)
+
+
+def test_tma_tile_height_does_not_change_bits(ws):
+    x = S.random_matrix(5, (2, 16, 37, 34), S.BF16, "normal")
+    w = S.random_matrix(6, (64, 16, 3, 3), S.BF16, "normal")
+    outs = [run_conv(x, w, S.BF16, S.F32, (2, 1), (1, 1), (1, 1), t, ws, producer="tma")
+            for t in (1, 2, 3, 7, 19, 40)]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    check_against_oracle(outs[0], S.widen(x, S.BF16), S.widen(w, S.BF16), (2, 1), (1, 1), (1, 1),
+                         S.F32)
+
+
+def test_tma_wide_rows_and_many_h_tiles(ws):
+    # W wider than one TMA box (several column blocks) and 300 output rows at
+    # tile height 1 (three launches of H-tiles).
+    x = S.random_matrix(7, (1, 8, 300, 600), S.F16)
+    w = S.random_matrix(8, (12, 8, 3, 3), S.F16)
+    got = run_conv(x, w, S.F16, S.F16, (1, 2), (1, 1), (1, 1), 1, ws, guard=32, producer="tma")
+    check_against_oracle(got, S.widen(x, S.F16), S.widen(w, S.F16), (1, 2), (1, 1), (1, 1), S.F16)
+
+
+def test_tma_channels_not_multiple_of_64(ws):
+    x = S.random_matrix(9, (2, 40, 20, 22), S.BF16, "normal")
+    w = S.random_matrix(10, (300, 40, 3, 3), S.BF16, "normal")
+    got = run_conv(x, w, S.BF16, S.BF16, (1, 1), (1, 1), (1, 1), 6, ws, guard=16, producer="tma")
+    check_against_oracle(got, S.widen(x, S.BF16), S.widen(w, S.BF16), (1, 1), (1, 1), (1, 1),
+                         S.BF16)
+
+
+@pytest.mark.parametrize("layout", ["nchw", "nhwc"])
+def test_tma_conv_workload_full(ws, layout):
+    wl = S.WORKLOADS["conv_htiled"]
+    x, w = S.conv_inputs(wl)
+    got = run_conv(x, w, wl.in_dtype, wl.out_dtype, (wl.sh, wl.sw), (wl.ph, wl.pw),
+                   (wl.dh, wl.dw), wl.tile_oh, ws, producer="tma", layout=layout)
+    check_against_oracle(got, S.widen(x, wl.in_dtype), S.widen(w, wl.in_dtype), (wl.sh, wl.sw),
+                         (wl.ph, wl.pw), (wl.dh, wl.dw), wl.out_dtype)
+
+
+def test_default_producer_with_workspace_is_tma(ws):
+    # cfg=None with a workspace of conv_workspace size takes the TMA producer,
+    # whose K order (r, s, ci) differs from the gather's (ci, r, s): both
+    # stay within tolerance of the oracle.
+    wl = S.WORKLOADS["conv_htiled"]
+    x_np, w_np = S.conv_inputs(wl)
+    x, w = to_cuda(x_np, wl.in_dtype), to_cuda(w_np, wl.in_dtype)
+    big = T.conv_workspace(x, w, (2, 2), (1, 1), (1, 1), 16)
+    assert big.numel() > 8 * 64 * 224 * 224 * 2
+    y1 = T.conv2d_htiled(x, w, (2, 2), (1, 1), (1, 1), 16, workspace=big)
+    y2 = T.conv2d_htiled(x, w, (2, 2), (1, 1), (1, 1), 16, workspace=big,
+                         cfg=T.make_config(128, 256, 64, 4, 192, "tcgen05", 2, 1))
+    T.check(big)
+    assert torch.equal(y1, y2)
+
+
+def test_nhwc_without_workspace_is_refused(ws):
+    x = torch.zeros((1, 8, 8, 16), dtype=torch.float16, device="cuda")
+    w = torch.zeros((4, 16, 3, 3), dtype=torch.float16, device="cuda")
+    with pytest.raises(T.TilesError) as e:
+        T.conv2d_htiled(x, w, (1, 1), (1, 1), (1, 1), 4, workspace=ws, layout="nhwc")
+    assert e.value.status == -4

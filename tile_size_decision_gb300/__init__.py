@@ -17,7 +17,7 @@ from ._abi import TilesError, check as _check
 __all__ = [
     "TilesError", "load", "version", "device_preset", "device_query", "evaluate",
     "finish_parallelism", "c0_bytes", "plan", "htile_rows", "workspace_bytes", "workspace",
-    "gemm", "gemm_batched", "gemm_schedule", "gemm_workspace", "gemm_noalloc", "conv2d_htiled", "check", "selftest_wait_timeout", "make_config",
+    "gemm", "gemm_batched", "gemm_schedule", "gemm_workspace", "gemm_noalloc", "conv2d_htiled", "conv_workspace", "check", "selftest_wait_timeout", "make_config",
 ]
 
 
@@ -206,31 +206,64 @@ def conv_out_hw(h, w, kh, kw, stride, pad, dil):
     return oh, ow
 
 
-def conv2d_htiled(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), tile_oh=16, out=None,
-                  out_dtype=None, cfg=None, workspace=None, stream=None):
-    """NCHW conv2d with OIHW weights as an implicit GEMM per output H-tile."""
+def _conv_desc(x, w, stride, pad, dil, out, layout):
     for t, nm in ((x, "x"), (w, "w")):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{nm} must be a contiguous CUDA tensor")
-    n, c, h, wd = x.shape
+    if layout == "nchw":
+        n, c, h, wd = x.shape
+    elif layout == "nhwc":
+        n, h, wd, c = x.shape
+    else:
+        raise ValueError(f"unknown layout {layout!r}")
     co, c2, kh, kw = w.shape
     if c2 != c:
         raise ValueError("channel mismatch")
-    oh, ow = conv_out_hw(h, wd, kh, kw, stride, pad, dil)
-    if out is None:
-        out = _alloc_out((n, co, oh, ow), x, out_dtype)
-    if not out.is_contiguous() or tuple(out.shape) != (n, co, oh, ow):
-        raise ValueError("out must be contiguous with shape (n, c_out, oh, ow)")
     d = _abi.ConvDesc()
     d.n, d.c, d.h, d.w = n, c, h, wd
     d.c_out, d.kh, d.kw = co, kh, kw
     d.sh, d.sw = stride
     d.ph, d.pw = pad
     d.dh, d.dw = dil
-    d.in_dtype, d.out_dtype = _dtype_code(x), _dtype_code(out)
+    d.in_dtype = _dtype_code(x)
     if _dtype_code(w) != d.in_dtype:
         raise TypeError("x and w must share a dtype")
-    d.x, d.wt, d.y = x.data_ptr(), w.data_ptr(), out.data_ptr()
+    d.x_layout = _abi.LAYOUT_NHWC if layout == "nhwc" else _abi.LAYOUT_NCHW
+    d.x, d.wt = x.data_ptr(), w.data_ptr()
+    if out is not None:
+        d.y = out.data_ptr()
+        d.out_dtype = _dtype_code(out)
+    return d
+
+
+def conv_out_shape(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), layout="nchw"):
+    n, c, h, wd = x.shape if layout == "nchw" else (x.shape[0], x.shape[3], x.shape[1], x.shape[2])
+    co, _, kh, kw = w.shape
+    oh, ow = conv_out_hw(h, wd, kh, kw, stride, pad, dil)
+    return (n, co, oh, ow)
+
+
+def conv_workspace(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), tile_oh=16, layout="nchw"):
+    """A zeroed workspace for the TMA im2col producer of this convolution."""
+    torch = _torch()
+    d = _conv_desc(x, w, stride, pad, dil, None, layout)
+    nbytes = int(load().tiles_conv_workspace_bytes(C.byref(d), tile_oh))
+    if nbytes == 0:
+        raise ValueError("invalid convolution arguments")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=x.device)
+
+
+def conv2d_htiled(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), tile_oh=16, out=None,
+                  out_dtype=None, cfg=None, workspace=None, stream=None, layout="nchw"):
+    """conv2d with OIHW weights and NCHW output, as an implicit GEMM per output
+    H-tile; x is NCHW or NHWC (layout).  With a workspace of conv_workspace
+    size the im2col operand is built by TMA, else gathered by threads."""
+    shape = conv_out_shape(x, w, stride, pad, dil, layout)
+    if out is None:
+        out = _alloc_out(shape, x, out_dtype)
+    if not out.is_contiguous() or tuple(out.shape) != shape:
+        raise ValueError("out must be contiguous with shape (n, c_out, oh, ow)")
+    d = _conv_desc(x, w, stride, pad, dil, out, layout)
     ws = workspace.data_ptr() if workspace is not None else None
     wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().tiles_conv2d_htiled(C.byref(d), tile_oh, _cfg_ptr(cfg), ws, wsb,

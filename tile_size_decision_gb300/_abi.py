@@ -113,7 +113,11 @@ class Schedule(C.Structure):
 class ConvDesc(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "n", "c", "h", "w", "c_out", "kh", "kw", "sh", "sw", "ph", "pw", "dh", "dw",
-        "in_dtype", "out_dtype")] + [("x", C.c_void_p), ("wt", C.c_void_p), ("y", C.c_void_p)]
+        "in_dtype", "out_dtype", "x_layout")] + \
+        [("x", C.c_void_p), ("wt", C.c_void_p), ("y", C.c_void_p)]
+
+
+LAYOUT_NCHW, LAYOUT_NHWC = 0, 1
 
 
 # Every exported entry point: name -> (restype, argtypes).
@@ -144,6 +148,7 @@ SIGNATURES = {
                                       C.c_void_p, C.c_size_t, C.c_void_p]),
     "tiles_gemm_noalloc": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_void_p,
                                      C.c_int]),
+    "tiles_conv_workspace_bytes": (C.c_size_t, [C.POINTER(ConvDesc), C.c_int]),
     "tiles_check": (C.c_int, [C.c_void_p, C.c_void_p]),
     "tiles_selftest_wait_timeout": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
 }

@@ -44,6 +44,7 @@ def units():
         ("planner.cpp", "planner.o", []),
         ("api.cu", "api.o", []),
         ("conv_sm103a.cu", "conv_sm103a.o", []),
+        ("conv_tma_sm103a.cu", "conv_tma_sm103a.o", []),
     ]
     for bn, cg in GEMM_VARIANTS:
         out.append(("gemm_sm103a.cu", f"gemm_bn{bn}_cg{cg}.o",

@@ -602,6 +602,10 @@ int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_co
     return conv2d_htiled(desc, tile_oh, cfg, ws, ws_bytes, stream);
 }
 
+size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh) {
+    return static_cast<size_t>(conv_workspace_bytes(desc, tile_oh));
+}
+
 int tiles_gemm_noalloc(const tiles_gemm_desc* desc, const tiles_config* cfg, void* stream,
                        int wait) {
     if (tiles_workspace_bytes() > kNoAllocScratchBytes)

@@ -309,15 +309,12 @@ int conv2d_htiled(const tiles_conv_desc* d, int tile_oh, const tiles_config* cfg
         return fail(TILES_ERR_UNSUPPORTED_DTYPE, "x and w must be f16 or bf16");
     const int ob = bytes_of(d->out_dtype);
     if (!ob) return fail(TILES_ERR_UNSUPPORTED_DTYPE, "y must be f32, f16 or bf16");
-    if (cfg && (cfg->bm != 128 || cfg->bn != kConvBN || cfg->bk != 64 || cfg->stages != kConvStages ||
-                cfg->cta_group != 1 || cfg->acc_bufs != 2 || cfg->threads != kConvThreads ||
-                cfg->instr != TILES_INSTR_TCGEN05))
-        return fail(TILES_ERR_INFEASIBLE, "the convolution runs the 128x256x64, 4-stage variant");
+    if (d->x_layout != TILES_LAYOUT_NCHW && d->x_layout != TILES_LAYOUT_NHWC)
+        return fail(TILES_ERR_INVALID_ARG, "unknown input layout %d", d->x_layout);
     const int64_t k = static_cast<int64_t>(d->c) * d->kh * d->kw;
-    if (k % 8) return fail(TILES_ERR_MISALIGNED, "c*kh*kw must be a multiple of 8 (weight rows)");
-    if ((reinterpret_cast<uintptr_t>(d->wt) & 15u) || (reinterpret_cast<uintptr_t>(d->x) & 1u) ||
-        (reinterpret_cast<uintptr_t>(d->y) & (ob - 1)))
-        return fail(TILES_ERR_MISALIGNED, "w must be 16-byte aligned, x and y element aligned");
+    if ((reinterpret_cast<uintptr_t>(d->x) & 1u) || (reinterpret_cast<uintptr_t>(d->y) & (ob - 1)) ||
+        (reinterpret_cast<uintptr_t>(d->wt) & 1u))
+        return fail(TILES_ERR_MISALIGNED, "x, w and y must be element aligned");
     const int64_t oh = (static_cast<int64_t>(d->h) + 2 * d->ph - static_cast<int64_t>(d->kh - 1) * d->dh - 1) / d->sh + 1;
     const int64_t ow = (static_cast<int64_t>(d->w) + 2 * d->pw - static_cast<int64_t>(d->kw - 1) * d->dw - 1) / d->sw + 1;
     if (d->h + 2 * d->ph < (d->kh - 1) * d->dh + 1 || d->w + 2 * d->pw < (d->kw - 1) * d->dw + 1 ||
@@ -328,6 +325,24 @@ int conv2d_htiled(const tiles_conv_desc* d, int tile_oh, const tiles_config* cfg
         return fail(TILES_ERR_TOO_LARGE, "tile_oh and the pad must be below 32768");
     if (k > (1 << 24) || tile_cols > (1 << 30) || static_cast<int64_t>(d->n) * d->c * d->h * d->w > (1ll << 40))
         return fail(TILES_ERR_TOO_LARGE, "convolution too large");
+
+    // Producer: the TMA im2col when it applies and the workspace holds its
+    // prepared operands (or when forced), else the thread gather.
+    const bool force_tma = cfg && cfg->threads == kGemmThreads;
+    const bool force_gather = cfg && cfg->threads == kConvThreads;
+    if (cfg && !force_tma && !force_gather)
+        return fail(TILES_ERR_INFEASIBLE, "conv cfg: threads 192 (TMA producer) or 320 (gather)");
+    ConvTmaGeometry g;
+    const bool tma_ok = conv_tma_geometry(d, oh, ow, tile_oh, &g);
+    if (force_tma && !tma_ok)
+        return fail(TILES_ERR_INFEASIBLE, "the TMA producer does not apply to this convolution");
+    if (!force_gather && tma_ok && (force_tma || (ws && static_cast<int64_t>(ws_bytes) >= g.ws_bytes)))
+        return conv2d_tma(d, tile_oh, oh, ow, g, ws, ws_bytes, stream);
+    if (d->x_layout != TILES_LAYOUT_NCHW)
+        return fail(TILES_ERR_INFEASIBLE, "NHWC input needs the TMA producer (and its workspace)");
+    if (k % 8) return fail(TILES_ERR_MISALIGNED, "c*kh*kw must be a multiple of 8 (weight rows)");
+    if (reinterpret_cast<uintptr_t>(d->wt) & 15u)
+        return fail(TILES_ERR_MISALIGNED, "w must be 16-byte aligned");
 
     auto fn = conv_encode_fn();
     if (!fn) return fail(TILES_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (no CUDA driver?)");
@@ -401,6 +416,17 @@ int conv2d_htiled(const tiles_conv_desc* d, int tile_oh, const tiles_config* cfg
         if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "conv launch: %s", cudaGetErrorString(e));
     }
     return TILES_OK;
+}
+
+int64_t conv_workspace_bytes(const tiles_conv_desc* d, int tile_oh) {
+    if (!d || tile_oh < 1 || d->kh < 1 || d->kw < 1 || d->sh < 1 || d->sw < 1 || d->dh < 1 ||
+        d->dw < 1 || d->n < 1 || d->c < 1 || d->h < 1 || d->w < 1 || d->c_out < 1)
+        return 0;
+    const int64_t oh = (static_cast<int64_t>(d->h) + 2 * d->ph - static_cast<int64_t>(d->kh - 1) * d->dh - 1) / d->sh + 1;
+    const int64_t ow = (static_cast<int64_t>(d->w) + 2 * d->pw - static_cast<int64_t>(d->kw - 1) * d->dw - 1) / d->sw + 1;
+    if (oh < 1 || ow < 1) return 0;
+    ConvTmaGeometry g;
+    return conv_tma_geometry(d, oh, ow, tile_oh, &g) ? g.ws_bytes : 256;
 }
 
 }  // namespace tiles

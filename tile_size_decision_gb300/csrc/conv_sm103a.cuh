@@ -12,6 +12,7 @@
 
 #include <cstdint>
 
+#include "gemm_sm103a.cuh"
 #include "tiles_internal.h"
 
 namespace tiles {
@@ -33,6 +34,20 @@ constexpr int kConvMaxHTiles = 128;
 // that gather the im2col operand.
 constexpr int kConvThreads = 320;
 constexpr int kConvGatherThreads = 128;
+
+// Geometry of the TMA convolution (conv_tma_sm103a.cu).
+struct ConvTmaGeometry {
+    int owc, nr, bn;              // tile: nr output rows x owc columns, MMA N = bn
+    int ch_blocks, cp;            // 64-channel blocks, channels padded to them
+    int64_t weights_bytes, x_bytes;
+    int64_t weights_offset, x_offset, ws_bytes;   // workspace layout
+};
+
+bool conv_tma_geometry(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh,
+                       ConvTmaGeometry* g);
+int conv2d_tma(const tiles_conv_desc* d, int tile_oh, int64_t oh, int64_t ow,
+               const ConvTmaGeometry& g, void* ws, size_t ws_bytes, void* stream);
+int64_t conv_workspace_bytes(const tiles_conv_desc* d, int tile_oh);
 
 struct ConvArgs {
     const void* x;

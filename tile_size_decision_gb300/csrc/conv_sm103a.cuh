@@ -37,7 +37,8 @@ constexpr int kConvGatherThreads = 128;
 
 // Geometry of the TMA convolution (conv_tma_sm103a.cu).
 struct ConvTmaGeometry {
-    int owc, nr, bn;              // tile: nr output rows x owc columns, MMA N = bn
+    int owc, nr, bn;              // tile: nr output rows x owc columns (MMA M = 128),
+                                  // bn output channels (MMA N)
     int ch_blocks, cp;            // 64-channel blocks, channels padded to them
     int64_t weights_bytes, x_bytes;
     int64_t weights_offset, x_offset, ws_bytes;   // workspace layout

@@ -118,8 +118,20 @@ typedef struct {
     int32_t acc_bufs;        /* GB300: TMEM accumulator buffers (0 on the page) */
     int32_t cta_group;       /* GB300: 1 or 2 SMs per MMA (0 on the page) */
     int32_t tail;            /* GB300 last-round schedule, tiles_tail (0 = planner's choice) */
-    int32_t reserved[3];
+    int32_t conv_weights;    /* convolution with the TMA producer: where the weights sit,
+                                tiles_conv_weights (0 = tensor memory when they fit) */
+    int32_t reserved[2];
 } tiles_config;
+
+/* Where the TMA convolution keeps the filter (tiles_config.conv_weights).
+ * TMEM: the weights are the MMA's A operand in tensor memory (M = 128
+ * output channels, N = a tile of output pixels); it applies when c_out <=
+ * 128 and the K columns plus two accumulators fit the 512 columns.  SMEM:
+ * the weights are the B operand in shared memory (M = 128 output pixels,
+ * N = a block of output channels); it applies to every TMA convolution. */
+typedef enum {
+    TILES_CONV_W_AUTO = 0, TILES_CONV_W_SMEM = 1, TILES_CONV_W_TMEM = 2
+} tiles_conv_weights;
 
 /* Schedules of a last round of tiles that would leave resident CTA groups
  * idle (constraint C4): as whole tiles, as N-half tiles, or split along K
@@ -327,8 +339,12 @@ int tiles_gemm_batched(const tiles_gemm_desc* desc, const tiles_config* cfg, voi
  *    pads arriving as zero fill;
  *  - gather (NCHW input only; c*kh*kw a multiple of 8): four warps gather
  *    the operand from global memory into shared memory.
+ * With the TMA producer the filter sits in tensor memory as the MMA's A
+ * operand when it fits (tiles_conv_weights), else in shared memory.
  * cfg == NULL picks the TMA producer when the workspace allows; a cfg with
- * threads 192 forces it, threads 320 forces the gather.  tile_oh >= 1. */
+ * threads 192 forces it (cfg->conv_weights then picks the filter's place:
+ * TILES_ERR_INFEASIBLE when TMEM is asked for and it does not fit), threads
+ * 320 forces the gather.  tile_oh >= 1. */
 int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
                         void* workspace, size_t ws_bytes, void* stream);
 

@@ -32,10 +32,19 @@ def ws():
     return T.workspace()
 
 
+def tmem_fits(c, co, kh, kw):
+    # The weights-in-tensor-memory form: one 128-channel output block and
+    # kh*kw*ceil(c/64) K blocks of 32 columns next to two 16-column
+    # accumulators in 512 columns.
+    return co <= 128 and kh * kw * ((c + 63) // 64) * 32 + 32 <= 512
+
+
 def run_conv(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, ws, guard=0, producer="gather",
              layout="nchw"):
     # producer "gather": the small workspace (threads gather the operand);
-    # "tma": a workspace sized for the TMA producer.
+    # "tma": a workspace sized for the TMA producer, weights where they fit
+    # best; "tma_smem" / "tma_tmem" force the weights into shared or tensor
+    # memory, "tma_tmem1" / "tma_tmem2" also fix one or two accumulators.
     x = to_cuda(x_np, in_dt)
     if layout == "nhwc":
         x = x.permute(0, 2, 3, 1).contiguous()
@@ -47,9 +56,12 @@ def run_conv(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, ws, guard=0, 
     total = n * co * oh * ow
     flat = torch.full((total + 2 * guard,), 2048.0, dtype=TORCH_DT[out_dt], device="cuda")
     y = flat[guard:guard + total].view(n, co, oh, ow)
-    if producer == "tma":
+    if producer.startswith("tma"):
         ws = T.conv_workspace(x, w, stride, pad, dil, tile_oh, layout=layout)
-        cfg = T.make_config(128, 256, 64, 4, 192, "tcgen05", 2, 1)
+        place = producer[4:] or "auto"
+        acc = int(place[4:]) if place.startswith("tmem") and len(place) > 4 else 0
+        cfg = T.make_config(128, 256, 64, 4, 192, "tcgen05", acc, 1,
+                            conv_weights=place[:4] if place != "auto" else "auto")
     else:
         cfg = None
     T.conv2d_htiled(x, w, stride, pad, dil, tile_oh, out=y, workspace=ws, cfg=cfg, layout=layout)
@@ -150,13 +162,19 @@ def test_rejects_unaligned_weights(ws):
 # The TMA im2col producer
 # --------------------------------------------------------------------------- #
 
+PLACES = ["smem", "tmem1", "tmem2"]
+
+
 @pytest.mark.parametrize("case", TINY, ids=lambda c: "_".join(str(v) for v in c[:7]))
 @pytest.mark.parametrize("layout", ["nchw", "nhwc"])
-def test_tma_tiny_against_loops(ws, case, layout):
+@pytest.mark.parametrize("place", PLACES)
+def test_tma_tiny_against_loops(ws, case, layout, place):
     n, c, h, wd, co, kh, kw, st, pad, dil, tile = case
+    if place.startswith("tmem") and not tmem_fits(c, co, kh, kw):
+        pytest.skip("filter does not fit tensor memory")
     x = S.random_matrix(1, (n, c, h, wd), S.F16)
     w = S.random_matrix(2, (co, c, kh, kw), S.F16)
-    got = run_conv(x, w, S.F16, S.F32, st, pad, dil, tile, ws, guard=64, producer="tma",
+    got = run_conv(x, w, S.F16, S.F32, st, pad, dil, tile, ws, guard=64, producer="tma_" + place,
                    layout=layout)
     x64, w64 = S.widen(x, S.F16), S.widen(w, S.F16)
     if n * co * c * h * wd < 200000:
@@ -168,18 +186,23 @@ def test_tma_tiny_against_loops(ws, case, layout):
 
 
 @pytest.mark.parametrize("dt", [S.F16, S.BF16])
-def test_tma_integer_inputs_exact(ws, dt):
-    x = S.integer_matrix(3, (2, 72, 30, 28), dt)
-    w = S.integer_matrix(4, (40, 72, 3, 3), dt)
-    got = run_conv(x, w, dt, S.F32, (2, 2), (1, 1), (1, 1), 4, ws, producer="tma")
+@pytest.mark.parametrize("place", PLACES)
+def test_tma_integer_inputs_exact(ws, dt, place):
+    # 72 channels are 18 K blocks, more than tensor memory holds next to
+    # the accumulators; the TMEM form takes 48 (one zero-padded block).
+    c = 72 if place == "smem" else 48
+    x = S.integer_matrix(3, (2, c, 30, 28), dt)
+    w = S.integer_matrix(4, (40, c, 3, 3), dt)
+    got = run_conv(x, w, dt, S.F32, (2, 2), (1, 1), (1, 1), 4, ws, producer="tma_" + place)
     ref = OC.conv2d(S.widen(x, dt), S.widen(w, dt), (2, 2), (1, 1), (1, 1))
     assert np.array_equal(got, ref)
 
 
-def test_tma_tile_height_does_not_change_bits(ws):
+@pytest.mark.parametrize("place", PLACES)
+def test_tma_tile_height_does_not_change_bits(ws, place):
     x = S.random_matrix(5, (2, 16, 37, 34), S.BF16, "normal")
     w = S.random_matrix(6, (64, 16, 3, 3), S.BF16, "normal")
-    outs = [run_conv(x, w, S.BF16, S.F32, (2, 1), (1, 1), (1, 1), t, ws, producer="tma")
+    outs = [run_conv(x, w, S.BF16, S.F32, (2, 1), (1, 1), (1, 1), t, ws, producer="tma_" + place)
             for t in (1, 2, 3, 7, 19, 40)]
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
@@ -187,12 +210,14 @@ def test_tma_tile_height_does_not_change_bits(ws):
                          S.F32)
 
 
-def test_tma_wide_rows_and_many_h_tiles(ws):
+@pytest.mark.parametrize("place", PLACES)
+def test_tma_wide_rows_and_many_h_tiles(ws, place):
     # W wider than one TMA box (several column blocks) and 300 output rows at
     # tile height 1 (three launches of H-tiles).
     x = S.random_matrix(7, (1, 8, 300, 600), S.F16)
     w = S.random_matrix(8, (12, 8, 3, 3), S.F16)
-    got = run_conv(x, w, S.F16, S.F16, (1, 2), (1, 1), (1, 1), 1, ws, guard=32, producer="tma")
+    got = run_conv(x, w, S.F16, S.F16, (1, 2), (1, 1), (1, 1), 1, ws, guard=32,
+                   producer="tma_" + place)
     check_against_oracle(got, S.widen(x, S.F16), S.widen(w, S.F16), (1, 2), (1, 1), (1, 1), S.F16)
 
 
@@ -205,11 +230,12 @@ def test_tma_channels_not_multiple_of_64(ws):
 
 
 @pytest.mark.parametrize("layout", ["nchw", "nhwc"])
-def test_tma_conv_workload_full(ws, layout):
+@pytest.mark.parametrize("place", PLACES)
+def test_tma_conv_workload_full(ws, layout, place):
     wl = S.WORKLOADS["conv_htiled"]
     x, w = S.conv_inputs(wl)
     got = run_conv(x, w, wl.in_dtype, wl.out_dtype, (wl.sh, wl.sw), (wl.ph, wl.pw),
-                   (wl.dh, wl.dw), wl.tile_oh, ws, producer="tma", layout=layout)
+                   (wl.dh, wl.dw), wl.tile_oh, ws, producer="tma_" + place, layout=layout)
     check_against_oracle(got, S.widen(x, wl.in_dtype), S.widen(w, wl.in_dtype), (wl.sh, wl.sw),
                          (wl.ph, wl.pw), (wl.dh, wl.dw), wl.out_dtype)
 
@@ -228,6 +254,31 @@ def test_default_producer_with_workspace_is_tma(ws):
                          cfg=T.make_config(128, 256, 64, 4, 192, "tcgen05", 2, 1))
     T.check(big)
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("out_dt", [S.F16, S.BF16, S.F32])
+@pytest.mark.parametrize("place", ["tmem", "tmem1", "tmem2"])
+def test_tmem_weights_ragged_channels_and_columns(ws, out_dt, place):
+    # c_out below 128 (zero rows of the tensor-memory filter), a channel
+    # count that is not a multiple of 64, odd output widths (scalar tails)
+    # and stride 1 and 3.
+    for seed, (n, c, h, wd, co, st) in enumerate([(2, 24, 19, 27, 72, 1), (1, 56, 23, 41, 100, 3)]):
+        x = S.random_matrix(20 + seed, (n, c, h, wd), S.BF16, "normal")
+        w = S.random_matrix(30 + seed, (co, c, 3, 3), S.BF16, "normal")
+        got = run_conv(x, w, S.BF16, out_dt, (st, st), (1, 1), (1, 1), 5, ws, guard=16,
+                       producer="tma_" + place)
+        check_against_oracle(got, S.widen(x, S.BF16), S.widen(w, S.BF16), (st, st), (1, 1),
+                             (1, 1), out_dt)
+
+
+def test_tmem_weights_refused_when_they_do_not_fit(ws):
+    x = torch.zeros((1, 64, 8, 8), dtype=torch.float16, device="cuda")
+    w = torch.zeros((200, 64, 3, 3), dtype=torch.float16, device="cuda")   # c_out > 128
+    big = T.conv_workspace(x, w, (1, 1), (1, 1), (1, 1), 4)
+    with pytest.raises(T.TilesError) as e:
+        T.conv2d_htiled(x, w, (1, 1), (1, 1), (1, 1), 4, workspace=big,
+                        cfg=T.make_config(128, 256, 64, 4, 192, "tcgen05", 2, 1, conv_weights="tmem"))
+    assert e.value.status == -4
 
 
 def test_nhwc_without_workspace_is_refused(ws):

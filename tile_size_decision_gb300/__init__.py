@@ -42,17 +42,19 @@ def device_query(ordinal: int = 0) -> _abi.Device:
     return d
 
 
+CONV_WEIGHTS = {"auto": _abi.CONV_W_AUTO, "smem": _abi.CONV_W_SMEM, "tmem": _abi.CONV_W_TMEM}
 TAILS = {"auto": _abi.TAIL_AUTO, "whole": _abi.TAIL_WHOLE, "nhalf": _abi.TAIL_NHALF,
          "ksplit": _abi.TAIL_KSPLIT}
 
 
 def make_config(bm, bn, bk, stages=3, threads=128, instr="wgmma", acc_bufs=0,
-                cta_group=0, tail="auto") -> _abi.Config:
+                cta_group=0, tail="auto", conv_weights="auto") -> _abi.Config:
     c = _abi.Config()
     c.bm, c.bn, c.bk, c.stages, c.threads = bm, bn, bk, stages, threads
     c.instr = _abi.INSTR_CODES[instr] if isinstance(instr, str) else instr
     c.acc_bufs, c.cta_group = acc_bufs, cta_group
     c.tail = TAILS[tail] if isinstance(tail, str) else tail
+    c.conv_weights = CONV_WEIGHTS[conv_weights] if isinstance(conv_weights, str) else conv_weights
     return c
 
 

@@ -51,11 +51,12 @@ class Device(C.Structure):
 
 class Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
-        "bm", "bn", "bk", "stages", "threads", "instr", "acc_bufs", "cta_group", "tail")] + \
-        [("reserved", C.c_int32 * 3)]
+        "bm", "bn", "bk", "stages", "threads", "instr", "acc_bufs", "cta_group", "tail",
+        "conv_weights")] + [("reserved", C.c_int32 * 2)]
 
 
 TAIL_AUTO, TAIL_WHOLE, TAIL_NHALF, TAIL_KSPLIT = 0, 1, 2, 3
+CONV_W_AUTO, CONV_W_SMEM, CONV_W_TMEM = 0, 1, 2
 
 
 class Verdict(C.Structure):

@@ -337,7 +337,7 @@ int conv2d_htiled(const tiles_conv_desc* d, int tile_oh, const tiles_config* cfg
     if (force_tma && !tma_ok)
         return fail(TILES_ERR_INFEASIBLE, "the TMA producer does not apply to this convolution");
     if (!force_gather && tma_ok && (force_tma || (ws && static_cast<int64_t>(ws_bytes) >= g.ws_bytes)))
-        return conv2d_tma(d, tile_oh, oh, ow, g, ws, ws_bytes, stream);
+        return conv2d_tma(d, cfg, tile_oh, oh, ow, g, ws, ws_bytes, stream);
     if (d->x_layout != TILES_LAYOUT_NCHW)
         return fail(TILES_ERR_INFEASIBLE, "NHWC input needs the TMA producer (and its workspace)");
     if (k % 8) return fail(TILES_ERR_MISALIGNED, "c*kh*kw must be a multiple of 8 (weight rows)");

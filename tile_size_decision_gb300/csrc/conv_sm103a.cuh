@@ -46,8 +46,10 @@ struct ConvTmaGeometry {
 
 bool conv_tma_geometry(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh,
                        ConvTmaGeometry* g);
-int conv2d_tma(const tiles_conv_desc* d, int tile_oh, int64_t oh, int64_t ow,
-               const ConvTmaGeometry& g, void* ws, size_t ws_bytes, void* stream);
+// cfg (may be NULL): conv_weights picks the filter's place, acc_bufs the
+// TMEM accumulator count of the weights-in-TMEM form (0 = planned).
+int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, int64_t oh,
+               int64_t ow, const ConvTmaGeometry& g, void* ws, size_t ws_bytes, void* stream);
 int64_t conv_workspace_bytes(const tiles_conv_desc* d, int tile_oh);
 
 struct ConvArgs {

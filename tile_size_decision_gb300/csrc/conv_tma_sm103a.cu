@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cudaTypedefs.h>
 
 #include "conv_sm103a.cuh"
@@ -51,6 +52,17 @@ struct ConvTmaArgs {
     uint32_t idesc;
     int32_t* err;
     uint64_t wait_limit_ns;
+    // Weights in tensor memory (conv_wtmem_kernel): the reordered weights,
+    // their row length kh*kw*Cp, the pixels of a tile (MMA N), the first
+    // TMEM column of the weights (after the accumulators) and the shared-
+    // memory layout.
+    const uint16_t* wr;
+    int32_t kp, npix, a_col;
+    int32_t acc_bufs;                     // TMEM accumulators (1 or 2)
+    int32_t stages;                       // pixel-box ring depth
+    int32_t stg_off, stg_pitch;           // staging tile: offset and row pitch (bytes)
+    int32_t bar_off;                      // barrier block offset (bytes)
+    int32_t w_slots;                      // 16 KB filter blocks per start-up pass
     ConvHTile ht[kConvMaxHTiles];
 };
 
@@ -366,6 +378,416 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Weights in tensor memory.  For c_out <= 128 and a short K the whole filter
+// fits in TMEM (K/2 columns: two 16-bit values per column) beside one or two
+// accumulators, so it is the MMA's A operand for the kernel's lifetime:
+// M = 128 output channels on the TMEM lanes, N = npix output pixels (nr rows
+// x owc columns), K = (r, s, ci).  Per K block only the pixel box crosses
+// shared memory.  One tcgen05.mma costs the issuing thread a roughly fixed
+// time, so wide pixel tiles (N up to 256 with a single accumulator) keep the
+// tensor core busy; with two accumulators the epilogue overlaps the next
+// tile's MMAs at half the width.
+//
+// Warps: 0 TMA producer, 1 MMA issuer, 2-9 epilogue.
+//  - Start: the producer TMA-loads the reordered filter into the (still
+//    unused) shared memory, in passes of as many 16 KB K blocks as fit; the
+//    epilogue warps copy each block's rows into tensor memory (warp w owns
+//    lanes 32*(w%4) .. +31 and every other K block) and release the space.
+//  - Per tile: the epilogue warps read the accumulator (a thread = one output
+//    channel, npix/2 consecutive pixels), write it as 16-bit or fp32 rows to
+//    a shared staging tile whose row pitch is an odd number of 16-byte
+//    chunks (no bank conflicts), then store the tile row-contiguously to the
+//    NCHW output: consecutive threads write consecutive 16 bytes.
+constexpr int kWtThreads = 320;
+constexpr int kWtEpilogueWarps = 8;
+constexpr int kWtEpilogueThreads = kWtEpilogueWarps * 32;
+constexpr int kWtTmemCols = 512;
+constexpr int kWtWeightBlockBytes = 128 * 128;   // 128 rows x 64 channels x 2 bytes
+
+struct WtBarriers {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint64_t wfull;      // a pass of filter blocks landed in shared memory
+    uint64_t wcons;      // the epilogue warps copied that pass to tensor memory
+    uint64_t wready;     // the whole filter is in tensor memory
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(WtBarriers) <= kSmemBarrierBytes, "barrier block");
+
+// Named barrier 1 over the epilogue warps, and the same barrier returning
+// the AND of every thread's flag (one answer for all, so the warps take the
+// same branch after it).
+__device__ __forceinline__ void epilogue_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(kWtEpilogueThreads) : "memory");
+}
+__device__ __forceinline__ bool epilogue_bar_and(bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(flag ? 1u : 0u), "r"(kWtEpilogueThreads) : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(kWtThreads, 1)
+    conv_wtmem_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                      const __grid_constant__ ConvTmaArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    // [stages x pixel box][staging tile][barriers]; at the start the filter
+    // passes use [0, w_slots x 16 KB) of the first two.
+    uint8_t* ring = base;
+    uint8_t* staging = base + args.stg_off;
+    WtBarriers* bar = reinterpret_cast<WtBarriers*>(base + args.bar_off);
+    const int stages = args.stages;
+    const uint32_t stage_bytes = static_cast<uint32_t>(args.npix) * 128u;
+    const int passes = (args.k_blocks + args.w_slots - 1) / args.w_slots;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            ptx::mbar_init(&bar->full[s], 1);
+            ptx::mbar_init(&bar->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&bar->acc_full[a], 1);
+            ptx::mbar_init(&bar->acc_empty[a], kWtEpilogueWarps);
+        }
+        ptx::mbar_init(&bar->drain, 1);
+        ptx::mbar_init(&bar->wfull, 1);
+        ptx::mbar_init(&bar->wcons, kWtEpilogueWarps);
+        ptx::mbar_init(&bar->wready, kWtEpilogueWarps);
+        bar->abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tmW);
+        ptx::tma_prefetch_desc(&tmX);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<1>(&bar->tmem_base, kWtTmemCols);
+        ptx::tmem_relinquish<1>();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    const uint32_t tmem = bar->tmem_base;
+    volatile int* abort = &bar->abort;
+    const uint64_t limit = args.wait_limit_ns;
+    const bool has_work = static_cast<int>(blockIdx.x) < args.units;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool aborted = false;
+            // ---------------- the filter, pass by pass ----------------
+            for (int p = 0; p < passes && has_work; ++p) {
+                if (p > 0 && !ptx::mbar_wait(&bar->wcons, (p - 1) & 1, abort, limit)) {
+                    raise_error(args.err, abort, kErrProducer);
+                    aborted = true;
+                    break;
+                }
+                const int kb0 = p * args.w_slots;
+                const int nkb = min(args.w_slots, args.k_blocks - kb0);
+                ptx::mbar_arrive_expect_tx(&bar->wfull, static_cast<uint32_t>(nkb * kWtWeightBlockBytes));
+                for (int i = 0; i < nkb; ++i)
+                    ptx::tma_load_3d(base + i * kWtWeightBlockBytes, &tmW, &bar->wfull,
+                                     (kb0 + i) * 64, 0, 0);
+            }
+            // The pixel boxes reuse that space once the last pass is copied.
+            if (!aborted && has_work && !ptx::mbar_wait(&bar->wcons, (passes - 1) & 1, abort, limit)) {
+                raise_error(args.err, abort, kErrProducer);
+                aborted = true;
+            }
+            // ---------------- TMA producer: one pixel box per K block ----------------
+            uint32_t stage = 0, phase = 0;
+            int issued = 0;
+            for (int u = blockIdx.x; u < args.units && !aborted; u += gridDim.x) {
+                const ConvUnit cu = decode_conv_unit(u, args);
+                const ConvHTile ht = args.ht[cu.ht];
+                const int row0 = ht.in_start - ht.pt + cu.rb * args.nr * args.sh;
+                const int col0 = cu.cb * args.owc * args.sw - args.pw;
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    const int tap = kb / args.ch_blocks;
+                    const int chb = kb - tap * args.ch_blocks;
+                    const int r = tap / args.kw;
+                    const int s = tap - r * args.kw;
+                    if (!ptx::mbar_wait(&bar->empty[stage], phase ^ 1u, abort, limit)) {
+                        raise_error(args.err, abort, kErrProducer);
+                        aborted = true;
+                        break;
+                    }
+                    uint8_t* st = ring + stage * stage_bytes;
+                    ptx::mbar_arrive_expect_tx(&bar->full[stage], args.tx_bytes);
+                    tma_load_4d(st, &tmX, &bar->full[stage], chb * 64, col0 + s * args.dw,
+                                row0 + r * args.dh, cu.img);
+                    ++issued;
+                    if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (aborted) {
+                settle_after_abort();
+            } else {
+                for (int i = 0; i < (issued < stages ? issued : stages); ++i) {
+                    if (stage == 0) { stage = stages - 1; phase ^= 1u; } else { --stage; }
+                    ptx::mbar_wait(&bar->full[stage], phase, nullptr, limit);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = !has_work || ptx::mbar_wait(&bar->wready, 0, abort, limit);
+            if (!ok) raise_error(args.err, abort, kErrMma);
+            ptx::tc_fence_after();
+            for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+                if (!ptx::mbar_wait(&bar->acc_empty[acc], acc_phase ^ 1u, abort, limit)) {
+                    raise_error(args.err, abort, kErrMma);
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d = tmem + acc * static_cast<uint32_t>(args.npix);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!ptx::mbar_wait(&bar->full[stage], phase, abort, limit)) {
+                        raise_error(args.err, abort, kErrMma);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t b0 = ptx::smem_addr(ring + stage * stage_bytes);
+                    const uint32_t a0 = tmem + static_cast<uint32_t>(args.a_col + kb * 32);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // 16 channels: 8 TMEM columns of A, 32 bytes of each
+                        // 128-byte pixel row of B.
+                        const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                        ptx::mma_f16_tmem_a(d, a0 + kk * 8, bd, args.idesc, (kb | kk) != 0);
+                    }
+                    ptx::mma_commit<1>(&bar->empty[stage]);
+                    if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::mma_commit<1>(&bar->acc_full[acc]);
+                if (args.acc_bufs == 2) acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            ptx::mma_commit_local<1>(&bar->drain);
+            ptx::mbar_wait(&bar->drain, 0, nullptr, limit);
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int et = threadIdx.x - 64;                // 0 .. 255
+        const int co = quarter * 32 + lane;             // output channel = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        // ---------------- the filter into tensor memory ----------------
+        bool ok = true;
+        for (int p = 0; p < passes && has_work; ++p) {
+            ok = ptx::mbar_wait(&bar->wfull, p & 1, abort, limit);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) raise_error(args.err, abort, kErrEpilogue);
+                ok = false;
+                break;
+            }
+            const int kb0 = p * args.w_slots;
+            const int nkb = min(args.w_slots, args.k_blocks - kb0);
+            for (int i = half; i < nkb; i += 2) {
+                // Row co of a 128-byte-swizzled block: 16-byte chunk j sits
+                // at chunk j ^ (co & 7).
+                const uint8_t* row = base + i * kWtWeightBlockBytes + co * 128;
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 t = *reinterpret_cast<const uint4*>(row + ((j ^ (co & 7)) << 4));
+                    v[4 * j + 0] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+                }
+                ptx::tmem_st_32cols(tmem + lane_base + static_cast<uint32_t>(args.a_col + (kb0 + i) * 32), v);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar->wcons);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (has_work && ok && lane == 0) ptx::mbar_arrive(&bar->wready);
+        // Every epilogue warp enters the tile loop, or none does.
+        ok = epilogue_bar_and(ok);
+        // ---------------- epilogue ----------------
+        const int ob = args.out_dtype == TILES_F32 ? 4 : 2;
+        const bool bf16_out = args.out_dtype == TILES_BF16;
+        const int col_begin = half * (args.npix >> 1);
+        const int col_end = col_begin + (args.npix >> 1);
+        const int64_t plane = static_cast<int64_t>(args.oh) * args.ow;
+        // Output chunks of 16 bytes: per (channel, pixel row) owc*ob/16.
+        const int seg_chunks = args.owc * ob / 16;
+        const int tile_chunks = 128 * args.nr * seg_chunks;
+        const int ch_elems = 16 / ob;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+            const ConvUnit cu = decode_conv_unit(u, args);
+            const bool okw = ptx::mbar_wait(&bar->acc_full[acc], acc_phase, abort, limit);
+            // One decision for all epilogue warps; passing this barrier also
+            // means the previous tile's stores have read the staging tile.
+            if (!epilogue_bar_and(okw)) {
+                if (et == 0) raise_error(args.err, abort, kErrEpilogue);
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t tacc = tmem + lane_base + acc * static_cast<uint32_t>(args.npix);
+            uint8_t* srow = staging + co * args.stg_pitch;
+#pragma unroll 1
+            for (int c0 = col_begin; c0 < col_end; c0 += 32) {
+                const int groups = (col_end - c0) >= 32 ? 4 : (col_end - c0) >> 3;
+                uint32_t v[32];
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    if (g < groups)
+                        ptx::tmem_ld_8cols(tacc + c0 + 8 * g, v[8 * g + 0], v[8 * g + 1],
+                                           v[8 * g + 2], v[8 * g + 3], v[8 * g + 4],
+                                           v[8 * g + 5], v[8 * g + 6], v[8 * g + 7]);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (g >= groups) continue;
+                    if (ob == 2) {
+                        uint4 t;
+                        t.x = pack_half2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]), bf16_out);
+                        t.y = pack_half2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]), bf16_out);
+                        t.z = pack_half2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]), bf16_out);
+                        t.w = pack_half2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]), bf16_out);
+                        *reinterpret_cast<uint4*>(srow + (c0 + 8 * g) * 2) = t;
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(srow + (c0 + 8 * g) * 4);
+                        dst[0] = make_uint4(v[8 * g + 0], v[8 * g + 1], v[8 * g + 2], v[8 * g + 3]);
+                        dst[1] = make_uint4(v[8 * g + 4], v[8 * g + 5], v[8 * g + 6], v[8 * g + 7]);
+                    }
+                }
+            }
+            // The accumulator is free once this warp's loads have returned.
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar->acc_empty[acc]);
+            if (args.acc_bufs == 2) acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+            epilogue_bar_sync();
+            // Staging tile -> NCHW output, 16 bytes per thread per step.
+            const ConvHTile ht = args.ht[cu.ht];
+            const int oh0 = ht.o0 + cu.rb * args.nr;
+            const int oh_end = ht.o0 + ht.rows;
+            const int ow0 = cu.cb * args.owc;
+            for (int i = et; i < tile_chunks; i += kWtEpilogueThreads) {
+                const int j = i % seg_chunks;
+                const int seg = i / seg_chunks;
+                const int rr = seg % args.nr;
+                const int c = seg / args.nr;
+                const int oh = oh0 + rr;
+                const int ow = ow0 + j * ch_elems;
+                if (c >= args.c_out || oh >= oh_end || ow >= args.ow) continue;
+                const uint8_t* src = staging + c * args.stg_pitch + (rr * args.owc + j * ch_elems) * ob;
+                const uint4 t = *reinterpret_cast<const uint4*>(src);
+                const int64_t idx = (static_cast<int64_t>(cu.img) * args.c_out + c) * plane +
+                                    static_cast<int64_t>(oh) * args.ow + ow;
+                char* dst = static_cast<char*>(args.y) + idx * ob;
+                if (args.vec_ok && ow + ch_elems <= args.ow) {
+                    *reinterpret_cast<uint4*>(dst) = t;
+                } else {
+                    const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (e >= ch_elems || ow + e >= args.ow) continue;
+                        if (ob == 2)
+                            reinterpret_cast<uint16_t*>(dst)[e] =
+                                static_cast<uint16_t>(w4[e >> 1] >> ((e & 1) * 16));
+                        else
+                            reinterpret_cast<uint32_t*>(dst)[e] = w4[e & 3];
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<1>(tmem, kWtTmemCols);
+    }
+}
+
+// NCHW -> NHWC for 16-bit elements with 16-byte accesses on both sides (C
+// and W multiples of 8, x 16-byte aligned), fused with the weight reorder.
+// A warp moves 64 channels x 32 columns of one (image, row): lane (cg, q)
+// loads channels 8cg..8cg+7 at columns 8q..8q+7 as eight 16-byte words,
+// transposes the 8 x 8 block with byte permutes and stores eight pixels of
+// 8 channels.  For a fixed register a warp reads 8 runs of 64 bytes and
+// writes 4 runs of 128 bytes.  Blocks past the transpose reorder the
+// weights as reorder_weights_kernel does.
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+
+__global__ void __launch_bounds__(256)
+    conv_prep_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xt, int C, int H,
+                     int W, int64_t items, unsigned transpose_blocks,
+                     const uint16_t* __restrict__ w, uint16_t* __restrict__ wr, int Cp, int kh,
+                     int kw, int64_t w_total) {
+    if (blockIdx.x >= transpose_blocks) {
+        const int64_t i = static_cast<int64_t>(blockIdx.x - transpose_blocks) * 256 + threadIdx.x;
+        if (i >= w_total) return;
+        const int ci = static_cast<int>(i % Cp);
+        int64_t t = i / Cp;
+        const int s = static_cast<int>(t % kw);
+        t /= kw;
+        const int r = static_cast<int>(t % kh);
+        const int64_t co = t / kh;
+        wr[i] = ci < C ? w[((co * C + ci) * kh + r) * kw + s] : static_cast<uint16_t>(0);
+        return;
+    }
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (item >= items) return;
+    const int lane = threadIdx.x & 31;
+    const int wblks = (W + 31) >> 5, cblks = (C + 63) >> 6;
+    int64_t t = item;
+    const int wb = static_cast<int>(t % wblks);
+    t /= wblks;
+    const int cb = static_cast<int>(t % cblks);
+    t /= cblks;
+    const int h = static_cast<int>(t % H);
+    const int64_t n = t / H;
+    const int c = cb * 64 + (lane & 7) * 8;
+    const int w0 = wb * 32 + (lane >> 3) * 8;
+    if (c >= C || w0 >= W) return;     // whole octets: C and W are multiples of 8
+    const int64_t plane = static_cast<int64_t>(H) * W;
+    const uint16_t* src = x + ((n * C + c) * H + h) * static_cast<int64_t>(W) + w0;
+    uint4 r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[j] = __ldg(reinterpret_cast<const uint4*>(src + j * plane));
+    uint16_t* dst = xt + ((n * H + h) * static_cast<int64_t>(W) + w0) * C + c;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        // Pixel p: channel pairs (2i, 2i+1) from word p/2 of rows 2i, 2i+1.
+        const uint32_t sel = (p & 1) ? 0x7632u : 0x5410u;
+        uint4 o;
+        o.x = __byte_perm(word_of(r[0], p >> 1), word_of(r[1], p >> 1), sel);
+        o.y = __byte_perm(word_of(r[2], p >> 1), word_of(r[3], p >> 1), sel);
+        o.z = __byte_perm(word_of(r[4], p >> 1), word_of(r[5], p >> 1), sel);
+        o.w = __byte_perm(word_of(r[6], p >> 1), word_of(r[7], p >> 1), sel);
+        *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(p) * C) = o;
+    }
+}
+
 // NCHW -> NHWC for 16-bit elements, one 64-channel x 64-column tile of one
 // (image, row) per block.  PAIRS moves 32-bit pairs on both sides (W even;
 // C is a multiple of 8), else single elements.
@@ -470,33 +892,111 @@ bool conv_tma_geometry(const tiles_conv_desc* d, int64_t oh, int64_t ow, int til
     return true;
 }
 
-int conv2d_tma(const tiles_conv_desc* d, int tile_oh, int64_t oh, int64_t ow,
-               const ConvTmaGeometry& g, void* ws, size_t ws_bytes, void* stream) {
+// Geometry and shared-memory layout of the weights-in-TMEM kernel.
+struct WtPlan {
+    int owc = 0, nr = 0, acc_bufs = 0, stages = 0;
+    int stg_pitch = 0, stg_bytes = 0, w_slots = 0, smem = 0;
+};
+
+// Pixel tile owc (a multiple of 8) x nr with npix = owc * nr a multiple of
+// 16; acc_bufs accumulators of npix columns beside the k_blocks * 32 filter
+// columns.  Time model per tile: each K block issues 4 MMAs of npix/2 clocks
+// but no faster than ~345 issue clocks (4 MMAs + 1 commit, measured), plus,
+// with one accumulator, the drain before the next tile (2 * npix + 400);
+// tiles run in rounds over the SMs.  forced_acc = 1 or 2 fixes the count.
+// False when the filter does not fit.
+bool wtmem_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, int64_t k_blocks,
+                int sms, int forced_acc, WtPlan* out) {
+    if (d->c_out > 128) return false;
+    const int64_t a_cols = k_blocks * 32;
+    const int ob = d->out_dtype == TILES_F32 ? 4 : 2;
+    const int budget = 227 * 1024 - kSmemBarrierBytes - kSmemAlignSlack;
+    const int64_t rows = std::min<int64_t>(tile_oh, oh);
+    const int64_t n_ht = (oh + tile_oh - 1) / tile_oh;
+    int64_t best = -1;
+    for (int acc = 1; acc <= 2; ++acc) {
+        if (forced_acc && acc != forced_acc) continue;
+        const int64_t nmax = std::min<int64_t>(256, (kWtTmemCols - a_cols) / acc) / 16 * 16;
+        for (int owc = 8; owc <= nmax && owc * d->sw <= 256; owc += 8) {
+            for (int nr = 1; owc * nr <= nmax && nr * d->sh <= 256; ++nr) {
+                const int npix = owc * nr;
+                if (npix % 16) continue;
+                const int pitch = npix * ob + 16;
+                const int stg = 128 * pitch;
+                const int stage = npix * 128;
+                const int stages = std::min(kMaxStages, (budget - stg) / stage);
+                if (stages < 2) continue;
+                const int64_t units = static_cast<int64_t>(d->n) * n_ht * ((rows + nr - 1) / nr) *
+                                      ((ow + owc - 1) / owc);
+                const int64_t per_unit = k_blocks * std::max<int64_t>(2 * npix, 345) +
+                                         (acc == 1 ? 2 * npix + 400 : 0);
+                const int64_t cost = (units + sms - 1) / sms * per_unit;
+                if (best < 0 || cost < best || (cost == best && owc > out->owc)) {
+                    best = cost;
+                    out->owc = owc;
+                    out->nr = nr;
+                    out->acc_bufs = acc;
+                    out->stages = stages;
+                    out->stg_pitch = pitch;
+                    out->stg_bytes = stg;
+                    out->w_slots = (stages * stage + stg) / kWtWeightBlockBytes;
+                    // At least half an SM's shared memory, so that one block
+                    // (and one 512-column TMEM allocation) sits on each SM.
+                    out->smem = std::max(stages * stage + stg + kSmemBarrierBytes + kSmemAlignSlack,
+                                         116 * 1024);
+                }
+            }
+        }
+    }
+    return best >= 0;
+}
+
+// cudaFuncSetAttribute once per kernel and size.
+cudaError_t set_smem_attr(const void* fn, std::atomic<int>* cached, int smem) {
+    if (cached->load(std::memory_order_relaxed) == smem) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) cached->store(smem, std::memory_order_relaxed);
+    return e;
+}
+std::atomic<int> g_smem_wtmem{0}, g_smem_tma{0};
+
+int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, int64_t oh,
+               int64_t ow, const ConvTmaGeometry& g, void* ws, size_t ws_bytes, void* stream) {
+    const int weights_mode = cfg ? cfg->conv_weights : TILES_CONV_W_AUTO;
     if (!ws || static_cast<int64_t>(ws_bytes) < g.ws_bytes)
         return fail(TILES_ERR_INVALID_ARG, "the TMA convolution needs %lld workspace bytes",
                     (long long)g.ws_bytes);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) || (reinterpret_cast<uintptr_t>(d->x) & 15u))
         return fail(TILES_ERR_MISALIGNED, "workspace must be 256-byte and x 16-byte aligned");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (weights_mode < TILES_CONV_W_AUTO || weights_mode > TILES_CONV_W_TMEM)
+        return fail(TILES_ERR_INVALID_ARG, "conv_weights must be auto, smem or tmem");
+    const int forced_acc = cfg ? cfg->acc_bufs : 0;
+    if (weights_mode == TILES_CONV_W_TMEM && (forced_acc < 0 || forced_acc > 2))
+        return fail(TILES_ERR_INVALID_ARG, "acc_bufs must be 0 (auto), 1 or 2");
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+
+    // ---- the whole launch is planned before the first kernel goes out ----
+    const int64_t k_blocks = static_cast<int64_t>(d->kh) * d->kw * g.ch_blocks;
+    WtPlan wp;
+    bool use_tmem = false;
+    if (weights_mode != TILES_CONV_W_SMEM)
+        use_tmem = wtmem_plan(d, oh, ow, tile_oh, k_blocks, sms,
+                              weights_mode == TILES_CONV_W_TMEM ? forced_acc : 0, &wp);
+    if (weights_mode == TILES_CONV_W_TMEM && !use_tmem)
+        return fail(TILES_ERR_INFEASIBLE,
+                    "the filter does not fit tensor memory (needs c_out <= 128 and kh*kw*ceil(c/64) <= 14)");
+    const int owc = use_tmem ? wp.owc : g.owc;
+    const int nr = use_tmem ? wp.nr : g.nr;
+
     char* wsb = static_cast<char*>(ws);
     uint16_t* wr = reinterpret_cast<uint16_t*>(wsb + g.weights_offset);
-    const uint16_t* xn = static_cast<const uint16_t*>(d->x);
-    {
-        const int64_t total = static_cast<int64_t>(d->c_out) * d->kh * d->kw * g.cp;
-        reorder_weights_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(
-            static_cast<const uint16_t*>(d->wt), wr, d->c, g.cp, d->kh, d->kw, total);
-    }
-    if (d->x_layout == TILES_LAYOUT_NCHW) {
-        uint16_t* xt = reinterpret_cast<uint16_t*>(wsb + g.x_offset);
-        dim3 grid((d->w + 63) / 64, (d->c + 63) / 64, static_cast<unsigned>(d->n) * d->h);
-        if (d->w % 2 == 0 && (reinterpret_cast<uintptr_t>(xn) & 3u) == 0)
-            nchw_to_nhwc_kernel<true><<<grid, 256, 0, st>>>(xn, xt, d->c, d->h, d->w);
-        else
-            nchw_to_nhwc_kernel<false><<<grid, 256, 0, st>>>(xn, xt, d->c, d->h, d->w);
-        xn = xt;
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "conv prep: %s", cudaGetErrorString(e));
+    const uint16_t* x_src = static_cast<const uint16_t*>(d->x);
+    uint16_t* xt = d->x_layout == TILES_LAYOUT_NCHW ? reinterpret_cast<uint16_t*>(wsb + g.x_offset)
+                                                     : nullptr;
+    const uint16_t* xn = xt ? xt : x_src;
 
     auto fn = encode_fn_tma_conv();
     if (!fn) return fail(TILES_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (no CUDA driver?)");
@@ -504,11 +1004,13 @@ int conv2d_tma(const tiles_conv_desc* d, int tile_oh, int64_t oh, int64_t ow,
                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tw, tx;
     {
+        // Weight rows [c_out][kh*kw*Cp]: K blocks of 64 channels x (the
+        // output-channel block, or 128 rows with zero fill for TMEM).
         const int64_t k = static_cast<int64_t>(d->kh) * d->kw * g.cp;
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(d->c_out), 1};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(k) * 2,
                                  static_cast<cuuint64_t>(k) * 2 * static_cast<cuuint64_t>(d->c_out)};
-        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g.bn), 1};
+        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(use_tmem ? 128 : g.bn), 1};
         cuuint32_t estr[3] = {1, 1, 1};
         CUresult r = fn(&tw, dt, 3, wr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -522,8 +1024,8 @@ int conv2d_tma(const tiles_conv_desc* d, int tile_oh, int64_t oh, int64_t ow,
         cuuint64_t strides[3] = {static_cast<cuuint64_t>(d->c) * 2,
                                  static_cast<cuuint64_t>(d->w) * d->c * 2,
                                  static_cast<cuuint64_t>(d->h) * d->w * d->c * 2};
-        cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g.owc * d->sw),
-                             static_cast<cuuint32_t>(g.nr * d->sh), 1};
+        cuuint32_t box[4] = {64, static_cast<cuuint32_t>(owc * d->sw),
+                             static_cast<cuuint32_t>(nr * d->sh), 1};
         cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(d->sw), static_cast<cuuint32_t>(d->sh), 1};
         CUresult r = fn(&tx, dt, 4, const_cast<uint16_t*>(xn), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -531,47 +1033,100 @@ int conv2d_tma(const tiles_conv_desc* d, int tile_oh, int64_t oh, int64_t ow,
         if (r != CUDA_SUCCESS)
             return fail(TILES_ERR_CUDA, "cuTensorMapEncodeTiled(input) failed (%d)", (int)r);
     }
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
-    // Weights stay resident in shared memory when there is one output-
-    // channel block and they leave room for at least 3 pixel stages; the
-    // ring then carries 16 KB pixel tiles.  Otherwise each stage holds a
-    // pixel tile and a weight tile.  At most kMaxStages - 1 stages (the last
-    // barrier slot marks the resident weights).
-    const int budget = 227 * 1024 - kSmemBarrierBytes - kSmemAlignSlack;
-    const int64_t k_blocks = static_cast<int64_t>(d->kh) * d->kw * g.ch_blocks;
-    const int64_t w_res_bytes = k_blocks * g.bn * 128;
-    const bool w_resident = (d->c_out + g.bn - 1) / g.bn == 1 && w_res_bytes + 3 * kTmaConvA <= budget;
-    const int stage_bytes = w_resident ? kTmaConvA : (kTmaConvA + g.bn * 128 + 1023) / 1024 * 1024;
-    const int stages = static_cast<int>(std::min<int64_t>(
-        kMaxStages - 1, (budget - (w_resident ? w_res_bytes : 0)) / stage_bytes));
-    const int smem = static_cast<int>((w_resident ? w_res_bytes : 0) + stages * stage_bytes) +
-                     kSmemBarrierBytes + kSmemAlignSlack;
-    e = cudaFuncSetAttribute(conv_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
 
+    const int budget = 227 * 1024 - kSmemBarrierBytes - kSmemAlignSlack;
     ConvTmaArgs a{};
     a.y = d->y;
     a.n = d->n; a.c = d->c; a.h = d->h; a.w = d->w; a.c_out = d->c_out; a.kh = d->kh; a.kw = d->kw;
     a.sh = d->sh; a.sw = d->sw; a.pw = d->pw; a.dh = d->dh; a.dw = d->dw;
     a.oh = static_cast<int32_t>(oh); a.ow = static_cast<int32_t>(ow);
-    a.owc = g.owc; a.nr = g.nr; a.nco = g.bn;
-    a.cblocks = static_cast<int32_t>((ow + g.owc - 1) / g.owc);
-    a.co_blocks = (d->c_out + g.bn - 1) / g.bn;
+    a.owc = owc; a.nr = nr;
+    a.cblocks = static_cast<int32_t>((ow + owc - 1) / owc);
     a.ch_blocks = g.ch_blocks;
-    a.k_blocks = d->kh * d->kw * g.ch_blocks;
-    // TMA loads ceil(box / stride) elements per dimension: 64 channels x owc
-    // x nr = 128 pixel rows of 128 bytes, and bn weight rows of 128 bytes.
-    a.vec_ok = ((reinterpret_cast<uintptr_t>(d->y) & 15u) == 0 && ow % 8 == 0) ? 1 : 0;
-    a.w_resident = w_resident ? 1 : 0;
-    a.w_bytes = static_cast<uint32_t>(w_res_bytes);
-    a.tx_bytes = static_cast<uint32_t>(kTmaConvA + (w_resident ? 0 : g.bn * 128));
+    a.k_blocks = static_cast<int32_t>(k_blocks);
     a.out_dtype = d->out_dtype;
-    a.idesc = ptx::idesc_f16_f32acc(d->in_dtype == TILES_BF16, false, kTmaConvPixels, g.bn);
     a.err = static_cast<int32_t*>(ws);
     a.wait_limit_ns = 2000000000ull;
+    a.wr = wr;
+    a.kp = static_cast<int32_t>(d->kh * d->kw * g.cp);
+    const bool y16 = (reinterpret_cast<uintptr_t>(d->y) & 15u) == 0;
+    int stages = 0, stage_bytes = 0, smem = 0;
+    if (use_tmem) {
+        // M = 128 output channels (one block), N = the pixel tile; TMA
+        // delivers owc x nr pixel rows of 128 bytes per K block.
+        a.npix = owc * nr;
+        a.acc_bufs = wp.acc_bufs;
+        a.a_col = wp.acc_bufs * a.npix;
+        a.nco = 128;
+        a.co_blocks = 1;
+        a.tx_bytes = static_cast<uint32_t>(a.npix * 128);
+        a.vec_ok = (y16 && ow % (d->out_dtype == TILES_F32 ? 4 : 8) == 0) ? 1 : 0;
+        a.idesc = ptx::idesc_f16_f32acc(d->in_dtype == TILES_BF16, false, 128, a.npix);
+        a.stages = wp.stages;
+        a.stg_off = wp.stages * a.npix * 128;
+        a.stg_pitch = wp.stg_pitch;
+        a.bar_off = a.stg_off + wp.stg_bytes;
+        a.w_slots = wp.w_slots;
+        smem = wp.smem;
+        e = set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel), &g_smem_wtmem, smem);
+    } else {
+        // Weights stay resident in shared memory when there is one output-
+        // channel block and they leave room for at least 3 pixel stages;
+        // the ring then carries 16 KB pixel tiles.  Otherwise each stage
+        // holds a pixel tile and a weight tile.  At most kMaxStages - 1
+        // stages (the last barrier slot marks the resident weights).
+        const int64_t w_res_bytes = k_blocks * g.bn * 128;
+        const bool w_resident =
+            (d->c_out + g.bn - 1) / g.bn == 1 && w_res_bytes + 3 * kTmaConvA <= budget;
+        stage_bytes = w_resident ? kTmaConvA : (kTmaConvA + g.bn * 128 + 1023) / 1024 * 1024;
+        stages = static_cast<int>(std::min<int64_t>(
+            kMaxStages - 1, (budget - (w_resident ? w_res_bytes : 0)) / stage_bytes));
+        smem = static_cast<int>((w_resident ? w_res_bytes : 0) + stages * stage_bytes) +
+               kSmemBarrierBytes + kSmemAlignSlack;
+        a.nco = g.bn;
+        a.co_blocks = (d->c_out + g.bn - 1) / g.bn;
+        // TMA loads ceil(box / stride) elements per dimension: 64 channels
+        // x owc x nr = 128 pixel rows of 128 bytes, and bn weight rows.
+        a.vec_ok = (y16 && ow % 8 == 0) ? 1 : 0;
+        a.w_resident = w_resident ? 1 : 0;
+        a.w_bytes = static_cast<uint32_t>(w_res_bytes);
+        a.tx_bytes = static_cast<uint32_t>(kTmaConvA + (w_resident ? 0 : g.bn * 128));
+        a.idesc = ptx::idesc_f16_f32acc(d->in_dtype == TILES_BF16, false, kTmaConvPixels, g.bn);
+        e = set_smem_attr(reinterpret_cast<const void*>(conv_tma_kernel), &g_smem_tma, smem);
+    }
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
+
+    // ---- launches: operand preparation, then the convolution ----
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t* wsrc = static_cast<const uint16_t*>(d->wt);
+    const int64_t w_total = static_cast<int64_t>(d->c_out) * d->kh * d->kw * g.cp;
+    const unsigned w_blocks = static_cast<unsigned>((w_total + 255) / 256);
+    if (xt) {
+        if (d->c % 8 == 0 && d->w % 8 == 0) {
+            // One launch: 16-byte transpose blocks, then weight blocks.
+            const int64_t items = static_cast<int64_t>(d->n) * d->h * ((d->c + 63) / 64) *
+                                  ((d->w + 31) / 32);
+            const int64_t t_blocks = (items + 7) / 8;
+            if (t_blocks + w_blocks > INT32_MAX)
+                return fail(TILES_ERR_TOO_LARGE, "input too large for one transpose launch");
+            conv_prep_kernel<<<static_cast<unsigned>(t_blocks + w_blocks), 256, 0, st>>>(
+                x_src, xt, d->c, d->h, d->w, items, static_cast<unsigned>(t_blocks), wsrc, wr,
+                g.cp, d->kh, d->kw, w_total);
+        } else {
+            reorder_weights_kernel<<<w_blocks, 256, 0, st>>>(wsrc, wr, d->c, g.cp, d->kh, d->kw,
+                                                             w_total);
+            dim3 grid((d->w + 63) / 64, (d->c + 63) / 64, static_cast<unsigned>(d->n) * d->h);
+            if (d->w % 2 == 0)
+                nchw_to_nhwc_kernel<true><<<grid, 256, 0, st>>>(x_src, xt, d->c, d->h, d->w);
+            else
+                nchw_to_nhwc_kernel<false><<<grid, 256, 0, st>>>(x_src, xt, d->c, d->h, d->w);
+        }
+    } else {
+        reorder_weights_kernel<<<w_blocks, 256, 0, st>>>(wsrc, wr, d->c, g.cp, d->kh, d->kw,
+                                                         w_total);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "conv prep: %s", cudaGetErrorString(e));
 
     const int64_t n_ht_total = (oh + tile_oh - 1) / tile_oh;
     for (int64_t first = 0; first < n_ht_total; first += kConvMaxHTiles) {
@@ -591,12 +1146,15 @@ int conv2d_tma(const tiles_conv_desc* d, int tile_oh, int64_t oh, int64_t ow,
             max_rows = std::max(max_rows, o1 - o0);
         }
         a.n_htiles = count;
-        a.rblocks = (max_rows + g.nr - 1) / g.nr;
+        a.rblocks = (max_rows + nr - 1) / nr;
         const int64_t units = static_cast<int64_t>(d->n) * count * a.rblocks * a.cblocks * a.co_blocks;
         if (units > INT32_MAX) return fail(TILES_ERR_TOO_LARGE, "too many tiles");
         a.units = static_cast<int32_t>(units);
         const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-        conv_tma_kernel<<<grid, kGemmThreads, smem, st>>>(tw, tx, a, stages, stage_bytes);
+        if (use_tmem)
+            conv_wtmem_kernel<<<grid, kWtThreads, smem, st>>>(tw, tx, a);
+        else
+            conv_tma_kernel<<<grid, kGemmThreads, smem, st>>>(tw, tx, a, stages, stage_bytes);
         e = cudaGetLastError();
         if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "conv launch: %s", cudaGetErrorString(e));
     }

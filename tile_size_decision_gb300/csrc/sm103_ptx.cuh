@@ -229,6 +229,18 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
             "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem], kind::f16, one CTA: A's M rows are the
+// TMEM lanes and its K elements run along the columns, two 16-bit values
+// per 32-bit column (K = 16 per instruction = 8 columns).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive once on *bar (in this CTA, and with CG == 2 also on the same barrier
 // of the peer CTA) when every tcgen05 operation this thread issued so far
 // has completed.
@@ -274,6 +286,16 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
+}
+
+// The same for 8 columns.
+__device__ __forceinline__ void tmem_ld_8cols(uint32_t taddr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3, uint32_t& r4,
+                                              uint32_t& r5, uint32_t& r6, uint32_t& r7) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6),
+                   "=r"(r7)
+                 : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    ptx::grid_dependency_wait();     // the prepared operands are complete
 
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort = &bar->abort;
@@ -481,6 +482,9 @@ __global__ void __launch_bounds__(kWtThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    // Set-up above overlaps the operand preparation; its results (filter,
+    // NHWC input) are read only after this point.
+    ptx::grid_dependency_wait();
 
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort = &bar->abort;
@@ -728,7 +732,8 @@ __global__ void __launch_bounds__(kWtThreads, 1)
 
 // NCHW -> NHWC for 16-bit elements with 16-byte accesses on both sides (C
 // and W multiples of 8, x 16-byte aligned), fused with the weight reorder.
-// A warp moves 64 channels x 32 columns of one (image, row): lane (cg, q)
+// A warp moves kPrepItemsPerWarp items of 64 channels x 32 columns of one
+// (image, row): lane (cg, q)
 // loads channels 8cg..8cg+7 at columns 8q..8q+7 as eight 16-byte words,
 // transposes the 8 x 8 block with byte permutes and stores eight pixels of
 // 8 channels.  For a fixed register a warp reads 8 runs of 64 bytes and
@@ -738,11 +743,16 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
     return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
+// Items (64 channels x 32 columns of one row) per warp: all their loads are
+// in flight before the first transpose.
+constexpr int kPrepItemsPerWarp = 1;
+
 __global__ void __launch_bounds__(256)
     conv_prep_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xt, int C, int H,
                      int W, int64_t items, unsigned transpose_blocks,
                      const uint16_t* __restrict__ w, uint16_t* __restrict__ wr, int Cp, int kh,
                      int kw, int64_t w_total) {
+    ptx::grid_launch_dependents();
     if (blockIdx.x >= transpose_blocks) {
         const int64_t i = static_cast<int64_t>(blockIdx.x - transpose_blocks) * 256 + threadIdx.x;
         if (i >= w_total) return;
@@ -755,36 +765,54 @@ __global__ void __launch_bounds__(256)
         wr[i] = ci < C ? w[((co * C + ci) * kh + r) * kw + s] : static_cast<uint16_t>(0);
         return;
     }
-    const int64_t item = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (item >= items) return;
     const int lane = threadIdx.x & 31;
     const int wblks = (W + 31) >> 5, cblks = (C + 63) >> 6;
-    int64_t t = item;
-    const int wb = static_cast<int>(t % wblks);
-    t /= wblks;
-    const int cb = static_cast<int>(t % cblks);
-    t /= cblks;
-    const int h = static_cast<int>(t % H);
-    const int64_t n = t / H;
-    const int c = cb * 64 + (lane & 7) * 8;
-    const int w0 = wb * 32 + (lane >> 3) * 8;
-    if (c >= C || w0 >= W) return;     // whole octets: C and W are multiples of 8
     const int64_t plane = static_cast<int64_t>(H) * W;
-    const uint16_t* src = x + ((n * C + c) * H + h) * static_cast<int64_t>(W) + w0;
-    uint4 r[8];
+    const int64_t first =
+        (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kPrepItemsPerWarp;
+    // Item -> (image, row, channel octet, column octet) of this lane; false
+    // past the end (whole octets: C and W are multiples of 8).
+    auto locate = [&](int64_t item, int64_t* n, int* h, int* c, int* w0) {
+        int64_t t = item;
+        const int wb = static_cast<int>(t % wblks);
+        t /= wblks;
+        const int cb = static_cast<int>(t % cblks);
+        t /= cblks;
+        *h = static_cast<int>(t % H);
+        *n = t / H;
+        *c = cb * 64 + (lane & 7) * 8;
+        *w0 = wb * 32 + (lane >> 3) * 8;
+        return item < items && *c < C && *w0 < W;
+    };
+    uint4 r[kPrepItemsPerWarp][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) r[j] = __ldg(reinterpret_cast<const uint4*>(src + j * plane));
-    uint16_t* dst = xt + ((n * H + h) * static_cast<int64_t>(W) + w0) * C + c;
+    for (int it = 0; it < kPrepItemsPerWarp; ++it) {
+        int64_t n;
+        int h, c, w0;
+        if (locate(first + it, &n, &h, &c, &w0)) {
+            const uint16_t* src = x + ((n * C + c) * H + h) * static_cast<int64_t>(W) + w0;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        // Pixel p: channel pairs (2i, 2i+1) from word p/2 of rows 2i, 2i+1.
-        const uint32_t sel = (p & 1) ? 0x7632u : 0x5410u;
-        uint4 o;
-        o.x = __byte_perm(word_of(r[0], p >> 1), word_of(r[1], p >> 1), sel);
-        o.y = __byte_perm(word_of(r[2], p >> 1), word_of(r[3], p >> 1), sel);
-        o.z = __byte_perm(word_of(r[4], p >> 1), word_of(r[5], p >> 1), sel);
-        o.w = __byte_perm(word_of(r[6], p >> 1), word_of(r[7], p >> 1), sel);
-        *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(p) * C) = o;
+            for (int j = 0; j < 8; ++j)
+                r[it][j] = __ldg(reinterpret_cast<const uint4*>(src + j * plane));
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < kPrepItemsPerWarp; ++it) {
+        int64_t n;
+        int h, c, w0;
+        if (!locate(first + it, &n, &h, &c, &w0)) continue;
+        uint16_t* dst = xt + ((n * H + h) * static_cast<int64_t>(W) + w0) * C + c;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            // Pixel p: channel pairs (2i, 2i+1) from word p/2 of rows 2i, 2i+1.
+            const uint32_t sel = (p & 1) ? 0x7632u : 0x5410u;
+            uint4 o;
+            o.x = __byte_perm(word_of(r[it][0], p >> 1), word_of(r[it][1], p >> 1), sel);
+            o.y = __byte_perm(word_of(r[it][2], p >> 1), word_of(r[it][3], p >> 1), sel);
+            o.z = __byte_perm(word_of(r[it][4], p >> 1), word_of(r[it][5], p >> 1), sel);
+            o.w = __byte_perm(word_of(r[it][6], p >> 1), word_of(r[it][7], p >> 1), sel);
+            *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(p) * C) = o;
+        }
     }
 }
 
@@ -831,6 +859,7 @@ __global__ void __launch_bounds__(256)
 // OIHW weights -> [c_out][r][s][Cp] with the channels zero-padded to Cp.
 __global__ void reorder_weights_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ wr,
                                        int C, int Cp, int kh, int kw, int64_t total) {
+    ptx::grid_launch_dependents();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= total) return;
     const int ci = static_cast<int>(i % Cp);
@@ -1106,7 +1135,7 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
             // One launch: 16-byte transpose blocks, then weight blocks.
             const int64_t items = static_cast<int64_t>(d->n) * d->h * ((d->c + 63) / 64) *
                                   ((d->w + 31) / 32);
-            const int64_t t_blocks = (items + 7) / 8;
+            const int64_t t_blocks = (items + 8 * kPrepItemsPerWarp - 1) / (8 * kPrepItemsPerWarp);
             if (t_blocks + w_blocks > INT32_MAX)
                 return fail(TILES_ERR_TOO_LARGE, "input too large for one transpose launch");
             conv_prep_kernel<<<static_cast<unsigned>(t_blocks + w_blocks), 256, 0, st>>>(
@@ -1150,12 +1179,25 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         const int64_t units = static_cast<int64_t>(d->n) * count * a.rblocks * a.cblocks * a.co_blocks;
         if (units > INT32_MAX) return fail(TILES_ERR_TOO_LARGE, "too many tiles");
         a.units = static_cast<int32_t>(units);
-        const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-        if (use_tmem)
-            conv_wtmem_kernel<<<grid, kWtThreads, smem, st>>>(tw, tx, a);
-        else
-            conv_tma_kernel<<<grid, kGemmThreads, smem, st>>>(tw, tx, a, stages, stage_bytes);
-        e = cudaGetLastError();
+        // Programmatic serialization: the blocks launch while the
+        // preparation kernel drains and wait for it in-kernel.
+        cudaLaunchConfig_t lc{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(units, sms)));
+        lc.dynamicSmemBytes = static_cast<size_t>(smem);
+        lc.stream = st;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        if (use_tmem) {
+            lc.blockDim = dim3(kWtThreads);
+            e = cudaLaunchKernelEx(&lc, conv_wtmem_kernel, tw, tx, a);
+        } else {
+            lc.blockDim = dim3(kGemmThreads);
+            e = cudaLaunchKernelEx(&lc, conv_tma_kernel, tw, tx, a, stages, stage_bytes);
+        }
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "conv launch: %s", cudaGetErrorString(e));
     }
     return TILES_OK;

@@ -179,6 +179,21 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+
+// Wait until the grids this one depends on (launched before it on the stream
+// with programmatic serialization) have completed and their memory
+// operations are visible.  A no-op for a grid launched without it.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid on the stream to start launching (its blocks still
+// wait in grid_dependency_wait before they read this grid's results).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- descriptors -----------------------------------------------------------
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading- and

@@ -58,6 +58,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--autotune", type=int, default=4, metavar="K",
+                    help="GEMM workloads: time the planner's top K configurations (with "
+                         "their last-round schedules) before the timed steps and run the "
+                         "fastest; 0 runs the planner's first choice")
     return ap.parse_args()
 
 
@@ -301,6 +305,28 @@ def gemm_job(wl, dev, tiles, torch):
     }
     j.dtype = "f16" if wl.in_dtype == S.F16 else "bf16"
     j.oracle = lambda budget: oracle_sample(wl, budget, a_np, b_np)
+
+    def autotune(top_k):
+        # The measured shortlist (outside the timed steps): the winner becomes
+        # the problem's tuned configuration, which the steps' calls use.
+        best, rows = tiles.gemm_autotune(a_d, b_d, j.out, top_k=top_k, reps=10, workspace=j.ws,
+                                         batched=wl.b > 1)
+        tiles.check(j.ws)
+        sch_t = tiles.gemm_schedule(a_d, b_d, j.out, workspace=j.ws)
+        return {"top_k": top_k, "reps": 10,
+                "winner": {"bm": best.bm, "bn": best.bn, "stages": best.stages,
+                           "cta_group": best.cta_group,
+                           "tail": ["whole", "n_halves", "k_split"][sch_t.tail_mode],
+                           "k_parts": sch_t.ksplit},
+                "planner_choice_kept": (best.bm, best.bn, best.stages, best.cta_group,
+                                        sch_t.tail_mode) == (c.bm, c.bn, c.stages, c.cta_group,
+                                                             sch.tail_mode),
+                "shortlist_us": [
+                    [f'{r["bm"]}x{r["bn"]}/{r["stages"]}/cg{r["cta_group"]}/{r["tail_mode"]}'
+                     + ("/planner" if r["tail_asked"] == 0 else ""),
+                     round(r["us"], 2)] for r in rows if r["status"] == 0]}
+
+    j.autotune = autotune
     return j
 
 
@@ -378,6 +404,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     job_ws = getattr(job, "ws", ws)
+    if getattr(job, "autotune", None) and args.autotune > 0:
+        job.config["autotune"] = job.autotune(args.autotune)
     for _ in range(args.warmup):
         flush.zero_()
         job.step(ws, stream)

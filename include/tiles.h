@@ -371,6 +371,54 @@ size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh);
 int tiles_gemm_noalloc(const tiles_gemm_desc* desc, const tiles_config* cfg, void* stream,
                        int wait);
 
+/* ---- Measured shortlist (tutorial, "自动调优": enumerate the tile
+ * configurations, drop those that break a hardware constraint, time each
+ * survivor on the target GPU, keep the fastest) ---------------------------- */
+
+/* One timed candidate. */
+typedef struct {
+    tiles_config cfg;        /* the configuration; cfg.tail is the last-round schedule asked for */
+    int32_t status;          /* TILES_OK, or why the candidate could not run (us is then 0) */
+    int32_t tail_mode;       /* the schedule the launches used: 0 none needed, 1 N-halves, 2 K split */
+    int32_t ksplit;          /* K parts of a split last round (1 otherwise) */
+    float us;                /* median launch time over the timed repetitions, microseconds */
+} tiles_tune_result;
+
+/* Time the planner's top_k configurations (GB300 mode, in rank order) for
+ * this GEMM, each with every last-round schedule it admits (the planner's
+ * own choice first, then whole tiles, N-halves, a K split when the
+ * workspace holds its partials; ties keep the earlier): one untimed
+ * launch, then reps launches bracketed by CUDA events on `stream`, of which
+ * the median counts.  The fastest becomes the tuned configuration of the
+ * problem (batch, m, n, k, dtypes, SM count), which tiles_gemm and
+ * tiles_gemm_batched use when called with cfg == NULL; *best receives it.
+ *
+ * Runs the caller's GEMM (desc->c is overwritten) and synchronises
+ * `stream`.  results (capacity entries, may be NULL) receives the
+ * candidates in the order tried and *n_results their number.  1 <= top_k <=
+ * 16, 1 <= reps <= 100.  TILES_ERR_INFEASIBLE when no candidate ran. */
+int tiles_gemm_autotune(const tiles_gemm_desc* desc, int top_k, int reps, void* workspace,
+                        size_t ws_bytes, void* stream, tiles_tune_result* results,
+                        int capacity, int* n_results, tiles_config* best);
+
+/* The tuned configuration of a problem: TILES_OK and *out filled when one
+ * is recorded, TILES_ERR_INFEASIBLE when none is.  Host only. */
+int tiles_tuned_lookup(int sm_count, int64_t batch, int64_t m, int64_t n, int64_t k, int in_dtype,
+                       int out_dtype, tiles_config* out);
+
+/* Write every tuned configuration to a text file: a header line, then one
+ * line per problem with sm_count batch m n k in_dtype out_dtype bm bn bk
+ * stages threads instr acc_bufs cta_group tail us.  Host only. */
+int tiles_tuned_save(const char* path);
+
+/* Merge the entries of a file written by tiles_tuned_save into the table.
+ * A missing file or a malformed line returns TILES_ERR_INVALID_ARG and
+ * merges nothing.  Host only. */
+int tiles_tuned_load(const char* path);
+
+/* Forget every tuned configuration.  Host only. */
+int tiles_tuned_clear(void);
+
 /* Synchronise `stream`, read and clear the workspace's error word:
  * TILES_OK, or TILES_ERR_TIMEOUT if a kernel's bounded wait expired. */
 int tiles_check(void* workspace, void* stream);

@@ -10,6 +10,7 @@ streams.  Names follow the C ABI without the ``tiles_`` prefix.
 from __future__ import annotations
 
 import ctypes as C
+import os
 
 from . import _abi
 from ._abi import TilesError, check as _check
@@ -17,7 +18,9 @@ from ._abi import TilesError, check as _check
 __all__ = [
     "TilesError", "load", "version", "device_preset", "device_query", "evaluate",
     "finish_parallelism", "c0_bytes", "plan", "htile_rows", "workspace_bytes", "workspace",
-    "gemm", "gemm_batched", "gemm_schedule", "gemm_workspace", "gemm_noalloc", "conv2d_htiled", "conv_workspace", "check", "selftest_wait_timeout", "make_config",
+    "gemm", "gemm_batched", "gemm_schedule", "gemm_workspace", "gemm_noalloc", "gemm_autotune",
+    "tuned_lookup", "tuned_save", "tuned_load", "tuned_clear", "conv2d_htiled", "conv_workspace",
+    "conv_out_shape", "check", "selftest_wait_timeout", "make_config",
 ]
 
 
@@ -188,6 +191,57 @@ def gemm(a, b, out=None, out_dtype=None, cfg=None, workspace=None, stream=None):
     _check(load().tiles_gemm(C.byref(d), _cfg_ptr(cfg), ws, wsb, _stream_handle(stream)),
            "tiles_gemm")
     return out
+
+
+def gemm_autotune(a, b, out, top_k=4, reps=5, workspace=None, stream=None, batched=None):
+    """Time the planner's top_k configurations for out = a @ b (each with
+    every last-round schedule it admits) and record the fastest as the tuned
+    configuration of the problem, which later calls with cfg=None use.
+    Overwrites `out`.  Returns (best Config, list of per-candidate dicts)."""
+    if batched is None:
+        batched = a.dim() == 3
+    d = _gemm_desc(a, b, out, batched=batched)
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    cap = 3 * top_k
+    res = (_abi.TuneResult * cap)()
+    n = C.c_int(0)
+    best = _abi.Config()
+    _check(load().tiles_gemm_autotune(C.byref(d), top_k, reps, ws, wsb, _stream_handle(stream),
+                                      res, cap, C.byref(n), C.byref(best)),
+           "tiles_gemm_autotune")
+    rows = []
+    for r in res[:min(n.value, cap)]:
+        rows.append({"bm": r.cfg.bm, "bn": r.cfg.bn, "stages": r.cfg.stages,
+                     "cta_group": r.cfg.cta_group, "tail_asked": r.cfg.tail,
+                     "tail_mode": ["none", "n_halves", "k_split"][r.tail_mode],
+                     "ksplit": r.ksplit, "status": r.status, "us": r.us})
+    return best, rows
+
+
+def tuned_lookup(sm_count, b, m, n, k, in_dtype, out_dtype):
+    """The tuned Config of a problem (dtypes as "f16"/"bf16"/"f32" or codes),
+    or None."""
+    in_dtype = _abi.DTYPE_CODES.get(in_dtype, in_dtype)
+    out_dtype = _abi.DTYPE_CODES.get(out_dtype, out_dtype)
+    cfg = _abi.Config()
+    s = load().tiles_tuned_lookup(sm_count, b, m, n, k, in_dtype, out_dtype, C.byref(cfg))
+    if s == _abi.ERR_INFEASIBLE:
+        return None
+    _check(s, "tiles_tuned_lookup")
+    return cfg
+
+
+def tuned_save(path):
+    _check(load().tiles_tuned_save(os.fsencode(path)), "tiles_tuned_save")
+
+
+def tuned_load(path):
+    _check(load().tiles_tuned_load(os.fsencode(path)), "tiles_tuned_load")
+
+
+def tuned_clear():
+    _check(load().tiles_tuned_clear(), "tiles_tuned_clear")
 
 
 def gemm_batched(a, b, out=None, out_dtype=None, cfg=None, workspace=None, stream=None):

@@ -111,6 +111,11 @@ class Schedule(C.Structure):
                 ("tail_mode", C.c_int32), ("ksplit", C.c_int32), ("workspace_bytes", C.c_int64)]
 
 
+class TuneResult(C.Structure):
+    _fields_ = [("cfg", Config), ("status", C.c_int32), ("tail_mode", C.c_int32),
+                ("ksplit", C.c_int32), ("us", C.c_float)]
+
+
 class ConvDesc(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "n", "c", "h", "w", "c_out", "kh", "kw", "sh", "sw", "ph", "pw", "dh", "dw",
@@ -150,6 +155,14 @@ SIGNATURES = {
     "tiles_gemm_noalloc": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_void_p,
                                      C.c_int]),
     "tiles_conv_workspace_bytes": (C.c_size_t, [C.POINTER(ConvDesc), C.c_int]),
+    "tiles_gemm_autotune": (C.c_int, [C.POINTER(GemmDesc), C.c_int, C.c_int, C.c_void_p,
+                                      C.c_size_t, C.c_void_p, C.POINTER(TuneResult), C.c_int,
+                                      C.POINTER(C.c_int), C.POINTER(Config)]),
+    "tiles_tuned_lookup": (C.c_int, [C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
+                                     C.c_int, C.c_int, C.POINTER(Config)]),
+    "tiles_tuned_save": (C.c_int, [C.c_char_p]),
+    "tiles_tuned_load": (C.c_int, [C.c_char_p]),
+    "tiles_tuned_clear": (C.c_int, []),
     "tiles_check": (C.c_int, [C.c_void_p, C.c_void_p]),
     "tiles_selftest_wait_timeout": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
 }

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -179,6 +180,22 @@ int launch_variant(int bn, int cg, const CUtensorMap& ta, const CUtensorMap& tb,
     return static_cast<int>(cudaErrorInvalidValue);
 }
 
+// Tuned configurations: the winners of measured shortlists
+// (tiles_gemm_autotune or a loaded file), keyed by the problem and the SM
+// count, consulted before the planner when no configuration is given.
+using TunedKey = std::tuple<int, int64_t, int64_t, int64_t, int64_t, int, int>;
+struct TunedEntry { tiles_config cfg; float us; };
+std::mutex g_tuned_mu;
+std::map<TunedKey, TunedEntry> g_tuned;
+
+bool tuned_config(const TunedKey& key, tiles_config* cfg) {
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    auto it = g_tuned.find(key);
+    if (it == g_tuned.end()) return false;
+    *cfg = it->second.cfg;
+    return true;
+}
+
 // Everything a GEMM launch decides before touching the GPU's queues:
 // validated arguments, the configuration and the wave-aware schedule.
 struct GemmPlan {
@@ -235,10 +252,21 @@ int gemm_prepare(const tiles_gemm_desc* d, const tiles_config* user_cfg, bool ba
     }
     int s = current_device(&gp->dev, &gp->ordinal);
     if (s != TILES_OK) return s;
+    // The configuration: the caller's, else a tuned one for this problem,
+    // else the planner's first choice.  A tuned last-round schedule is a
+    // preference: without the workspace for a K split it yields to the
+    // planner's choice instead of failing.
+    tiles_config tuned;
+    const tiles_config* eff = user_cfg;
     if (user_cfg) {
         gp->cfg = *user_cfg;
         s = check_config(gp->dev, gp->cfg, 2);
         if (s != TILES_OK) return s;
+    } else if (tuned_config(TunedKey{gp->dev.sm_count, d->batch, d->m, d->n, d->k, d->a_dtype,
+                                     d->c_dtype}, &tuned) &&
+               check_config(gp->dev, tuned, 2) == TILES_OK) {
+        gp->cfg = tuned;
+        eff = &tuned;
     } else {
         s = planned_config(gp->dev, gp->ordinal, d->batch, d->m, d->n, d->k, d->a_dtype,
                            d->c_dtype, &gp->cfg);
@@ -260,7 +288,7 @@ int gemm_prepare(const tiles_gemm_desc* d, const tiles_config* user_cfg, bool ba
     const int64_t k_blocks = (d->k + cfg.bk - 1) / cfg.bk;
     const int64_t rest = gp->tiles % gp->resident;
     const int64_t full = gp->tiles - rest;
-    const int forced = user_cfg ? user_cfg->tail : TILES_TAIL_AUTO;
+    int forced = eff ? eff->tail : TILES_TAIL_AUTO;
     if (forced < TILES_TAIL_AUTO || forced > TILES_TAIL_KSPLIT)
         return fail(TILES_ERR_INVALID_ARG, "unknown tail schedule %d", forced);
     TailChoice tc = gb300_tail_choice(gp->dev, cfg, gp->tiles, gp->resident, k_blocks, 2, forced);
@@ -273,7 +301,7 @@ int gemm_prepare(const tiles_gemm_desc* d, const tiles_config* user_cfg, bool ba
             gp->tail_mode = kTailKSplit;
             gp->full_units = full;
             gp->units = full + rest * tc.parts;
-        } else if (forced == TILES_TAIL_KSPLIT) {
+        } else if (forced == TILES_TAIL_KSPLIT && user_cfg) {
             return fail(TILES_ERR_INVALID_ARG, "a K-split last round needs %lld workspace bytes",
                         (long long)k.ws_needed);
         } else {
@@ -571,6 +599,191 @@ int tiles_gemm_schedule(const tiles_gemm_desc* desc, const tiles_config* cfg, si
     out->full_units = gp.full_units;
     out->units = gp.units;
     out->groups = gp.groups;
+    return TILES_OK;
+}
+
+int tiles_gemm_autotune(const tiles_gemm_desc* desc, int top_k, int reps, void* ws,
+                        size_t ws_bytes, void* stream, tiles_tune_result* results,
+                        int capacity, int* n_results, tiles_config* best) {
+    if (n_results) *n_results = 0;
+    if (!desc || !best) return fail(TILES_ERR_INVALID_ARG, "null descriptor or output");
+    if (top_k < 1 || top_k > 16 || reps < 1 || reps > 100)
+        return fail(TILES_ERR_INVALID_ARG, "top_k must be in [1, 16] and reps in [1, 100]");
+    if (capacity < 0 || (capacity > 0 && !results))
+        return fail(TILES_ERR_INVALID_ARG, "results must hold capacity entries");
+    // Validates the problem (shapes, pitches, dtypes) and finds the device.
+    GemmPlan gp0;
+    int s = gemm_prepare(desc, nullptr, true, ws ? ws_bytes : 0, &gp0);
+    if (s != TILES_OK) return s;
+    // Steps 1-2: the feasible configurations in the planner's rank order.
+    tiles_problem p{};
+    p.b = desc->batch; p.m = desc->m; p.n = desc->n; p.k = desc->k;
+    p.in_dtype = desc->a_dtype; p.out_dtype = desc->c_dtype;
+    p.instr = TILES_INSTR_TCGEN05; p.mode = TILES_MODE_GB300;
+    std::vector<tiles_verdict> ranked;
+    s = plan(gp0.dev, p, &ranked);
+    if (s != TILES_OK) return s;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<cudaEvent_t> ev(2 * reps);
+    for (auto& e : ev) {
+        cudaError_t ce = cudaEventCreate(&e);
+        if (ce != cudaSuccess) {
+            for (auto& x : ev) if (x) cudaEventDestroy(x);
+            return fail(TILES_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(ce));
+        }
+    }
+    int count = 0;
+    float best_us = 0.0f;
+    bool have_best = false;
+    tiles_config winner{};
+    auto record = [&](const tiles_tune_result& r) {
+        if (count < capacity) results[count] = r;
+        ++count;
+    };
+    const int n_cfg = std::min<int>(top_k, static_cast<int>(ranked.size()));
+    for (int i = 0; i < n_cfg; ++i) {
+        // Step 3: each schedule the configuration admits for the last round,
+        // the planner's own choice first (so that it wins ties).
+        std::vector<std::pair<int, int>> seen;   // (tail_mode, ksplit) already timed
+        const int tails[4] = {TILES_TAIL_AUTO, TILES_TAIL_WHOLE, TILES_TAIL_NHALF,
+                              TILES_TAIL_KSPLIT};
+        for (int t : tails) {
+            tiles_tune_result r{};
+            r.cfg = ranked[i].cfg;
+            r.cfg.tail = t;
+            r.ksplit = 1;
+            GemmPlan gp;
+            r.status = gemm_prepare(desc, &r.cfg, true, ws ? ws_bytes : 0, &gp);
+            if (r.status == TILES_OK) {
+                r.tail_mode = gp.tail_mode;
+                r.ksplit = static_cast<int32_t>(gp.ksplit);
+                const std::pair<int, int> sched{gp.tail_mode, r.ksplit};
+                if (std::find(seen.begin(), seen.end(), sched) != seen.end()) continue;
+                seen.push_back(sched);
+                r.status = gemm_common(desc, &r.cfg, ws, ws_bytes, stream, true);   // untimed
+                for (int k = 0; k < reps && r.status == TILES_OK; ++k) {
+                    cudaEventRecord(ev[2 * k], st);
+                    r.status = gemm_common(desc, &r.cfg, ws, ws_bytes, stream, true);
+                    cudaEventRecord(ev[2 * k + 1], st);
+                }
+                if (r.status == TILES_OK) r.status = tiles_check(ws, stream);
+                if (r.status == TILES_OK) {
+                    std::vector<float> ms(reps);
+                    for (int k = 0; k < reps && r.status == TILES_OK; ++k)
+                        if (cudaEventElapsedTime(&ms[k], ev[2 * k], ev[2 * k + 1]) != cudaSuccess)
+                            r.status = fail(TILES_ERR_CUDA, "cudaEventElapsedTime failed");
+                    if (r.status == TILES_OK) {
+                        std::sort(ms.begin(), ms.end());
+                        r.us = 1000.0f * ms[reps / 2];
+                        // Step 4: keep the fastest.
+                        if (!have_best || r.us < best_us) {
+                            have_best = true;
+                            best_us = r.us;
+                            winner = r.cfg;
+                        }
+                    }
+                }
+            }
+            record(r);
+        }
+    }
+    for (auto& e : ev) cudaEventDestroy(e);
+    if (n_results) *n_results = count;
+    if (!have_best) return fail(TILES_ERR_INFEASIBLE, "no candidate configuration ran");
+    *best = winner;
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    g_tuned[TunedKey{gp0.dev.sm_count, desc->batch, desc->m, desc->n, desc->k, desc->a_dtype,
+                     desc->c_dtype}] = TunedEntry{winner, best_us};
+    return TILES_OK;
+}
+
+int tiles_tuned_lookup(int sm_count, int64_t batch, int64_t m, int64_t n, int64_t k, int in_dtype,
+                       int out_dtype, tiles_config* out) {
+    if (!out) return fail(TILES_ERR_INVALID_ARG, "null output");
+    if (!tuned_config(TunedKey{sm_count, batch, m, n, k, in_dtype, out_dtype}, out))
+        return fail(TILES_ERR_INFEASIBLE, "no tuned configuration for this problem");
+    return TILES_OK;
+}
+
+static const char kTunedHeader[] = "tiles-tuned 1";
+
+int tiles_tuned_save(const char* path) {
+    if (!path) return fail(TILES_ERR_INVALID_ARG, "null path");
+    FILE* f = std::fopen(path, "w");
+    if (!f) return fail(TILES_ERR_INVALID_ARG, "cannot write %s", path);
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    std::fprintf(f, "%s\n", kTunedHeader);
+    for (const auto& kv : g_tuned) {
+        const TunedKey& key = kv.first;
+        const tiles_config& c = kv.second.cfg;
+        std::fprintf(f, "%d %lld %lld %lld %lld %d %d %d %d %d %d %d %d %d %d %d %.3f\n",
+                     std::get<0>(key), (long long)std::get<1>(key), (long long)std::get<2>(key),
+                     (long long)std::get<3>(key), (long long)std::get<4>(key), std::get<5>(key),
+                     std::get<6>(key), c.bm, c.bn, c.bk, c.stages, c.threads, c.instr, c.acc_bufs,
+                     c.cta_group, c.tail, kv.second.us);
+    }
+    const bool ok = std::fflush(f) == 0;
+    std::fclose(f);
+    return ok ? TILES_OK : fail(TILES_ERR_INVALID_ARG, "write to %s failed", path);
+}
+
+int tiles_tuned_load(const char* path) {
+    if (!path) return fail(TILES_ERR_INVALID_ARG, "null path");
+    FILE* f = std::fopen(path, "r");
+    if (!f) return fail(TILES_ERR_INVALID_ARG, "cannot read %s", path);
+    std::map<TunedKey, TunedEntry> loaded;
+    char line[512];
+    int lineno = 0;
+    int status = TILES_OK;
+    while (std::fgets(line, sizeof line, f)) {
+        ++lineno;
+        size_t len = std::strlen(line);
+        if (len == sizeof line - 1 && line[len - 1] != '\n') {
+            status = fail(TILES_ERR_INVALID_ARG, "%s:%d: line too long", path, lineno);
+            break;
+        }
+        while (len && (line[len - 1] == '\n' || line[len - 1] == '\r')) line[--len] = 0;
+        if (lineno == 1) {
+            if (std::strcmp(line, kTunedHeader) != 0) {
+                status = fail(TILES_ERR_INVALID_ARG, "%s: not a tuned-configuration file", path);
+                break;
+            }
+            continue;
+        }
+        if (len == 0) continue;
+        int sm, in_dt, out_dt;
+        long long b, m, n, k;
+        tiles_config c{};
+        float us = 0.0f;
+        int used = 0;
+        const int got = std::sscanf(line, "%d %lld %lld %lld %lld %d %d %d %d %d %d %d %d %d %d %d %f %n",
+                                    &sm, &b, &m, &n, &k, &in_dt, &out_dt, &c.bm, &c.bn, &c.bk,
+                                    &c.stages, &c.threads, &c.instr, &c.acc_bufs, &c.cta_group,
+                                    &c.tail, &us, &used);
+        const bool sizes_ok = sm > 0 && b >= 1 && m >= 1 && n >= 1 && k >= 1;
+        const bool dtypes_ok = (in_dt == TILES_F16 || in_dt == TILES_BF16) && bytes_of(out_dt) > 0;
+        const bool cfg_ok = c.bm > 0 && c.bn > 0 && c.bk > 0 && c.stages > 0 && c.threads > 0 &&
+                            c.tail >= TILES_TAIL_AUTO && c.tail <= TILES_TAIL_KSPLIT &&
+                            c.cta_group >= 1 && c.cta_group <= 2 && us >= 0.0f;
+        if (got != 17 || line[used] != 0 || !sizes_ok || !dtypes_ok || !cfg_ok) {
+            status = fail(TILES_ERR_INVALID_ARG, "%s:%d: malformed entry", path, lineno);
+            break;
+        }
+        loaded[TunedKey{sm, b, m, n, k, in_dt, out_dt}] = TunedEntry{c, us};
+    }
+    if (status == TILES_OK && lineno == 0)
+        status = fail(TILES_ERR_INVALID_ARG, "%s: empty file", path);
+    std::fclose(f);
+    if (status != TILES_OK) return status;
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    for (const auto& kv : loaded) g_tuned[kv.first] = kv.second;
+    return TILES_OK;
+}
+
+int tiles_tuned_clear(void) {
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    g_tuned.clear();
     return TILES_OK;
 }
 

@@ -123,6 +123,17 @@ __device__ __forceinline__ void transpose8x8_b16(uint32_t& w0, uint32_t& w1, uin
     }
 }
 
+// a / d for 0 <= a < 2^22 and d >= 1, from a float reciprocal of d: the
+// rounded product is within one of the quotient (its error is below
+// a * 2^-23 < 1), and one comparison each way fixes it.  The epilogue's
+// chunk indices stay below 128 * 256 * 4 / 16 = 8192.
+__device__ __forceinline__ int div_small(int a, int d, float inv_d) {
+    int q = __float2int_rz(__int2float_rn(a) * inv_d);
+    if (q * d > a) --q;
+    else if ((q + 1) * d <= a) ++q;
+    return q;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16) {
     if (bf16) {
         __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
@@ -636,6 +647,8 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         // Output chunks of 16 bytes: per (channel, pixel row) owc*ob/16.
         const int seg_chunks = args.owc * ob / 16;
         const int tile_chunks = 128 * args.nr * seg_chunks;
+        const float inv_seg = 1.0f / static_cast<float>(seg_chunks);
+        const float inv_nr = 1.0f / static_cast<float>(args.nr);
         const int ch_elems = 16 / ob;
         uint32_t acc = 0, acc_phase = 0;
         for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
@@ -650,51 +663,64 @@ __global__ void __launch_bounds__(kWtThreads, 1)
             ptx::tc_fence_after();
             const uint32_t tacc = tmem + lane_base + acc * static_cast<uint32_t>(args.npix);
             uint8_t* srow = staging + co * args.stg_pitch;
-#pragma unroll 1
-            for (int c0 = col_begin; c0 < col_end; c0 += 32) {
-                const int groups = (col_end - c0) >= 32 ? 4 : (col_end - c0) >> 3;
-                uint32_t v[32];
+            // All of this thread's columns (npix/2 <= 128) come out of TMEM in
+            // one round trip, after which the accumulator is released; the
+            // conversion and the staging writes overlap the next tile's MMAs.
+            const int ncols = col_end - col_begin;
+            uint32_t v[128];
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    if (g < groups)
-                        ptx::tmem_ld_8cols(tacc + c0 + 8 * g, v[8 * g + 0], v[8 * g + 1],
-                                           v[8 * g + 2], v[8 * g + 3], v[8 * g + 4],
-                                           v[8 * g + 5], v[8 * g + 6], v[8 * g + 7]);
-                ptx::tmem_ld_wait();
+            for (int q = 0; q < 4; ++q) {
+                const int c0 = 32 * q;
+                if (c0 + 32 <= ncols) {
+                    uint32_t (&w)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[c0]);
+                    ptx::tmem_ld_32cols(tacc + col_begin + c0, w);
+                } else {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    if (g >= groups) continue;
-                    if (ob == 2) {
-                        uint4 t;
-                        t.x = pack_half2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]), bf16_out);
-                        t.y = pack_half2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]), bf16_out);
-                        t.z = pack_half2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]), bf16_out);
-                        t.w = pack_half2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]), bf16_out);
-                        *reinterpret_cast<uint4*>(srow + (c0 + 8 * g) * 2) = t;
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(srow + (c0 + 8 * g) * 4);
-                        dst[0] = make_uint4(v[8 * g + 0], v[8 * g + 1], v[8 * g + 2], v[8 * g + 3]);
-                        dst[1] = make_uint4(v[8 * g + 4], v[8 * g + 5], v[8 * g + 6], v[8 * g + 7]);
-                    }
+                    for (int g = 0; g < 4; ++g)
+                        if (c0 + 8 * g + 8 <= ncols)
+                            ptx::tmem_ld_8cols(tacc + col_begin + c0 + 8 * g, v[c0 + 8 * g + 0],
+                                               v[c0 + 8 * g + 1], v[c0 + 8 * g + 2],
+                                               v[c0 + 8 * g + 3], v[c0 + 8 * g + 4],
+                                               v[c0 + 8 * g + 5], v[c0 + 8 * g + 6],
+                                               v[c0 + 8 * g + 7]);
                 }
             }
-            // The accumulator is free once this warp's loads have returned.
+            ptx::tmem_ld_wait();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar->acc_empty[acc]);
+#pragma unroll
+            for (int g = 0; g < 16; ++g) {
+                if (8 * g + 8 > ncols) continue;
+                const int c = col_begin + 8 * g;
+                if (ob == 2) {
+                    uint4 t;
+                    t.x = pack_half2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]), bf16_out);
+                    t.y = pack_half2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]), bf16_out);
+                    t.z = pack_half2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]), bf16_out);
+                    t.w = pack_half2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]), bf16_out);
+                    *reinterpret_cast<uint4*>(srow + c * 2) = t;
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(srow + c * 4);
+                    dst[0] = make_uint4(v[8 * g + 0], v[8 * g + 1], v[8 * g + 2], v[8 * g + 3]);
+                    dst[1] = make_uint4(v[8 * g + 4], v[8 * g + 5], v[8 * g + 6], v[8 * g + 7]);
+                }
+            }
             if (args.acc_bufs == 2) acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
             epilogue_bar_sync();
-            // Staging tile -> NCHW output, 16 bytes per thread per step.
+            // Staging tile -> NCHW output, 16 bytes per thread per step:
+            // consecutive threads take consecutive chunks of a (channel,
+            // row) segment, so a warp writes 512 contiguous bytes.
             const ConvHTile ht = args.ht[cu.ht];
             const int oh0 = ht.o0 + cu.rb * args.nr;
             const int oh_end = ht.o0 + ht.rows;
             const int ow0 = cu.cb * args.owc;
             for (int i = et; i < tile_chunks; i += kWtEpilogueThreads) {
-                const int j = i % seg_chunks;
-                const int seg = i / seg_chunks;
-                const int rr = seg % args.nr;
-                const int c = seg / args.nr;
+                const int seg = div_small(i, seg_chunks, inv_seg);
+                const int j = i - seg * seg_chunks;
+                const int c = div_small(seg, args.nr, inv_nr);
+                const int rr = seg - c * args.nr;
                 const int oh = oh0 + rr;
                 const int ow = ow0 + j * ch_elems;
                 if (c >= args.c_out || oh >= oh_end || ow >= args.ow) continue;
@@ -733,8 +759,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
 // NCHW -> NHWC for 16-bit elements with 16-byte accesses on both sides (C
 // and W multiples of 8, x 16-byte aligned), fused with the weight reorder.
 // A warp moves kPrepItemsPerWarp items of 64 channels x 32 columns of one
-// (image, row): lane (cg, q)
-// loads channels 8cg..8cg+7 at columns 8q..8q+7 as eight 16-byte words,
+// (image, row): lane (cg, q) loads channels 8cg..8cg+7 at columns 8q..8q+7 as eight 16-byte words,
 // transposes the 8 x 8 block with byte permutes and stores eight pixels of
 // 8 channels.  For a fixed register a warp reads 8 runs of 64 bytes and
 // writes 4 runs of 128 bytes.  Blocks past the transpose reorder the

@@ -145,6 +145,42 @@ def conv2d_htiled(x64: np.ndarray, w64: np.ndarray, stride=(1, 1), pad=(0, 0), d
     return y
 
 
+def conv2d_tiled(x64: np.ndarray, w64: np.ndarray, stride=(1, 1), pad=(0, 0), dil=(1, 1),
+                 tile_oh: int = 1, tile_ow: int | None = None, tile_n: int | None = None
+                 ) -> np.ndarray:
+    """The convolution assembled from independent sub-convolutions over
+    batch tiles, H-tiles and W-tiles.
+
+    The tutorial's slicing formulas ("H/W 维切分的通用公式") apply to each
+    spatial dimension alike: an output tile [q0, q1) of the width reads the
+    input columns [in_start, min(in_end, W)) with left pad pl' and right pad
+    pr' from the same formulas (``htile_rows`` with the width's sizes).  A
+    batch tile of images needs no halo at all (the tutorial's reason to tile
+    the batch first, "为什么教学工程先切 batch 维"): each image is its own
+    sub-problem.  Every tile convolves only its own slice.
+    """
+    x64 = np.asarray(x64, dtype=np.float64)
+    n, c, h, w = x64.shape
+    co, _, kh, kw = np.asarray(w64).shape
+    oh = out_size(h, kh, stride[0], pad[0], pad[0], dil[0])
+    ow = out_size(w, kw, stride[1], pad[1], pad[1], dil[1])
+    tile_ow = ow if tile_ow is None else tile_ow
+    tile_n = n if tile_n is None else tile_n
+    y = np.zeros((n, co, oh, ow), dtype=np.float64)
+    for n0 in range(0, n, tile_n):
+        n1 = min(n0 + tile_n, n)
+        for o0, o1 in htile_ranges(oh, tile_oh):
+            th = htile_rows(h, kh, stride[0], pad[0], dil[0], o0, o1)
+            for q0, q1 in htile_ranges(ow, tile_ow):
+                tw = htile_rows(w, kw, stride[1], pad[1], dil[1], q0, q1)
+                sl = x64[n0:n1, :, th.in_start:min(th.in_end, h), tw.in_start:min(tw.in_end, w)]
+                sub = conv2d(sl, w64, stride, (th.pt, th.pb), (tw.pt, tw.pb), dil)
+                if sub.shape[2:] != (o1 - o0, q1 - q0):
+                    raise AssertionError(f"tile [{o0},{o1})x[{q0},{q1}) produced {sub.shape[2:]}")
+                y[n0:n1, :, o0:o1, q0:q1] = sub
+    return y
+
+
 def conv2d_points(x64: np.ndarray, w64: np.ndarray, pts, stride=(1, 1), pad=(0, 0),
                   dil=(1, 1), absolute: bool = False) -> np.ndarray:
     """y (or its bound with |x|, |w|) at sampled points (n, co, oh, ow) only."""

@@ -135,3 +135,49 @@ def test_htile_rows_zero_and_negative_halo():
     # bottom pad: the last tile reaches past H
     t = C.htile_rows(H=9, kh=3, sh=2, pt=1, d=1, o0=4, o1=5)
     assert (t.in_start, t.in_end, t.pt, t.pb) == (7, 10, 0, 1)
+
+
+def test_tiled_over_batch_h_and_w_equals_untiled():
+    # The slicing formulas applied to both spatial dimensions, and batch
+    # tiles without halo, rebuild the untiled convolution exactly (integer
+    # inputs: every sum is exact in float64).
+    rng = np.random.default_rng(12)
+    checked = 0
+    for (H, W), (kh, kw), (sh, sw), (ph, pw), (dh, dw) in itertools.product(
+            ((9, 7), (16, 13), (5, 23)), ((3, 3), (2, 5), (1, 3)), ((1, 1), (2, 2), (3, 1)),
+            ((0, 0), (1, 1), (1, 2)), ((1, 1), (2, 1))):
+        if ph >= kh or pw >= kw:
+            continue
+        OH = C.out_size(H, kh, sh, ph, ph, dh)
+        OW = C.out_size(W, kw, sw, pw, pw, dw)
+        if OH <= 0 or OW <= 0:
+            continue
+        x = rng.integers(-3, 4, size=(3, 2, H, W)).astype(np.float64)
+        w = rng.integers(-2, 3, size=(2, 2, kh, kw)).astype(np.float64)
+        full = C.conv2d(x, w, (sh, sw), (ph, ph), (pw, pw), (dh, dw))
+        for tile_oh, tile_ow, tile_n in ((1, 1, 1), (2, 3, 2), (OH, 2, 3), (3, OW, 1), (4, 5, 2)):
+            tiled = C.conv2d_tiled(x, w, (sh, sw), (ph, pw), (dh, dw), tile_oh, tile_ow, tile_n)
+            assert np.array_equal(tiled, full), (H, W, kh, kw, sh, sw, ph, pw, dh, dw,
+                                                  tile_oh, tile_ow, tile_n)
+            checked += 1
+    assert checked > 200
+
+
+def test_tiled_with_full_width_is_the_h_tiling():
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((2, 3, 11, 10))
+    w = rng.standard_normal((4, 3, 3, 3))
+    a = C.conv2d_tiled(x, w, (2, 1), (1, 1), (1, 1), tile_oh=2)
+    b = C.conv2d_htiled(x, w, (2, 1), (1, 1), (1, 1), tile_oh=2)
+    assert np.array_equal(a, b)
+
+
+def test_w_tile_halo_columns():
+    # Adjacent W-tiles share (kw-1)*d + 1 - sw input columns, as rows do.
+    W, kw, sw, pw, d = 20, 3, 1, 1, 1
+    OW = C.out_size(W, kw, sw, pw, pw, d)
+    tiles = C.htile_ranges(OW, 6)
+    for (q0, q1), (r0, r1) in zip(tiles, tiles[1:]):
+        a = C.htile_rows(W, kw, sw, pw, d, q0, q1)
+        b = C.htile_rows(W, kw, sw, pw, d, r0, r1)
+        assert a.in_end - b.in_start == a.halo == 2

@@ -348,6 +348,21 @@ int tiles_gemm_batched(const tiles_gemm_desc* desc, const tiles_config* cfg, voi
 int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
                         void* workspace, size_t ws_bytes, void* stream);
 
+/* The same convolution tiled over the batch, the output height and the
+ * output width: output tiles of tile_n images x tile_oh rows x tile_ow
+ * columns, each an independent sub-convolution of its input slice.  The
+ * width's slices follow the same formulas as the rows (tutorial, "H/W 维切
+ * 分的通用公式", applied to W, kw, sw, pw, dw); images need no halo, so a
+ * batch tile is just fewer images (tutorial, "为什么教学工程先切 batch 维").
+ * tile_ow <= 0 or >= the output width means one W-tile, tile_n <= 0 or >=
+ * n one batch tile; tiles_conv2d_htiled(desc, t, ...) is
+ * tiles_conv2d_tiled(desc, t, 0, 0, ...).  W-tiles narrower than the
+ * output need the TMA producer (TILES_ERR_INFEASIBLE otherwise); tile_ow
+ * and the pads must be below 32768.  For a given producer the tiling
+ * changes no output bit: each output's K sum runs in the same order. */
+int tiles_conv2d_tiled(const tiles_conv_desc* desc, int tile_oh, int tile_ow, int tile_n,
+                       const tiles_config* cfg, void* workspace, size_t ws_bytes, void* stream);
+
 /* Workspace bytes the TMA producer needs for this convolution (256 when it
  * does not apply; 0 on invalid arguments). */
 size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh);

@@ -287,3 +287,83 @@ def test_nhwc_without_workspace_is_refused(ws):
     with pytest.raises(T.TilesError) as e:
         T.conv2d_htiled(x, w, (1, 1), (1, 1), (1, 1), 4, workspace=ws, layout="nhwc")
     assert e.value.status == -4
+
+
+# --------------------------------------------------------------------------- #
+# Tiling over the batch and the width (tiles_conv2d_tiled)
+# --------------------------------------------------------------------------- #
+
+def run_tiled(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, tile_ow, tile_n, place,
+              layout="nchw", guard=16):
+    x = to_cuda(x_np, in_dt)
+    if layout == "nhwc":
+        x = x.permute(0, 2, 3, 1).contiguous()
+    w = to_cuda(w_np, in_dt)
+    n, c, h, wd = x_np.shape
+    co, _, kh, kw = w_np.shape
+    oh = OC.out_size(h, kh, stride[0], pad[0], pad[0], dil[0])
+    ow = OC.out_size(wd, kw, stride[1], pad[1], pad[1], dil[1])
+    total = n * co * oh * ow
+    flat = torch.full((total + 2 * guard,), 2048.0, dtype=TORCH_DT[out_dt], device="cuda")
+    y = flat[guard:guard + total].view(n, co, oh, ow)
+    if place == "gather":
+        ws, cfg = T.workspace(), None
+    else:
+        ws = T.conv_workspace(x, w, stride, pad, dil, tile_oh, layout=layout)
+        acc = int(place[4:]) if place.startswith("tmem") and len(place) > 4 else 0
+        cfg = T.make_config(128, 256, 64, 4, 192, "tcgen05", acc, 1, conv_weights=place[:4])
+    T.conv2d_tiled(x, w, stride, pad, dil, tile_oh, tile_ow, tile_n, out=y, workspace=ws, cfg=cfg,
+                   layout=layout)
+    T.check(ws)
+    host = to_f64(flat)
+    assert np.all(host[:guard] == 2048.0) and np.all(host[guard + total:] == 2048.0)
+    return host[guard:guard + total].reshape(n, co, oh, ow)
+
+
+@pytest.mark.parametrize("place", ["smem", "tmem1", "tmem2"])
+@pytest.mark.parametrize("layout", ["nchw", "nhwc"])
+def test_w_and_batch_tiles_do_not_change_bits(place, layout):
+    # The width's slices follow the rows' formulas; batch tiles need no halo.
+    # For one producer every tiling gives the same bits, and the oracle's
+    # tiled convolution (exactly the untiled one) bounds them.
+    x = S.random_matrix(70, (3, 16, 21, 45), S.BF16, "normal")
+    w = S.random_matrix(71, (40, 16, 3, 3), S.BF16, "normal")
+    st, pad, dil = (2, 1), (1, 1), (1, 1)
+    base = run_tiled(x, w, S.BF16, S.F32, st, pad, dil, 4, 0, 0, place, layout)
+    for tile_ow, tile_n in ((1, 0), (5, 2), (8, 1), (17, 3), (40, 0), (45, 2)):
+        got = run_tiled(x, w, S.BF16, S.F32, st, pad, dil, 4, tile_ow, tile_n, place, layout)
+        assert np.array_equal(got, base), (tile_ow, tile_n)
+    x64, w64 = S.widen(x, S.BF16), S.widen(w, S.BF16)
+    ref = OC.conv2d_tiled(x64, w64, st, pad, dil, tile_oh=4, tile_ow=5, tile_n=2)
+    bound = OC.conv2d(np.abs(x64), np.abs(w64), st, (pad[0], pad[0]), (pad[1], pad[1]), dil)
+    ok, worst, idx = OT.check(base, ref, bound, S.F32)
+    assert ok, f"worst ratio {worst} at {idx}"
+
+
+def test_many_w_tiles_take_several_launches():
+    # 150 output columns at tile_ow 1: three launches of at most 64 W-tiles,
+    # 16-bit output with scalar stores at every tile edge.
+    x = S.random_matrix(72, (1, 8, 6, 150), S.F16)
+    w = S.random_matrix(73, (12, 8, 3, 3), S.F16)
+    got = run_tiled(x, w, S.F16, S.F16, (1, 1), (1, 1), (1, 1), 2, 1, 0, "tmem")
+    check_against_oracle(got, S.widen(x, S.F16), S.widen(w, S.F16), (1, 1), (1, 1), (1, 1), S.F16)
+
+
+def test_gather_batch_tiles_and_w_tiles_refused():
+    x = S.random_matrix(74, (5, 8, 12, 12), S.F16)
+    w = S.random_matrix(75, (16, 8, 3, 3), S.F16)
+    got = run_tiled(x, w, S.F16, S.F32, (1, 1), (1, 1), (1, 1), 3, 0, 2, "gather")
+    check_against_oracle(got, S.widen(x, S.F16), S.widen(w, S.F16), (1, 1), (1, 1), (1, 1), S.F32)
+    xt, wt_ = to_cuda(x, S.F16), to_cuda(w, S.F16)
+    with pytest.raises(T.TilesError) as e:
+        T.conv2d_tiled(xt, wt_, (1, 1), (1, 1), (1, 1), 3, 4, 0, workspace=T.workspace())
+    assert e.value.status == -4
+
+
+def test_conv_workload_tiled_over_w_and_batch():
+    wl = S.WORKLOADS["conv_htiled"]
+    x, w = S.conv_inputs(wl)
+    got = run_tiled(x, w, wl.in_dtype, wl.out_dtype, (wl.sh, wl.sw), (wl.ph, wl.pw),
+                    (wl.dh, wl.dw), wl.tile_oh, 56, 2, "tmem")
+    check_against_oracle(got, S.widen(x, wl.in_dtype), S.widen(w, wl.in_dtype), (wl.sh, wl.sw),
+                         (wl.ph, wl.pw), (wl.dh, wl.dw), wl.out_dtype)

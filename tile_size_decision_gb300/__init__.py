@@ -19,7 +19,8 @@ __all__ = [
     "TilesError", "load", "version", "device_preset", "device_query", "evaluate",
     "finish_parallelism", "c0_bytes", "plan", "htile_rows", "workspace_bytes", "workspace",
     "gemm", "gemm_batched", "gemm_schedule", "gemm_workspace", "gemm_noalloc", "gemm_autotune",
-    "tuned_lookup", "tuned_save", "tuned_load", "tuned_clear", "conv2d_htiled", "conv_workspace",
+    "tuned_lookup", "tuned_save", "tuned_load", "tuned_clear", "conv2d_htiled", "conv2d_tiled",
+    "conv_workspace",
     "conv_out_shape", "check", "selftest_wait_timeout", "make_config",
 ]
 
@@ -324,6 +325,24 @@ def conv2d_htiled(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), tile_oh=16, out=N
     wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().tiles_conv2d_htiled(C.byref(d), tile_oh, _cfg_ptr(cfg), ws, wsb,
                                       _stream_handle(stream)), "tiles_conv2d_htiled")
+    return out
+
+
+def conv2d_tiled(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), tile_oh=16, tile_ow=0, tile_n=0,
+                 out=None, out_dtype=None, cfg=None, workspace=None, stream=None, layout="nchw"):
+    """conv2d tiled over the batch (tile_n images, no halo), the output
+    height (tile_oh rows) and the output width (tile_ow columns, the same
+    slicing formulas as the rows); 0 means the whole batch or width."""
+    shape = conv_out_shape(x, w, stride, pad, dil, layout)
+    if out is None:
+        out = _alloc_out(shape, x, out_dtype)
+    if not out.is_contiguous() or tuple(out.shape) != shape:
+        raise ValueError("out must be contiguous with shape (n, c_out, oh, ow)")
+    d = _conv_desc(x, w, stride, pad, dil, out, layout)
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().tiles_conv2d_tiled(C.byref(d), tile_oh, tile_ow, tile_n, _cfg_ptr(cfg), ws,
+                                     wsb, _stream_handle(stream)), "tiles_conv2d_tiled")
     return out
 
 

@@ -815,6 +815,11 @@ int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_co
     return conv2d_htiled(desc, tile_oh, cfg, ws, ws_bytes, stream);
 }
 
+int tiles_conv2d_tiled(const tiles_conv_desc* desc, int tile_oh, int tile_ow, int tile_n,
+                       const tiles_config* cfg, void* ws, size_t ws_bytes, void* stream) {
+    return conv2d_tiled(desc, tile_oh, tile_ow, tile_n, cfg, ws, ws_bytes, stream);
+}
+
 size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh) {
     return static_cast<size_t>(conv_workspace_bytes(desc, tile_oh));
 }

@@ -298,8 +298,8 @@ PFN_cuTensorMapEncodeTiled_v12000 conv_encode_fn() {
 
 }  // namespace
 
-int conv2d_htiled(const tiles_conv_desc* d, int tile_oh, const tiles_config* cfg, void* ws,
-                  size_t ws_bytes, void* stream) {
+int conv2d_tiled(const tiles_conv_desc* d, int tile_oh, int tile_ow, int tile_n,
+                 const tiles_config* cfg, void* ws, size_t ws_bytes, void* stream) {
     if (!d) return fail(TILES_ERR_INVALID_ARG, "null descriptor");
     if (!d->x || !d->wt || !d->y) return fail(TILES_ERR_INVALID_ARG, "null tensor pointer");
     if (d->n < 1 || d->c < 1 || d->h < 1 || d->w < 1 || d->c_out < 1 || d->kh < 1 || d->kw < 1 ||
@@ -320,9 +320,14 @@ int conv2d_htiled(const tiles_conv_desc* d, int tile_oh, const tiles_config* cfg
     if (d->h + 2 * d->ph < (d->kh - 1) * d->dh + 1 || d->w + 2 * d->pw < (d->kw - 1) * d->dw + 1 ||
         oh < 1 || ow < 1)
         return fail(TILES_ERR_INVALID_ARG, "empty output");
+    // tile_ow / tile_n <= 0: the whole width / batch in one tile.
+    if (tile_ow <= 0 || tile_ow > ow) tile_ow = static_cast<int>(std::min<int64_t>(ow, INT32_MAX));
+    if (tile_n <= 0 || tile_n > d->n) tile_n = d->n;
     const int64_t tile_cols = static_cast<int64_t>(std::min<int64_t>(tile_oh, oh)) * ow;
-    if (tile_oh > 32767 || d->ph > 32767)
-        return fail(TILES_ERR_TOO_LARGE, "tile_oh and the pad must be below 32768");
+    if (tile_oh > 32767 || d->ph > 32767 || d->pw > 32767)
+        return fail(TILES_ERR_TOO_LARGE, "tile_oh and the pads must be below 32768");
+    if (tile_ow < ow && tile_ow > 32767)
+        return fail(TILES_ERR_TOO_LARGE, "tile_ow must be below 32768");
     if (k > (1 << 24) || tile_cols > (1 << 30) || static_cast<int64_t>(d->n) * d->c * d->h * d->w > (1ll << 40))
         return fail(TILES_ERR_TOO_LARGE, "convolution too large");
 
@@ -333,13 +338,30 @@ int conv2d_htiled(const tiles_conv_desc* d, int tile_oh, const tiles_config* cfg
     if (cfg && !force_tma && !force_gather)
         return fail(TILES_ERR_INFEASIBLE, "conv cfg: threads 192 (TMA producer) or 320 (gather)");
     ConvTmaGeometry g;
-    const bool tma_ok = conv_tma_geometry(d, oh, ow, tile_oh, &g);
+    const bool tma_ok = conv_tma_geometry(d, oh, ow, tile_oh, tile_ow, &g);
     if (force_tma && !tma_ok)
         return fail(TILES_ERR_INFEASIBLE, "the TMA producer does not apply to this convolution");
     if (!force_gather && tma_ok && (force_tma || (ws && static_cast<int64_t>(ws_bytes) >= g.ws_bytes)))
-        return conv2d_tma(d, cfg, tile_oh, oh, ow, g, ws, ws_bytes, stream);
+        return conv2d_tma(d, cfg, tile_oh, tile_ow, tile_n, oh, ow, g, ws, ws_bytes, stream);
     if (d->x_layout != TILES_LAYOUT_NCHW)
         return fail(TILES_ERR_INFEASIBLE, "NHWC input needs the TMA producer (and its workspace)");
+    if (tile_ow < ow)
+        return fail(TILES_ERR_INFEASIBLE, "W-tiles need the TMA producer (and its workspace)");
+    if (tile_n < d->n) {
+        // Batch tiles share no input rows: each is the same convolution on
+        // its own images (pointers moved by whole images).
+        for (int n0 = 0; n0 < d->n; n0 += tile_n) {
+            tiles_conv_desc sub = *d;
+            sub.n = std::min(tile_n, d->n - n0);
+            const int ib = bytes_of(d->in_dtype);
+            sub.x = static_cast<const char*>(d->x) +
+                    static_cast<int64_t>(n0) * d->c * d->h * d->w * ib;
+            sub.y = static_cast<char*>(d->y) + static_cast<int64_t>(n0) * d->c_out * oh * ow * ob;
+            const int s = conv2d_tiled(&sub, tile_oh, tile_ow, sub.n, cfg, ws, ws_bytes, stream);
+            if (s != TILES_OK) return s;
+        }
+        return TILES_OK;
+    }
     if (k % 8) return fail(TILES_ERR_MISALIGNED, "c*kh*kw must be a multiple of 8 (weight rows)");
     if (reinterpret_cast<uintptr_t>(d->wt) & 15u)
         return fail(TILES_ERR_MISALIGNED, "w must be 16-byte aligned");
@@ -426,7 +448,13 @@ int64_t conv_workspace_bytes(const tiles_conv_desc* d, int tile_oh) {
     const int64_t ow = (static_cast<int64_t>(d->w) + 2 * d->pw - static_cast<int64_t>(d->kw - 1) * d->dw - 1) / d->sw + 1;
     if (oh < 1 || ow < 1) return 0;
     ConvTmaGeometry g;
-    return conv_tma_geometry(d, oh, ow, tile_oh, &g) ? g.ws_bytes : 256;
+    return conv_tma_geometry(d, oh, ow, tile_oh, static_cast<int>(std::min<int64_t>(ow, INT32_MAX)), &g)
+               ? g.ws_bytes : 256;
+}
+
+int conv2d_htiled(const tiles_conv_desc* d, int tile_oh, const tiles_config* cfg, void* ws,
+                  size_t ws_bytes, void* stream) {
+    return conv2d_tiled(d, tile_oh, 0, 0, cfg, ws, ws_bytes, stream);
 }
 
 }  // namespace tiles

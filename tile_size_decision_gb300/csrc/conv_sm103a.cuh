@@ -28,8 +28,21 @@ struct ConvHTile {
 };
 static_assert(sizeof(ConvHTile) == 16, "H-tile record");
 
-// H-tiles handled by one launch (the table travels in the kernel parameters).
+// Columns of one output W-tile: the same slicing formulas as the rows
+// (computed on the host by htile_rows with the width's sizes).
+struct ConvWTile {
+    int32_t o0;         // first output column
+    int16_t cols;       // q1 - q0
+    int16_t pl;         // left pad of the sub-operator, pl'
+    int32_t in_start;   // first input column of the slice
+    int32_t unused;
+};
+static_assert(sizeof(ConvWTile) == 16, "W-tile record");
+
+// H-tiles and W-tiles handled by one launch (the tables travel in the
+// kernel parameters).
 constexpr int kConvMaxHTiles = 128;
+constexpr int kConvMaxWTiles = 64;
 // Threads of the convolution block: the GEMM's six warps plus four warps
 // that gather the im2col operand.
 constexpr int kConvThreads = 320;
@@ -44,12 +57,15 @@ struct ConvTmaGeometry {
     int64_t weights_offset, x_offset, ws_bytes;   // workspace layout
 };
 
-bool conv_tma_geometry(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh,
+// tile_ow: output columns per W-tile (the full width when >= ow).
+bool conv_tma_geometry(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, int tile_ow,
                        ConvTmaGeometry* g);
 // cfg (may be NULL): conv_weights picks the filter's place, acc_bufs the
 // TMEM accumulator count of the weights-in-TMEM form (0 = planned).
-int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, int64_t oh,
-               int64_t ow, const ConvTmaGeometry& g, void* ws, size_t ws_bytes, void* stream);
+// tile_ow >= 1 and tile_n >= 1 (W-tile width, images per launch group).
+int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, int tile_ow,
+               int tile_n, int64_t oh, int64_t ow, const ConvTmaGeometry& g, void* ws,
+               size_t ws_bytes, void* stream);
 int64_t conv_workspace_bytes(const tiles_conv_desc* d, int tile_oh);
 
 struct ConvArgs {

@@ -44,6 +44,8 @@ struct ConvTmaArgs {
     int32_t owc, nr;                      // pixel tile: nr rows x owc columns (= 128)
     int32_t nco;                          // output channels per tile (MMA N)
     int32_t rblocks, cblocks, co_blocks, ch_blocks, k_blocks, n_htiles, units;
+    int32_t n_wtiles;                     // W-tiles in this launch (cblocks column blocks each)
+    int32_t img0;                         // first image of this launch's batch tile
     uint32_t tx_bytes;                    // bytes the boxes of a stage deliver
     int32_t vec_ok;                       // 16-byte output stores are aligned (OW % 8 == 0)
     int32_t w_resident;                   // weights loaded once into shared memory
@@ -64,16 +66,22 @@ struct ConvTmaArgs {
     int32_t bar_off;                      // barrier block offset (bytes)
     int32_t w_slots;                      // 16 KB filter blocks per start-up pass
     ConvHTile ht[kConvMaxHTiles];
+    ConvWTile wt[kConvMaxWTiles];
 };
 
-struct ConvUnit { int img, ht, rb, cb, mb; };
+struct ConvUnit { int img, ht, rb, wt, cb, mb; };
 
+// Unit index -> (image, H-tile, row block, W-tile, column block, channel
+// block), the channel and column blocks fastest.  img counts from the
+// launch's first image (args.img0).
 __device__ __forceinline__ ConvUnit decode_conv_unit(int u, const ConvTmaArgs& a) {
     ConvUnit c;
     c.mb = u % a.co_blocks;
     u /= a.co_blocks;
     c.cb = u % a.cblocks;
     u /= a.cblocks;
+    c.wt = u % a.n_wtiles;
+    u /= a.n_wtiles;
     c.rb = u % a.rblocks;
     u /= a.rblocks;
     c.ht = u % a.n_htiles;
@@ -216,8 +224,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // Input row and column under the unit's first output pixel,
                 // placed by the H-tile's slice: in_start - pt' is the row of
                 // the window over the tile's first output row.
+                const ConvWTile wt = args.wt[cu.wt];
                 const int row0 = ht.in_start - ht.pt + cu.rb * args.nr * args.sh;
-                const int col0 = cu.cb * args.owc * args.sw - args.pw;
+                const int col0 = wt.in_start - wt.pl + cu.cb * args.owc * args.sw;
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
                     const int tap = kb / args.ch_blocks;
                     const int chb = kb - tap * args.ch_blocks;
@@ -231,7 +240,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint8_t* st = ring + stage * stage_bytes;
                     ptx::mbar_arrive_expect_tx(&bar->full[stage], args.tx_bytes);
                     tma_load_4d(st, &tmX, &bar->full[stage], chb * 64, col0 + s * args.dw,
-                                row0 + r * args.dh, cu.img);
+                                row0 + r * args.dh, args.img0 + cu.img);
                     if (!args.w_resident)
                         ptx::tma_load_3d(st + kTmaConvA, &tmW, &bar->full[stage], kb * 64,
                                          cu.mb * args.nco, 0);
@@ -316,11 +325,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             ptx::tc_fence_after();
             const ConvHTile ht = args.ht[cu.ht];
+            const ConvWTile wt = args.wt[cu.wt];
+            const int ow_end = wt.o0 + wt.cols;               // the W-tile's last column + 1
+            const int img = args.img0 + cu.img;
             const int oh = ht.o0 + cu.rb * args.nr + rr;
-            const int ow = cu.cb * args.owc + cc;
-            const bool pix_ok = rr < args.nr && oh < ht.o0 + ht.rows && ow < args.ow;
+            const int ow = wt.o0 + cu.cb * args.owc + cc;
+            const bool pix_ok = rr < args.nr && oh < ht.o0 + ht.rows && ow < ow_end;
             // Element index of (img, co = 0, oh, ow); channel co adds co * plane.
-            const int64_t pix = static_cast<int64_t>(cu.img) * args.c_out * plane +
+            const int64_t pix = static_cast<int64_t>(img) * args.c_out * plane +
                                 static_cast<int64_t>(oh) * args.ow + ow;
             const uint32_t tacc = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kTmaConvMaxN;
             // 16-bit output: the 8 lanes of a group hold 8 consecutive pixels of
@@ -331,9 +343,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int pg = quarter * 32 + g8 * 8;              // first pixel of the group
             const int rr_g = pg / args.owc;
             const int oh_g = ht.o0 + cu.rb * args.nr + rr_g;
-            const int ow_g = cu.cb * args.owc + (pg - rr_g * args.owc);
+            const int ow_g = wt.o0 + cu.cb * args.owc + (pg - rr_g * args.owc);
             const bool row_g = rr_g < args.nr && oh_g < ht.o0 + ht.rows;
-            const int64_t pix_g = static_cast<int64_t>(cu.img) * args.c_out * plane +
+            const int64_t pix_g = static_cast<int64_t>(img) * args.c_out * plane +
                                   static_cast<int64_t>(oh_g) * args.ow + ow_g;
             const bool half_out = args.out_dtype != TILES_F32;
             const bool bf16_out = args.out_dtype == TILES_BF16;
@@ -355,13 +367,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (!row_g || co >= args.c_out) continue;
                         uint16_t* dst = static_cast<uint16_t*>(args.y) + pix_g +
                                         static_cast<int64_t>(co) * plane;
-                        if (args.vec_ok && ow_g + 8 <= args.ow) {
+                        if (args.vec_ok && ow_g + 8 <= ow_end) {
                             *reinterpret_cast<uint4*>(dst) = make_uint4(w0, w1, w2, w3);
                         } else {
                             const uint32_t wv[4] = {w0, w1, w2, w3};
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                if (ow_g + e < args.ow)
+                                if (ow_g + e < ow_end)
                                     dst[e] = static_cast<uint16_t>(wv[e >> 1] >> ((e & 1) * 16));
                         }
                     }
@@ -530,8 +542,9 @@ __global__ void __launch_bounds__(kWtThreads, 1)
             for (int u = blockIdx.x; u < args.units && !aborted; u += gridDim.x) {
                 const ConvUnit cu = decode_conv_unit(u, args);
                 const ConvHTile ht = args.ht[cu.ht];
+                const ConvWTile wt = args.wt[cu.wt];
                 const int row0 = ht.in_start - ht.pt + cu.rb * args.nr * args.sh;
-                const int col0 = cu.cb * args.owc * args.sw - args.pw;
+                const int col0 = wt.in_start - wt.pl + cu.cb * args.owc * args.sw;
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
                     const int tap = kb / args.ch_blocks;
                     const int chb = kb - tap * args.ch_blocks;
@@ -545,7 +558,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                     uint8_t* st = ring + stage * stage_bytes;
                     ptx::mbar_arrive_expect_tx(&bar->full[stage], args.tx_bytes);
                     tma_load_4d(st, &tmX, &bar->full[stage], chb * 64, col0 + s * args.dw,
-                                row0 + r * args.dh, cu.img);
+                                row0 + r * args.dh, args.img0 + cu.img);
                     ++issued;
                     if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
                 }
@@ -713,9 +726,12 @@ __global__ void __launch_bounds__(kWtThreads, 1)
             // consecutive threads take consecutive chunks of a (channel,
             // row) segment, so a warp writes 512 contiguous bytes.
             const ConvHTile ht = args.ht[cu.ht];
+            const ConvWTile wt = args.wt[cu.wt];
             const int oh0 = ht.o0 + cu.rb * args.nr;
             const int oh_end = ht.o0 + ht.rows;
-            const int ow0 = cu.cb * args.owc;
+            const int ow0 = wt.o0 + cu.cb * args.owc;
+            const int ow_end = wt.o0 + wt.cols;
+            const int img = args.img0 + cu.img;
             for (int i = et; i < tile_chunks; i += kWtEpilogueThreads) {
                 const int seg = div_small(i, seg_chunks, inv_seg);
                 const int j = i - seg * seg_chunks;
@@ -723,19 +739,19 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                 const int rr = seg - c * args.nr;
                 const int oh = oh0 + rr;
                 const int ow = ow0 + j * ch_elems;
-                if (c >= args.c_out || oh >= oh_end || ow >= args.ow) continue;
+                if (c >= args.c_out || oh >= oh_end || ow >= ow_end) continue;
                 const uint8_t* src = staging + c * args.stg_pitch + (rr * args.owc + j * ch_elems) * ob;
                 const uint4 t = *reinterpret_cast<const uint4*>(src);
-                const int64_t idx = (static_cast<int64_t>(cu.img) * args.c_out + c) * plane +
+                const int64_t idx = (static_cast<int64_t>(img) * args.c_out + c) * plane +
                                     static_cast<int64_t>(oh) * args.ow + ow;
                 char* dst = static_cast<char*>(args.y) + idx * ob;
-                if (args.vec_ok && ow + ch_elems <= args.ow) {
+                if (args.vec_ok && ow + ch_elems <= ow_end) {
                     *reinterpret_cast<uint4*>(dst) = t;
                 } else {
                     const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        if (e >= ch_elems || ow + e >= args.ow) continue;
+                        if (e >= ch_elems || ow + e >= ow_end) continue;
                         if (ob == 2)
                             reinterpret_cast<uint16_t*>(dst)[e] =
                                 static_cast<uint16_t>(w4[e >> 1] >> ((e & 1) * 16));
@@ -919,10 +935,11 @@ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 // pixel tile is nr rows x owc columns = 128 pixels, owc a power of two from
 // 8 to 128, chosen to compute the fewest pixels over an H-tile (ties: the
 // wider rows); output channels go in blocks of up to 256 (a multiple of 16).
-bool conv_tma_geometry(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh,
+bool conv_tma_geometry(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, int tile_ow,
                        ConvTmaGeometry* g) {
     if (d->c % 8 || d->sw > 8 || d->sh > 8 || d->dw < 1 || d->dh < 1) return false;
     const int64_t rows = std::min<int64_t>(tile_oh, oh);
+    ow = std::min<int64_t>(tile_ow, ow);     // columns of one W-tile
     int64_t best_cost = -1;
     int owc = 0;
     for (int cols = 128; cols >= 8; cols /= 2) {
@@ -959,14 +976,16 @@ struct WtPlan {
 // with one accumulator, the drain before the next tile (2 * npix + 400);
 // tiles run in rounds over the SMs.  forced_acc = 1 or 2 fixes the count.
 // False when the filter does not fit.
-bool wtmem_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, int64_t k_blocks,
-                int sms, int forced_acc, WtPlan* out) {
+bool wtmem_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, int tile_ow,
+                int64_t k_blocks, int sms, int forced_acc, WtPlan* out) {
     if (d->c_out > 128) return false;
     const int64_t a_cols = k_blocks * 32;
     const int ob = d->out_dtype == TILES_F32 ? 4 : 2;
     const int budget = 227 * 1024 - kSmemBarrierBytes - kSmemAlignSlack;
     const int64_t rows = std::min<int64_t>(tile_oh, oh);
     const int64_t n_ht = (oh + tile_oh - 1) / tile_oh;
+    const int64_t n_wt = (ow + tile_ow - 1) / tile_ow;
+    ow = std::min<int64_t>(tile_ow, ow);     // columns of one W-tile
     int64_t best = -1;
     for (int acc = 1; acc <= 2; ++acc) {
         if (forced_acc && acc != forced_acc) continue;
@@ -981,7 +1000,7 @@ bool wtmem_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, i
                 const int stages = std::min(kMaxStages, (budget - stg) / stage);
                 if (stages < 2) continue;
                 const int64_t units = static_cast<int64_t>(d->n) * n_ht * ((rows + nr - 1) / nr) *
-                                      ((ow + owc - 1) / owc);
+                                      n_wt * ((ow + owc - 1) / owc);
                 const int64_t per_unit = k_blocks * std::max<int64_t>(2 * npix, 345) +
                                          (acc == 1 ? 2 * npix + 400 : 0);
                 const int64_t cost = (units + sms - 1) / sms * per_unit;
@@ -1014,8 +1033,9 @@ cudaError_t set_smem_attr(const void* fn, std::atomic<int>* cached, int smem) {
 }
 std::atomic<int> g_smem_wtmem{0}, g_smem_tma{0};
 
-int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, int64_t oh,
-               int64_t ow, const ConvTmaGeometry& g, void* ws, size_t ws_bytes, void* stream) {
+int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, int tile_ow,
+               int tile_n, int64_t oh, int64_t ow, const ConvTmaGeometry& g, void* ws,
+               size_t ws_bytes, void* stream) {
     const int weights_mode = cfg ? cfg->conv_weights : TILES_CONV_W_AUTO;
     if (!ws || static_cast<int64_t>(ws_bytes) < g.ws_bytes)
         return fail(TILES_ERR_INVALID_ARG, "the TMA convolution needs %lld workspace bytes",
@@ -1037,7 +1057,7 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     WtPlan wp;
     bool use_tmem = false;
     if (weights_mode != TILES_CONV_W_SMEM)
-        use_tmem = wtmem_plan(d, oh, ow, tile_oh, k_blocks, sms,
+        use_tmem = wtmem_plan(d, oh, ow, tile_oh, tile_ow, k_blocks, sms,
                               weights_mode == TILES_CONV_W_TMEM ? forced_acc : 0, &wp);
     if (weights_mode == TILES_CONV_W_TMEM && !use_tmem)
         return fail(TILES_ERR_INFEASIBLE,
@@ -1095,7 +1115,9 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     a.sh = d->sh; a.sw = d->sw; a.pw = d->pw; a.dh = d->dh; a.dw = d->dw;
     a.oh = static_cast<int32_t>(oh); a.ow = static_cast<int32_t>(ow);
     a.owc = owc; a.nr = nr;
-    a.cblocks = static_cast<int32_t>((ow + owc - 1) / owc);
+    // Column blocks per W-tile (each W-tile's columns start a block).
+    const int64_t wcols = std::min<int64_t>(tile_ow, ow);
+    a.cblocks = static_cast<int32_t>((wcols + owc - 1) / owc);
     a.ch_blocks = g.ch_blocks;
     a.k_blocks = static_cast<int32_t>(k_blocks);
     a.out_dtype = d->out_dtype;
@@ -1114,7 +1136,10 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         a.nco = 128;
         a.co_blocks = 1;
         a.tx_bytes = static_cast<uint32_t>(a.npix * 128);
-        a.vec_ok = (y16 && ow % (d->out_dtype == TILES_F32 ? 4 : 8) == 0) ? 1 : 0;
+        {
+            const int chunk = d->out_dtype == TILES_F32 ? 4 : 8;
+            a.vec_ok = (y16 && ow % chunk == 0 && (wcols == ow || tile_ow % chunk == 0)) ? 1 : 0;
+        }
         a.idesc = ptx::idesc_f16_f32acc(d->in_dtype == TILES_BF16, false, 128, a.npix);
         a.stages = wp.stages;
         a.stg_off = wp.stages * a.npix * 128;
@@ -1141,7 +1166,7 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         a.co_blocks = (d->c_out + g.bn - 1) / g.bn;
         // TMA loads ceil(box / stride) elements per dimension: 64 channels
         // x owc x nr = 128 pixel rows of 128 bytes, and bn weight rows.
-        a.vec_ok = (y16 && ow % 8 == 0) ? 1 : 0;
+        a.vec_ok = (y16 && ow % 8 == 0 && (wcols == ow || tile_ow % 8 == 0)) ? 1 : 0;
         a.w_resident = w_resident ? 1 : 0;
         a.w_bytes = static_cast<uint32_t>(w_res_bytes);
         a.tx_bytes = static_cast<uint32_t>(kTmaConvA + (w_resident ? 0 : g.bn * 128));
@@ -1182,48 +1207,76 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "conv prep: %s", cudaGetErrorString(e));
 
+    // Launches: batch tiles (images need no halo) x chunks of up to
+    // kConvMaxHTiles H-tiles x chunks of up to kConvMaxWTiles W-tiles.
     const int64_t n_ht_total = (oh + tile_oh - 1) / tile_oh;
-    for (int64_t first = 0; first < n_ht_total; first += kConvMaxHTiles) {
-        const int count = static_cast<int>(std::min<int64_t>(kConvMaxHTiles, n_ht_total - first));
-        int max_rows = 0;
-        for (int i = 0; i < count; ++i) {
-            const int o0 = static_cast<int>((first + i) * tile_oh);
-            const int o1 = static_cast<int>(std::min<int64_t>(o0 + tile_oh, oh));
-            tiles_htile t;
-            int s = htile_rows(d->h, d->kh, d->sh, d->ph, d->dh, o0, o1, &t);
-            if (s != TILES_OK) return fail(s, "htile_rows failed");
-            a.ht[i].o0 = o0;
-            a.ht[i].rows = static_cast<int16_t>(o1 - o0);
-            a.ht[i].pt = static_cast<int16_t>(t.pt);
-            a.ht[i].in_start = t.in_start;
-            a.ht[i].real_rows = std::max(0, std::min(t.in_end, d->h) - t.in_start);
-            max_rows = std::max(max_rows, o1 - o0);
+    const int64_t n_wt_total = (ow + tile_ow - 1) / tile_ow;
+    for (int n0 = 0; n0 < d->n; n0 += tile_n) {
+        const int n_imgs = std::min(tile_n, d->n - n0);
+        a.img0 = n0;
+        for (int64_t hfirst = 0; hfirst < n_ht_total; hfirst += kConvMaxHTiles) {
+            const int hcount = static_cast<int>(std::min<int64_t>(kConvMaxHTiles, n_ht_total - hfirst));
+            int max_rows = 0;
+            for (int i = 0; i < hcount; ++i) {
+                const int o0 = static_cast<int>((hfirst + i) * tile_oh);
+                const int o1 = static_cast<int>(std::min<int64_t>(o0 + tile_oh, oh));
+                tiles_htile t;
+                int s = htile_rows(d->h, d->kh, d->sh, d->ph, d->dh, o0, o1, &t);
+                if (s != TILES_OK) return fail(s, "htile_rows failed");
+                a.ht[i].o0 = o0;
+                a.ht[i].rows = static_cast<int16_t>(o1 - o0);
+                a.ht[i].pt = static_cast<int16_t>(t.pt);
+                a.ht[i].in_start = t.in_start;
+                a.ht[i].real_rows = std::max(0, std::min(t.in_end, d->h) - t.in_start);
+                max_rows = std::max(max_rows, o1 - o0);
+            }
+            a.n_htiles = hcount;
+            a.rblocks = (max_rows + nr - 1) / nr;
+            for (int64_t wfirst = 0; wfirst < n_wt_total; wfirst += kConvMaxWTiles) {
+                const int wcount =
+                    static_cast<int>(std::min<int64_t>(kConvMaxWTiles, n_wt_total - wfirst));
+                for (int i = 0; i < wcount; ++i) {
+                    // The width's tiles follow the same slicing formulas.
+                    const int q0 = static_cast<int>((wfirst + i) * tile_ow);
+                    const int q1 = static_cast<int>(std::min<int64_t>(q0 + tile_ow, ow));
+                    tiles_htile t;
+                    int s = htile_rows(d->w, d->kw, d->sw, d->pw, d->dw, q0, q1, &t);
+                    if (s != TILES_OK) return fail(s, "htile_rows (width) failed");
+                    a.wt[i].o0 = q0;
+                    a.wt[i].cols = static_cast<int16_t>(q1 - q0);
+                    a.wt[i].pl = static_cast<int16_t>(t.pt);
+                    a.wt[i].in_start = t.in_start;
+                    a.wt[i].unused = 0;
+                }
+                a.n_wtiles = wcount;
+                const int64_t units = static_cast<int64_t>(n_imgs) * hcount * a.rblocks * wcount *
+                                      a.cblocks * a.co_blocks;
+                if (units > INT32_MAX) return fail(TILES_ERR_TOO_LARGE, "too many tiles");
+                a.units = static_cast<int32_t>(units);
+                // Programmatic serialization: the blocks launch while the
+                // previous kernel on the stream drains and wait for it
+                // in-kernel.
+                cudaLaunchConfig_t lc{};
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                lc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(units, sms)));
+                lc.dynamicSmemBytes = static_cast<size_t>(smem);
+                lc.stream = st;
+                lc.attrs = attr;
+                lc.numAttrs = 1;
+                if (use_tmem) {
+                    lc.blockDim = dim3(kWtThreads);
+                    e = cudaLaunchKernelEx(&lc, conv_wtmem_kernel, tw, tx, a);
+                } else {
+                    lc.blockDim = dim3(kGemmThreads);
+                    e = cudaLaunchKernelEx(&lc, conv_tma_kernel, tw, tx, a, stages, stage_bytes);
+                }
+                if (e == cudaSuccess) e = cudaGetLastError();
+                if (e != cudaSuccess)
+                    return fail(TILES_ERR_CUDA, "conv launch: %s", cudaGetErrorString(e));
+            }
         }
-        a.n_htiles = count;
-        a.rblocks = (max_rows + nr - 1) / nr;
-        const int64_t units = static_cast<int64_t>(d->n) * count * a.rblocks * a.cblocks * a.co_blocks;
-        if (units > INT32_MAX) return fail(TILES_ERR_TOO_LARGE, "too many tiles");
-        a.units = static_cast<int32_t>(units);
-        // Programmatic serialization: the blocks launch while the
-        // preparation kernel drains and wait for it in-kernel.
-        cudaLaunchConfig_t lc{};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        lc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(units, sms)));
-        lc.dynamicSmemBytes = static_cast<size_t>(smem);
-        lc.stream = st;
-        lc.attrs = attr;
-        lc.numAttrs = 1;
-        if (use_tmem) {
-            lc.blockDim = dim3(kWtThreads);
-            e = cudaLaunchKernelEx(&lc, conv_wtmem_kernel, tw, tx, a);
-        } else {
-            lc.blockDim = dim3(kGemmThreads);
-            e = cudaLaunchKernelEx(&lc, conv_tma_kernel, tw, tx, a, stages, stage_bytes);
-        }
-        if (e == cudaSuccess) e = cudaGetLastError();
-        if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "conv launch: %s", cudaGetErrorString(e));
     }
     return TILES_OK;
 }

@@ -63,6 +63,8 @@ constexpr int kMaxTailParts = 8;
 void device_preset_h100(tiles_device* d);
 void device_preset_gb300(tiles_device* d);
 int htile_rows(int H, int kh, int sh, int pt, int d, int o0, int o1, tiles_htile* t);
+int conv2d_tiled(const tiles_conv_desc* desc, int tile_oh, int tile_ow, int tile_n,
+                 const tiles_config* cfg, void* ws, size_t ws_bytes, void* stream);
 int conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg, void* ws,
                   size_t ws_bytes, void* stream);
 

@@ -327,6 +327,12 @@ def gemm_job(wl, dev, tiles, torch):
                      round(r["us"], 2)] for r in rows if r["status"] == 0]}
 
     j.autotune = autotune
+    c_lib = torch.empty_like(j.out)
+
+    def library_step():
+        torch.matmul(a_d, b_d, out=c_lib)
+
+    j.library_step = library_step if j.out.dtype == a_d.dtype else None
     return j
 
 
@@ -452,6 +458,27 @@ def run_ours(args, rank, world, local_rank):
 
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, world, dev)
 
+    # Context only (not on this library's path): cuBLAS through torch.matmul
+    # on the same operands, timed the same way.
+    context = None
+    if getattr(job, "library_step", None) is not None:
+        lib_ms = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            s_ev = torch.cuda.Event(enable_timing=True)
+            e_ev = torch.cuda.Event(enable_timing=True)
+            s_ev.record(stream)
+            job.library_step()
+            e_ev.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                lib_ms.append(s_ev.elapsed_time(e_ev))
+        lib_mean = float(np.mean(lib_ms))
+        context = {"cublas_torch_matmul": {
+            "ms_per_step": round(lib_mean, 5),
+            "tflops": round(job.flops / (lib_mean * 1e-3) / 1e12, 2),
+            "note": "torch.matmul on the same device tensors; context, not a baseline"}}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, secs, _, desc = job.oracle(args.cpu_seconds)
@@ -507,6 +534,8 @@ def run_ours(args, rank, world, local_rank):
             "kernel_ms_median": round(float(np.median(kernel_ms)), 5),
             "cpu_baseline": cpu,
         }
+        if context is not None:
+            line["context"] = context
         if args.workload != "gemm_4096":
             line["metric"] = f"TFLOP/s of {args.workload} (a parity workload, not the headline)"
         print(json.dumps(line), flush=True)

@@ -576,6 +576,10 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            // Pixel rows K-major: 16 channels = 32 bytes of each 128-byte row,
+            // 8-row groups 1024 B apart; stages and K steps move the
+            // descriptor's start-address field (address >> 4, no carry).
+            const uint64_t b_desc0 = ptx::smem_desc_sw128(ptx::smem_addr(ring), 16, 1024);
             bool ok = !has_work || ptx::mbar_wait(&bar->wready, 0, abort, limit);
             if (!ok) raise_error(args.err, abort, kErrMma);
             ptx::tc_fence_after();
@@ -593,15 +597,12 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t b0 = ptx::smem_addr(ring + stage * stage_bytes);
+                    const uint64_t b_st = b_desc0 + ((stage * stage_bytes) >> 4);
                     const uint32_t a0 = tmem + static_cast<uint32_t>(args.a_col + kb * 32);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // 16 channels: 8 TMEM columns of A, 32 bytes of each
-                        // 128-byte pixel row of B.
-                        const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                        ptx::mma_f16_tmem_a(d, a0 + kk * 8, bd, args.idesc, (kb | kk) != 0);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)   // 16 channels: 8 TMEM columns of A
+                        ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_st + kk * (32 >> 4), args.idesc,
+                                            (kb | kk) != 0);
                     ptx::mma_commit<1>(&bar->empty[stage]);
                     if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
                 }

@@ -363,6 +363,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (leader CTA) ----------------
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            // Descriptors of stage 0's operands; a stage or K step moves the
+            // start-address field (address >> 4, 14 bits: shared-memory
+            // addresses stay below 256 KB, so the sums never carry out).
+            //  A, K-major: 16 K elements = 32 bytes inside the 128-byte
+            //  swizzle row; 8-row groups 1024 B apart.
+            //  B, MN-major: 16 K rows = two 8-row groups of 1024 B; 64-column
+            //  atoms B_CHUNK apart.
+            const uint64_t a_desc0 = ptx::smem_desc_sw128(ptx::smem_addr(smA), 16, 1024);
+            const uint64_t b_desc0 = ptx::smem_desc_sw128(ptx::smem_addr(smB), L::B_CHUNK, 1024);
             for (int u = group; u < args.units; u += groups) {
                 const UnitCoord uc = decode_unit<BN>(u, args);
                 const uint32_t idesc = uc.width == BN ? args.idesc : args.idesc_half;
@@ -380,18 +389,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t a0 = ptx::smem_addr(smA + stage * L::A_BYTES);
-                    const uint32_t b0 = ptx::smem_addr(smB + stage * L::B_BYTES);
+                    const uint64_t a_st = a_desc0 + ((stage * L::A_BYTES) >> 4);
+                    const uint64_t b_st = b_desc0 + ((stage * L::B_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < L::BK / 16; ++kk) {
-                        // A, K-major: 16 K elements = 32 bytes inside the
-                        // 128-byte swizzle row; 8-row groups 1024 B apart.
-                        const uint64_t ad = ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                        // B, MN-major: 16 K rows = two 8-row groups of
-                        // 1024 B; 64-column atoms B_CHUNK apart.
-                        const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 2048, L::B_CHUNK, 1024);
-                        ptx::mma_f16<CG>(d, ad, bd, idesc, (kb != uc.kb0 || kk != 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < L::BK / 16; ++kk)
+                        ptx::mma_f16<CG>(d, a_st + kk * (32 >> 4), b_st + kk * (2048 >> 4), idesc,
+                                         (kb != uc.kb0 || kk != 0) ? 1u : 0u);
                     ptx::mma_commit<CG>(&bar->empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }

@@ -126,11 +126,18 @@ typedef struct {
 /* Where the TMA convolution keeps the filter (tiles_config.conv_weights).
  * TMEM: the weights are the MMA's A operand in tensor memory (M = 128
  * output channels, N = a tile of output pixels); it applies when c_out <=
- * 128 and the K columns plus two accumulators fit the 512 columns.  SMEM:
- * the weights are the B operand in shared memory (M = 128 output pixels,
- * N = a block of output channels); it applies to every TMA convolution. */
+ * 128 and the K columns plus one accumulator fit the 512 columns; each
+ * (filter tap, 64 channels) is one pixel box.  TMEM_ROWS: the same filter
+ * placement with one output row per tile, whose input rows are loaded once
+ * per (kernel row, 64 channels) as stride phases and shared by all the
+ * row's taps through shifted descriptors (kw <= 8, the row's input span
+ * within one TMA box).  SMEM: the weights are the B operand in shared
+ * memory (M = 128 output pixels, N = a block of output channels); it
+ * applies to every TMA convolution.  AUTO takes the first of TMEM_ROWS,
+ * TMEM, SMEM that applies. */
 typedef enum {
-    TILES_CONV_W_AUTO = 0, TILES_CONV_W_SMEM = 1, TILES_CONV_W_TMEM = 2
+    TILES_CONV_W_AUTO = 0, TILES_CONV_W_SMEM = 1, TILES_CONV_W_TMEM = 2,
+    TILES_CONV_W_TMEM_ROWS = 3
 } tiles_conv_weights;
 
 /* Schedules of a last round of tiles that would leave resident CTA groups

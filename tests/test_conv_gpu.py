@@ -59,7 +59,7 @@ def run_conv(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, ws, guard=0, 
     if producer.startswith("tma"):
         ws = T.conv_workspace(x, w, stride, pad, dil, tile_oh, layout=layout)
         place = producer[4:] or "auto"
-        acc = int(place[4:]) if place.startswith("tmem") and len(place) > 4 else 0
+        acc = int(place[4:]) if place.startswith(("tmem", "rows")) and len(place) > 4 else 0
         cfg = T.make_config(128, 256, 64, 4, 192, "tcgen05", acc, 1,
                             conv_weights=place[:4] if place != "auto" else "auto")
     else:
@@ -162,7 +162,7 @@ def test_rejects_unaligned_weights(ws):
 # The TMA im2col producer
 # --------------------------------------------------------------------------- #
 
-PLACES = ["smem", "tmem1", "tmem2"]
+PLACES = ["smem", "tmem1", "tmem2", "rows"]
 
 
 @pytest.mark.parametrize("case", TINY, ids=lambda c: "_".join(str(v) for v in c[:7]))
@@ -170,7 +170,7 @@ PLACES = ["smem", "tmem1", "tmem2"]
 @pytest.mark.parametrize("place", PLACES)
 def test_tma_tiny_against_loops(ws, case, layout, place):
     n, c, h, wd, co, kh, kw, st, pad, dil, tile = case
-    if place.startswith("tmem") and not tmem_fits(c, co, kh, kw):
+    if place.startswith(("tmem", "rows")) and not tmem_fits(c, co, kh, kw):
         pytest.skip("filter does not fit tensor memory")
     x = S.random_matrix(1, (n, c, h, wd), S.F16)
     w = S.random_matrix(2, (co, c, kh, kw), S.F16)
@@ -190,7 +190,7 @@ def test_tma_tiny_against_loops(ws, case, layout, place):
 def test_tma_integer_inputs_exact(ws, dt, place):
     # 72 channels are 18 K blocks, more than tensor memory holds next to
     # the accumulators; the TMEM form takes 48 (one zero-padded block).
-    c = 72 if place == "smem" else 48
+    c = 72 if place == "smem" else 48   # the tensor-memory forms hold 48 channels' filter
     x = S.integer_matrix(3, (2, c, 30, 28), dt)
     w = S.integer_matrix(4, (40, c, 3, 3), dt)
     got = run_conv(x, w, dt, S.F32, (2, 2), (1, 1), (1, 1), 4, ws, producer="tma_" + place)
@@ -257,7 +257,7 @@ def test_default_producer_with_workspace_is_tma(ws):
 
 
 @pytest.mark.parametrize("out_dt", [S.F16, S.BF16, S.F32])
-@pytest.mark.parametrize("place", ["tmem", "tmem1", "tmem2"])
+@pytest.mark.parametrize("place", ["tmem", "tmem1", "tmem2", "rows", "rows1", "rows2"])
 def test_tmem_weights_ragged_channels_and_columns(ws, out_dt, place):
     # c_out below 128 (zero rows of the tensor-memory filter), a channel
     # count that is not a multiple of 64, odd output widths (scalar tails)
@@ -310,7 +310,7 @@ def run_tiled(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, tile_ow, til
         ws, cfg = T.workspace(), None
     else:
         ws = T.conv_workspace(x, w, stride, pad, dil, tile_oh, layout=layout)
-        acc = int(place[4:]) if place.startswith("tmem") and len(place) > 4 else 0
+        acc = int(place[4:]) if place.startswith(("tmem", "rows")) and len(place) > 4 else 0
         cfg = T.make_config(128, 256, 64, 4, 192, "tcgen05", acc, 1, conv_weights=place[:4])
     T.conv2d_tiled(x, w, stride, pad, dil, tile_oh, tile_ow, tile_n, out=y, workspace=ws, cfg=cfg,
                    layout=layout)
@@ -367,3 +367,17 @@ def test_conv_workload_tiled_over_w_and_batch():
                     (wl.dh, wl.dw), wl.tile_oh, 56, 2, "tmem")
     check_against_oracle(got, S.widen(x, wl.in_dtype), S.widen(w, wl.in_dtype), (wl.sh, wl.sw),
                          (wl.ph, wl.pw), (wl.dh, wl.dw), wl.out_dtype)
+
+
+@pytest.mark.parametrize("st,dil,kw", [((1, 1), (1, 1), 3), ((2, 2), (1, 1), 3), ((1, 3), (1, 2), 5),
+                                       ((2, 2), (1, 3), 3), ((1, 1), (1, 1), 5), ((3, 2), (1, 1), 4)])
+def test_rows_form_strides_and_dilations(st, dil, kw):
+    # Tap s reads stride phase (s*dw) % sw from pixel (s*dw) // sw on: one,
+    # two or more phase planes per input row, shifted descriptors for the rest.
+    x = S.random_matrix(80, (2, 16, 15, 61), S.BF16, "normal")
+    w = S.random_matrix(81, (24, 16, 3, kw), S.BF16, "normal")
+    pad = (1, kw // 2)
+    got = run_tiled(x, w, S.BF16, S.F32, st, pad, dil, 4, 0, 0, "rows")
+    smem = run_tiled(x, w, S.BF16, S.F32, st, pad, dil, 4, 0, 0, "smem")
+    assert np.array_equal(got, smem)
+    check_against_oracle(got, S.widen(x, S.BF16), S.widen(w, S.BF16), st, pad, dil, S.F32)

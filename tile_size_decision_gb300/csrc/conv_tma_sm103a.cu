@@ -23,6 +23,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 #include <cudaTypedefs.h>
 
 #include "conv_sm103a.cuh"
@@ -65,6 +66,14 @@ struct ConvTmaArgs {
     int32_t stg_off, stg_pitch;           // staging tile: offset and row pitch (bytes)
     int32_t bar_off;                      // barrier block offset (bytes)
     int32_t w_slots;                      // 16 KB filter blocks per start-up pass
+    int32_t stage_b;                      // bytes of one ring stage
+    // Rows form (conv_wtmem_kernel<true>): a stage is one kernel row r and
+    // 64 channels; its n_planes stride phases of the input row hold pmax
+    // pixels each, plane_bytes apart; tap s reads plane tap_plane[s] from
+    // pixel tap_shift[s] on.  k_stages = kh * ch_blocks (else k_blocks).
+    int32_t k_stages, n_planes, plane_bytes, pmax;
+    int32_t tma_store;                    // rows form: the staged tile leaves by one TMA store
+    int32_t tap_plane[8], tap_shift[8], plane_phase[8];
     ConvHTile ht[kConvMaxHTiles];
     ConvWTile wt[kConvMaxWTiles];
 };
@@ -460,9 +469,16 @@ __device__ __forceinline__ bool epilogue_bar_and(bool flag) {
     return r != 0;
 }
 
+// ROWS = false: one pixel box per (tap, 64 channels).  ROWS = true: one
+// output row per tile and one stage per (kernel row, 64 channels), whose
+// stride phases of the input row serve every tap of that row: tap s's B
+// operand starts tap_shift[s] 128-byte rows into plane tap_plane[s] (a
+// K-major 128-byte-swizzled tile read from a whole-row offset is the same
+// tile shifted, the swizzle following the address bits).
+template <bool ROWS>
 __global__ void __launch_bounds__(kWtThreads, 1)
     conv_wtmem_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                      const __grid_constant__ ConvTmaArgs args) {
+                      const __grid_constant__ CUtensorMap tmY, const __grid_constant__ ConvTmaArgs args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -472,7 +488,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
     uint8_t* staging = base + args.stg_off;
     WtBarriers* bar = reinterpret_cast<WtBarriers*>(base + args.bar_off);
     const int stages = args.stages;
-    const uint32_t stage_bytes = static_cast<uint32_t>(args.npix) * 128u;
+    const uint32_t stage_bytes = static_cast<uint32_t>(args.stage_b);
     const int passes = (args.k_blocks + args.w_slots - 1) / args.w_slots;
 
     const int warp = threadIdx.x >> 5;
@@ -497,6 +513,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tmW);
         ptx::tma_prefetch_desc(&tmX);
+        if (args.tma_store) ptx::tma_prefetch_desc(&tmY);
     }
     if (warp == 1) {
         ptx::tmem_alloc<1>(&bar->tmem_base, kWtTmemCols);
@@ -545,11 +562,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                 const ConvWTile wt = args.wt[cu.wt];
                 const int row0 = ht.in_start - ht.pt + cu.rb * args.nr * args.sh;
                 const int col0 = wt.in_start - wt.pl + cu.cb * args.owc * args.sw;
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
-                    const int tap = kb / args.ch_blocks;
-                    const int chb = kb - tap * args.ch_blocks;
-                    const int r = tap / args.kw;
-                    const int s = tap - r * args.kw;
+                for (int kb = 0; kb < args.k_stages; ++kb) {
                     if (!ptx::mbar_wait(&bar->empty[stage], phase ^ 1u, abort, limit)) {
                         raise_error(args.err, abort, kErrProducer);
                         aborted = true;
@@ -557,8 +570,23 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                     }
                     uint8_t* st = ring + stage * stage_bytes;
                     ptx::mbar_arrive_expect_tx(&bar->full[stage], args.tx_bytes);
-                    tma_load_4d(st, &tmX, &bar->full[stage], chb * 64, col0 + s * args.dw,
-                                row0 + r * args.dh, args.img0 + cu.img);
+                    if constexpr (ROWS) {
+                        // Kernel row r, 64 channels: every stride phase of
+                        // the input row, pmax pixels each.
+                        const int r = kb / args.ch_blocks;
+                        const int chb = kb - r * args.ch_blocks;
+                        for (int p = 0; p < args.n_planes; ++p)
+                            tma_load_4d(st + p * args.plane_bytes, &tmX, &bar->full[stage], chb * 64,
+                                        col0 + args.plane_phase[p], row0 + r * args.dh,
+                                        args.img0 + cu.img);
+                    } else {
+                        const int tap = kb / args.ch_blocks;
+                        const int chb = kb - tap * args.ch_blocks;
+                        const int r = tap / args.kw;
+                        const int s = tap - r * args.kw;
+                        tma_load_4d(st, &tmX, &bar->full[stage], chb * 64, col0 + s * args.dw,
+                                    row0 + r * args.dh, args.img0 + cu.img);
+                    }
                     ++issued;
                     if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
                 }
@@ -580,6 +608,17 @@ __global__ void __launch_bounds__(kWtThreads, 1)
             // 8-row groups 1024 B apart; stages and K steps move the
             // descriptor's start-address field (address >> 4, no carry).
             const uint64_t b_desc0 = ptx::smem_desc_sw128(ptx::smem_addr(ring), 16, 1024);
+            // Rows form: each tap's descriptor offset (plane and pixel shift,
+            // in 16-byte units) and filter column stride, held in registers.
+            uint32_t tap_off[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                tap_off[t] = ROWS && t < args.kw
+                                 ? static_cast<uint32_t>((args.tap_plane[t] * args.plane_bytes +
+                                                          args.tap_shift[t] * 128) >> 4)
+                                 : 0u;
+            const int kw = args.kw;
+            const uint32_t tap_cols = static_cast<uint32_t>(args.ch_blocks * 32);
             bool ok = !has_work || ptx::mbar_wait(&bar->wready, 0, abort, limit);
             if (!ok) raise_error(args.err, abort, kErrMma);
             ptx::tc_fence_after();
@@ -590,7 +629,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(args.npix);
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                for (int kb = 0; kb < args.k_stages; ++kb) {
                     if (!ptx::mbar_wait(&bar->full[stage], phase, abort, limit)) {
                         raise_error(args.err, abort, kErrMma);
                         ok = false;
@@ -598,11 +637,29 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                     }
                     ptx::tc_fence_after();
                     const uint64_t b_st = b_desc0 + ((stage * stage_bytes) >> 4);
-                    const uint32_t a0 = tmem + static_cast<uint32_t>(args.a_col + kb * 32);
+                    if constexpr (ROWS) {
+                        const int r = kb / args.ch_blocks;
+                        const int chb = kb - r * args.ch_blocks;
+                        // Filter columns of tap (r, 0); tap s adds s * tap_cols.
+                        const uint32_t a_r = tmem + static_cast<uint32_t>(
+                            args.a_col + (r * kw * args.ch_blocks + chb) * 32);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)   // 16 channels: 8 TMEM columns of A
-                        ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_st + kk * (32 >> 4), args.idesc,
-                                            (kb | kk) != 0);
+                        for (int t = 0; t < 8; ++t) {
+                            if (t >= kw) break;
+                            const uint64_t b_tap = b_st + tap_off[t];
+                            const uint32_t a0 = a_r + static_cast<uint32_t>(t) * tap_cols;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_tap + kk * (32 >> 4),
+                                                    args.idesc, (kb | t | kk) != 0);
+                        }
+                    } else {
+                        const uint32_t a0 = tmem + static_cast<uint32_t>(args.a_col + kb * 32);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)   // 16 channels: 8 TMEM columns of A
+                            ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_st + kk * (32 >> 4), args.idesc,
+                                                (kb | kk) != 0);
+                    }
                     ptx::mma_commit<1>(&bar->empty[stage]);
                     if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
                 }
@@ -668,6 +725,9 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
             const ConvUnit cu = decode_conv_unit(u, args);
             const bool okw = ptx::mbar_wait(&bar->acc_full[acc], acc_phase, abort, limit);
+            // The previous tile's TMA store has read the staging tile
+            // before the barrier below lets anyone write it again.
+            if (args.tma_store && et == 0) ptx::bulk_wait_read_all();
             // One decision for all epilogue warps; passing this barrier also
             // means the previous tile's stores have read the staging tile.
             if (!epilogue_bar_and(okw)) {
@@ -722,6 +782,21 @@ __global__ void __launch_bounds__(kWtThreads, 1)
             }
             if (args.acc_bufs == 2) acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
+            if (args.tma_store) {
+                // One output row: [128 channels][owc pixels] leaves as one
+                // box of y at (ow0, oh, 0, img); channels past c_out and
+                // columns past the width fall outside the tensor.
+                ptx::fence_proxy_async_smem();
+                epilogue_bar_sync();
+                if (et == 0) {
+                    const ConvHTile ht = args.ht[cu.ht];
+                    const ConvWTile wt = args.wt[cu.wt];
+                    ptx::tma_store_4d(&tmY, staging, wt.o0 + cu.cb * args.owc, ht.o0 + cu.rb, 0,
+                                      args.img0 + cu.img);
+                    ptx::bulk_commit_group();
+                }
+                continue;
+            }
             epilogue_bar_sync();
             // Staging tile -> NCHW output, 16 bytes per thread per step:
             // consecutive threads take consecutive chunks of a (channel,
@@ -762,6 +837,9 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                 }
             }
         }
+        // The last TMA store completes before the block (and its shared
+        // memory) goes away.
+        if (args.tma_store && et == 0) ptx::bulk_wait_all();
     }
 
     ptx::tc_fence_before();
@@ -1025,6 +1103,80 @@ bool wtmem_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, i
     return best >= 0;
 }
 
+// Geometry of the rows form: one output row of owc pixels per tile.  Tap s
+// of a kernel row reads input columns base + s*dw + j*sw (j < owc): stride
+// phase (s*dw) % sw at pixel offset (s*dw) / sw.  Each distinct phase is a
+// plane of pmax = owc + max offset pixels (one TMA box, pmax*sw <= 256
+// columns wide).  Cost model as in wtmem_plan, with one wait and commit per
+// (kernel row, 64 channels) and kw taps of 4 MMAs each per stage.
+struct RowsPlan {
+    WtPlan wp;
+    int n_planes = 0, plane_bytes = 0, pmax = 0;
+    int tap_plane[8] = {}, tap_shift[8] = {}, plane_phase[8] = {};
+};
+
+bool rows_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, int tile_ow,
+               int64_t k_blocks, int sms, int forced_acc, RowsPlan* out) {
+    if (d->c_out > 128 || d->kw > 8) return false;
+    RowsPlan rp;
+    int qmax = 0;
+    for (int t = 0; t < d->kw; ++t) {
+        const int c = t * d->dw;
+        const int phase = c % d->sw, q = c / d->sw;
+        int p = 0;
+        while (p < rp.n_planes && rp.plane_phase[p] != phase) ++p;
+        if (p == rp.n_planes) rp.plane_phase[rp.n_planes++] = phase;
+        rp.tap_plane[t] = p;
+        rp.tap_shift[t] = q;
+        qmax = std::max(qmax, q);
+    }
+    const int64_t a_cols = k_blocks * 32;
+    const int ob = d->out_dtype == TILES_F32 ? 4 : 2;
+    const int budget = 227 * 1024 - kSmemBarrierBytes - kSmemAlignSlack;
+    const int64_t rows = std::min<int64_t>(tile_oh, oh);
+    const int64_t n_ht = (oh + tile_oh - 1) / tile_oh;
+    const int64_t n_wt = (ow + tile_ow - 1) / tile_ow;
+    const int64_t wcols = std::min<int64_t>(tile_ow, ow);
+    const int64_t stages_k = static_cast<int64_t>(d->kh) * (k_blocks / (d->kh * d->kw));
+    int64_t best = -1;
+    for (int owc = 16; owc <= 256; owc += 16) {
+        const int pmax = owc + qmax;
+        if (static_cast<int64_t>(pmax) * d->sw > 256) break;
+        int acc = 2 * owc + a_cols <= kWtTmemCols ? 2 : owc + a_cols <= kWtTmemCols ? 1 : 0;
+        if (forced_acc) acc = (forced_acc * owc + a_cols <= kWtTmemCols) ? forced_acc : 0;
+        if (!acc) continue;
+        const int plane_bytes = (pmax * 128 + 1023) / 1024 * 1024;
+        const int stage = rp.n_planes * plane_bytes;
+        const int pitch = owc * ob + 16;
+        const int stg = 128 * pitch;
+        const int stages = std::min(kMaxStages, (budget - stg) / stage);
+        if (stages < 2) continue;
+        const int64_t units = static_cast<int64_t>(d->n) * n_ht * rows * n_wt *
+                              ((wcols + owc - 1) / owc);
+        const int64_t per_unit = stages_k * (std::max<int64_t>(d->kw * 4 * (owc / 2),
+                                                               d->kw * 4 * 55) + 300) +
+                                 (acc == 1 ? 2 * owc + 400 : 0);
+        const int64_t cost = (units + sms - 1) / sms * per_unit;
+        if (best < 0 || cost < best || (cost == best && owc > rp.wp.owc)) {
+            best = cost;
+            rp.wp.owc = owc;
+            rp.wp.nr = 1;
+            rp.wp.acc_bufs = acc;
+            rp.wp.stages = stages;
+            rp.wp.stg_pitch = pitch;
+            rp.wp.stg_bytes = stg;
+            rp.wp.w_slots = (stages * stage + stg) / kWtWeightBlockBytes;
+            rp.wp.smem = std::max(stages * stage + stg + kSmemBarrierBytes + kSmemAlignSlack,
+                                  116 * 1024);
+            rp.pmax = pmax;
+            rp.plane_bytes = plane_bytes;
+        }
+    }
+    if (best < 0) return false;
+    *out = rp;
+    return true;
+}
+
 // cudaFuncSetAttribute once per kernel and size.
 cudaError_t set_smem_attr(const void* fn, std::atomic<int>* cached, int smem) {
     if (cached->load(std::memory_order_relaxed) == smem) return cudaSuccess;
@@ -1032,7 +1184,7 @@ cudaError_t set_smem_attr(const void* fn, std::atomic<int>* cached, int smem) {
     if (e == cudaSuccess) cached->store(smem, std::memory_order_relaxed);
     return e;
 }
-std::atomic<int> g_smem_wtmem{0}, g_smem_tma{0};
+std::atomic<int> g_smem_wtmem{0}, g_smem_rows{0}, g_smem_tma{0};
 
 int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, int tile_ow,
                int tile_n, int64_t oh, int64_t ow, const ConvTmaGeometry& g, void* ws,
@@ -1043,10 +1195,11 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
                     (long long)g.ws_bytes);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) || (reinterpret_cast<uintptr_t>(d->x) & 15u))
         return fail(TILES_ERR_MISALIGNED, "workspace must be 256-byte and x 16-byte aligned");
-    if (weights_mode < TILES_CONV_W_AUTO || weights_mode > TILES_CONV_W_TMEM)
-        return fail(TILES_ERR_INVALID_ARG, "conv_weights must be auto, smem or tmem");
+    if (weights_mode < TILES_CONV_W_AUTO || weights_mode > TILES_CONV_W_TMEM_ROWS)
+        return fail(TILES_ERR_INVALID_ARG, "conv_weights must be auto, smem, tmem or tmem_rows");
     const int forced_acc = cfg ? cfg->acc_bufs : 0;
-    if (weights_mode == TILES_CONV_W_TMEM && (forced_acc < 0 || forced_acc > 2))
+    if ((weights_mode == TILES_CONV_W_TMEM || weights_mode == TILES_CONV_W_TMEM_ROWS) &&
+        (forced_acc < 0 || forced_acc > 2))
         return fail(TILES_ERR_INVALID_ARG, "acc_bufs must be 0 (auto), 1 or 2");
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1056,10 +1209,22 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     // ---- the whole launch is planned before the first kernel goes out ----
     const int64_t k_blocks = static_cast<int64_t>(d->kh) * d->kw * g.ch_blocks;
     WtPlan wp;
-    bool use_tmem = false;
-    if (weights_mode != TILES_CONV_W_SMEM)
+    RowsPlan rp;
+    bool use_tmem = false, use_rows = false;
+    if (weights_mode == TILES_CONV_W_AUTO || weights_mode == TILES_CONV_W_TMEM_ROWS)
+        use_rows = rows_plan(d, oh, ow, tile_oh, tile_ow, k_blocks, sms,
+                             weights_mode == TILES_CONV_W_TMEM_ROWS ? forced_acc : 0, &rp);
+    if (weights_mode == TILES_CONV_W_TMEM_ROWS && !use_rows)
+        return fail(TILES_ERR_INFEASIBLE,
+                    "the rows form needs the filter in tensor memory, kw <= 8 and an input row "
+                    "span within one TMA box");
+    if (use_rows) {
+        wp = rp.wp;
+        use_tmem = true;
+    } else if (weights_mode != TILES_CONV_W_SMEM) {
         use_tmem = wtmem_plan(d, oh, ow, tile_oh, tile_ow, k_blocks, sms,
                               weights_mode == TILES_CONV_W_TMEM ? forced_acc : 0, &wp);
+    }
     if (weights_mode == TILES_CONV_W_TMEM && !use_tmem)
         return fail(TILES_ERR_INFEASIBLE,
                     "the filter does not fit tensor memory (needs c_out <= 128 and kh*kw*ceil(c/64) <= 14)");
@@ -1099,14 +1264,42 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         cuuint64_t strides[3] = {static_cast<cuuint64_t>(d->c) * 2,
                                  static_cast<cuuint64_t>(d->w) * d->c * 2,
                                  static_cast<cuuint64_t>(d->h) * d->w * d->c * 2};
-        cuuint32_t box[4] = {64, static_cast<cuuint32_t>(owc * d->sw),
-                             static_cast<cuuint32_t>(nr * d->sh), 1};
-        cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(d->sw), static_cast<cuuint32_t>(d->sh), 1};
+        // Rows form: one input row, pmax pixels at the column stride; else
+        // nr rows x owc columns at both strides.
+        cuuint32_t box[4] = {64, static_cast<cuuint32_t>((use_rows ? rp.pmax : owc) * d->sw),
+                             static_cast<cuuint32_t>(use_rows ? 1 : nr * d->sh), 1};
+        cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(d->sw),
+                              static_cast<cuuint32_t>(use_rows ? 1 : d->sh), 1};
         CUresult r = fn(&tx, dt, 4, const_cast<uint16_t*>(xn), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS)
             return fail(TILES_ERR_CUDA, "cuTensorMapEncodeTiled(input) failed (%d)", (int)r);
+    }
+
+    // Rows form: the epilogue's tile (one output row, owc columns, 128
+    // channels) leaves by one TMA store when y's rows are 16-byte multiples,
+    // tiles never straddle a W-tile, and y is 16-byte aligned.
+    CUtensorMap ty;
+    std::memset(&ty, 0, sizeof ty);
+    const int yb = d->out_dtype == TILES_F32 ? 4 : 2;
+    bool tma_store = false;
+    if (use_rows && (reinterpret_cast<uintptr_t>(d->y) & 15u) == 0 && (ow * yb) % 16 == 0 &&
+        (std::min<int64_t>(tile_ow, ow) == ow || tile_ow % owc == 0)) {
+        const CUtensorMapDataType yt = d->out_dtype == TILES_F32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : d->out_dtype == TILES_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        cuuint64_t dims[4] = {static_cast<cuuint64_t>(ow), static_cast<cuuint64_t>(oh),
+                              static_cast<cuuint64_t>(d->c_out), static_cast<cuuint64_t>(d->n)};
+        cuuint64_t strides[3] = {static_cast<cuuint64_t>(ow) * yb,
+                                 static_cast<cuuint64_t>(oh) * ow * yb,
+                                 static_cast<cuuint64_t>(d->c_out) * oh * ow * yb};
+        cuuint32_t box[4] = {static_cast<cuuint32_t>(owc), 1, 128, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult r = fn(&ty, yt, 4, d->y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        tma_store = r == CUDA_SUCCESS;
     }
 
     const int budget = 227 * 1024 - kSmemBarrierBytes - kSmemAlignSlack;
@@ -1136,19 +1329,40 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         a.a_col = wp.acc_bufs * a.npix;
         a.nco = 128;
         a.co_blocks = 1;
-        a.tx_bytes = static_cast<uint32_t>(a.npix * 128);
+        if (use_rows) {
+            a.k_stages = d->kh * g.ch_blocks;
+            a.n_planes = rp.n_planes;
+            a.plane_bytes = rp.plane_bytes;
+            a.pmax = rp.pmax;
+            for (int i = 0; i < 8; ++i) {
+                a.tap_plane[i] = rp.tap_plane[i];
+                a.tap_shift[i] = rp.tap_shift[i];
+                a.plane_phase[i] = rp.plane_phase[i];
+            }
+            a.stage_b = rp.n_planes * rp.plane_bytes;
+            a.tx_bytes = static_cast<uint32_t>(rp.n_planes * rp.pmax * 128);
+        } else {
+            a.k_stages = static_cast<int32_t>(k_blocks);
+            a.stage_b = a.npix * 128;
+            a.tx_bytes = static_cast<uint32_t>(a.npix * 128);
+        }
         {
             const int chunk = d->out_dtype == TILES_F32 ? 4 : 8;
             a.vec_ok = (y16 && ow % chunk == 0 && (wcols == ow || tile_ow % chunk == 0)) ? 1 : 0;
         }
         a.idesc = ptx::idesc_f16_f32acc(d->in_dtype == TILES_BF16, false, 128, a.npix);
         a.stages = wp.stages;
-        a.stg_off = wp.stages * a.npix * 128;
-        a.stg_pitch = wp.stg_pitch;
+        a.stg_off = wp.stages * a.stage_b;
+        // A TMA store reads the box densely: [channel][owc pixels].
+        a.tma_store = tma_store ? 1 : 0;
+        a.stg_pitch = tma_store ? owc * yb : wp.stg_pitch;
         a.bar_off = a.stg_off + wp.stg_bytes;
         a.w_slots = wp.w_slots;
         smem = wp.smem;
-        e = set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel), &g_smem_wtmem, smem);
+        e = use_rows ? set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel<true>),
+                                     &g_smem_rows, smem)
+                     : set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel<false>),
+                                     &g_smem_wtmem, smem);
     } else {
         // Weights stay resident in shared memory when there is one output-
         // channel block and they leave room for at least 3 pixel stages;
@@ -1268,7 +1482,8 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
                 lc.numAttrs = 1;
                 if (use_tmem) {
                     lc.blockDim = dim3(kWtThreads);
-                    e = cudaLaunchKernelEx(&lc, conv_wtmem_kernel, tw, tx, a);
+                    e = use_rows ? cudaLaunchKernelEx(&lc, conv_wtmem_kernel<true>, tw, tx, ty, a)
+                                 : cudaLaunchKernelEx(&lc, conv_wtmem_kernel<false>, tw, tx, ty, a);
                 } else {
                     lc.blockDim = dim3(kGemmThreads);
                     e = cudaLaunchKernelEx(&lc, conv_tma_kernel, tw, tx, a, stages, stage_bytes);

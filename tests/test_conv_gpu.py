@@ -381,3 +381,16 @@ def test_rows_form_strides_and_dilations(st, dil, kw):
     smem = run_tiled(x, w, S.BF16, S.F32, st, pad, dil, 4, 0, 0, "smem")
     assert np.array_equal(got, smem)
     check_against_oracle(got, S.widen(x, S.BF16), S.widen(w, S.BF16), st, pad, dil, S.F32)
+
+
+@pytest.mark.parametrize("place", ["smem", "tmem", "rows", "gather"])
+def test_single_output_channel_and_1x1(place):
+    # c_out = 1 (127 zero rows in the tensor-memory filter) with a 3x3 window,
+    # and a 1x1 stride-2 convolution (one tap, one phase plane).
+    x = S.random_matrix(100, (2, 24, 17, 19), S.F16)
+    w = S.random_matrix(101, (1, 24, 3, 3), S.F16)
+    got = run_tiled(x, w, S.F16, S.F32, (1, 1), (1, 1), (1, 1), 5, 0, 0, place)
+    check_against_oracle(got, S.widen(x, S.F16), S.widen(w, S.F16), (1, 1), (1, 1), (1, 1), S.F32)
+    w1 = S.random_matrix(102, (32, 24, 1, 1), S.F16)
+    got = run_tiled(x, w1, S.F16, S.F16, (2, 2), (0, 0), (1, 1), 3, 0, 0, place)
+    check_against_oracle(got, S.widen(x, S.F16), S.widen(w1, S.F16), (2, 2), (0, 0), (1, 1), S.F16)

@@ -310,3 +310,35 @@ def test_forced_tail_schedules(tail):
     T.gemm(a, b, out=c, cfg=cfg, workspace=w)
     T.check(w)
     assert_close(to_f64(c), S.widen(a_np, S.BF16), S.widen(b_np, S.BF16), S.BF16)
+
+
+# --------------------------------------------------------------------------- #
+# Extreme aspect ratios: long K, tall-skinny, very wide, many tiny items
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("m,n,k,in_dt,out_dt", [
+    (128, 256, 32768, S.BF16, S.F32),     # 512 K blocks per tile
+    (40000, 16, 64, S.F16, S.F16),        # 157 M blocks, one narrow N block
+    (16, 50000, 128, S.F16, S.F32),       # one M block, 196+ N blocks
+    (257, 4097, 72, S.BF16, S.BF16),      # ragged in every dimension
+])
+def test_extreme_aspect_ratios(ws, m, n, k, in_dt, out_dt):
+    a = S.random_matrix(90 + m % 7, (m, k), in_dt, "normal")
+    b = S.random_matrix(91 + n % 7, (k, n), in_dt, "normal")
+    pa, pb = -(-k // 8) * 8, -(-n // 8) * 8
+    pc = -(-n // 8) * 8 if out_dt != S.F32 else -(-n // 4) * 4
+    big = T.gemm_workspace(to_cuda(a, in_dt, pa), to_cuda(b, in_dt, pb), empty_out((m, n), out_dt, pc))
+    c = run_gemm(a, b, in_dt, out_dt, None, big, pa, pb, pc)
+    assert_close(to_f64(c), S.widen(a, in_dt), S.widen(b, in_dt), out_dt)
+
+
+def test_many_tiny_batch_items(ws):
+    batch, m, n, k = 1000, 16, 24, 32
+    a = S.random_matrix(95, (batch, m, k), S.F16)
+    b = S.random_matrix(96, (batch, k, n), S.F16)
+    c = empty_out((batch, m, n), S.F32)
+    T.gemm_batched(to_cuda(a, S.F16), to_cuda(b, S.F16), out=c, workspace=ws)
+    T.check(ws)
+    got = to_f64(c)
+    for i in (0, 1, 499, 998, 999):
+        assert_close(got[i], S.widen(a[i], S.F16), S.widen(b[i], S.F16), S.F32)

@@ -643,15 +643,29 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                         // Filter columns of tap (r, 0); tap s adds s * tap_cols.
                         const uint32_t a_r = tmem + static_cast<uint32_t>(
                             args.a_col + (r * kw * args.ch_blocks + chb) * 32);
+                        const uint32_t first = kb != 0 ? 1u : 0u;   // 0: the tile's first MMA
+                        if (kw == 3) {
+                            // The common 3-tap row, fully unrolled: 12 MMAs
+                            // with offsets in registers and no branches.
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) {
-                            if (t >= kw) break;
-                            const uint64_t b_tap = b_st + tap_off[t];
-                            const uint32_t a0 = a_r + static_cast<uint32_t>(t) * tap_cols;
+                            for (int t = 0; t < 3; ++t)
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_tap + kk * (32 >> 4),
-                                                    args.idesc, (kb | t | kk) != 0);
+                                for (int kk = 0; kk < 4; ++kk)
+                                    ptx::mma_f16_tmem_a(d, a_r + t * tap_cols + kk * 8,
+                                                        b_st + tap_off[t] + kk * (32 >> 4),
+                                                        args.idesc,
+                                                        (t | kk) != 0 ? 1u : first);
+                        } else {
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                if (t >= kw) break;
+                                const uint64_t b_tap = b_st + tap_off[t];
+                                const uint32_t a0 = a_r + static_cast<uint32_t>(t) * tap_cols;
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_tap + kk * (32 >> 4),
+                                                        args.idesc, (kb | t | kk) != 0);
+                            }
                         }
                     } else {
                         const uint32_t a0 = tmem + static_cast<uint32_t>(args.a_col + kb * 32);

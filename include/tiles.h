@@ -133,11 +133,14 @@ typedef struct {
  * row's taps through shifted descriptors (kw <= 8, the row's input span
  * within one TMA box).  SMEM: the weights are the B operand in shared
  * memory (M = 128 output pixels, N = a block of output channels); it
- * applies to every TMA convolution.  AUTO takes the first of TMEM_ROWS,
- * TMEM, SMEM that applies. */
+ * applies to every TMA convolution.  TMEM_ROWS_DIRECT: the rows form over
+ * an NCHW input read in place (W a multiple of 8, a stage's input span at
+ * most 249 columns): warps of the kernel transpose each stage's input rows
+ * into the stride-phase planes, so no NHWC copy is made.  AUTO takes the
+ * first of TMEM_ROWS_DIRECT, TMEM_ROWS, TMEM, SMEM that applies. */
 typedef enum {
     TILES_CONV_W_AUTO = 0, TILES_CONV_W_SMEM = 1, TILES_CONV_W_TMEM = 2,
-    TILES_CONV_W_TMEM_ROWS = 3
+    TILES_CONV_W_TMEM_ROWS = 3, TILES_CONV_W_TMEM_ROWS_DIRECT = 4
 } tiles_conv_weights;
 
 /* Schedules of a last round of tiles that would leave resident CTA groups

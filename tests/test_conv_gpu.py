@@ -394,3 +394,127 @@ def test_single_output_channel_and_1x1(place):
     w1 = S.random_matrix(102, (32, 24, 1, 1), S.F16)
     got = run_tiled(x, w1, S.F16, S.F16, (2, 2), (0, 0), (1, 1), 3, 0, 0, place)
     check_against_oracle(got, S.widen(x, S.F16), S.widen(w1, S.F16), (2, 2), (0, 0), (1, 1), S.F16)
+
+
+# --------------------------------------------------------------------------- #
+# The rows form over an NCHW input read in place (transposer warps)
+# --------------------------------------------------------------------------- #
+
+def run_place(x_np, w_np, in_dt, out_dt, stride, pad, dil, tile_oh, conv_weights, acc=0,
+              tile_ow=0, tile_n=0, layout="nchw", guard=16):
+    """One TMA convolution with the filter placement forced; tile_ow and
+    tile_n 0 take whole rows and the whole batch."""
+    x = to_cuda(x_np, in_dt)
+    if layout == "nhwc":
+        x = x.permute(0, 2, 3, 1).contiguous()
+    w = to_cuda(w_np, in_dt)
+    n, c, h, wd = x_np.shape
+    co, _, kh, kw = w_np.shape
+    oh = OC.out_size(h, kh, stride[0], pad[0], pad[0], dil[0])
+    ow = OC.out_size(wd, kw, stride[1], pad[1], pad[1], dil[1])
+    total = n * co * oh * ow
+    flat = torch.full((total + 2 * guard,), 2048.0, dtype=TORCH_DT[out_dt], device="cuda")
+    y = flat[guard:guard + total].view(n, co, oh, ow)
+    ws = T.conv_workspace(x, w, stride, pad, dil, tile_oh, layout=layout)
+    cfg = T.make_config(128, 256, 64, 4, 192, "tcgen05", acc, 1, conv_weights=conv_weights)
+    T.conv2d_tiled(x, w, stride, pad, dil, tile_oh, tile_ow, tile_n, out=y, workspace=ws, cfg=cfg,
+                   layout=layout)
+    T.check(ws)
+    host = to_f64(flat)
+    assert np.all(host[:guard] == 2048.0) and np.all(host[guard + total:] == 2048.0)
+    return host[guard:guard + total].reshape(n, co, oh, ow)
+
+
+# (n, c, h, w, c_out, kh, kw, stride, pad, dil, tile_oh): W a multiple of 8.
+DIRECT_CASES = [
+    (1, 8, 9, 16, 4, 3, 3, (2, 2), (1, 1), (1, 1), 2),       # the tutorial's H=9 rows, one channel group
+    (2, 16, 12, 24, 24, 3, 3, (1, 1), (1, 1), (1, 1), 5),
+    (1, 24, 15, 40, 72, 3, 3, (2, 2), (1, 1), (1, 1), 3),     # 24 channels: 3 of 8 groups live
+    (2, 64, 14, 32, 128, 3, 3, (2, 2), (1, 1), (1, 1), 7),
+    (1, 56, 11, 48, 100, 3, 3, (3, 3), (1, 1), (1, 1), 4),    # three phases, one shift
+    (1, 32, 13, 56, 40, 3, 5, (1, 2), (1, 2), (1, 1), 6),
+    (2, 16, 17, 64, 24, 3, 3, (2, 2), (2, 3), (1, 3), 5),     # dilation 3 at stride 2
+    (1, 16, 10, 40, 16, 3, 2, (1, 3), (1, 0), (2, 1), 3),     # taps 0, 1 at stride 3: phase 2 unread
+    (1, 72, 9, 32, 48, 1, 3, (1, 1), (0, 1), (1, 1), 4),      # two channel blocks
+    (1, 8, 7, 8, 8, 3, 3, (1, 1), (2, 2), (1, 1), 9),         # more padding than one group
+    (1, 16, 6, 16, 32, 1, 1, (2, 2), (0, 0), (1, 1), 2),      # 1x1 at stride 2: one phase plane
+]
+
+
+@pytest.mark.parametrize("case", DIRECT_CASES, ids=lambda c: "_".join(str(v) for v in c[:8]))
+@pytest.mark.parametrize("out_dt", [S.F32, S.BF16])
+def test_direct_rows_match_rows_form_bits(case, out_dt):
+    # The transposer warps build the same planes the TMA loads from the NHWC
+    # copy, and the MMAs run in the same order: identical bits.
+    n, c, h, wd, co, kh, kw, st, pad, dil, tile = case
+    x = S.random_matrix(110, (n, c, h, wd), S.BF16, "normal")
+    w = S.random_matrix(111, (co, c, kh, kw), S.BF16, "normal")
+    got = run_place(x, w, S.BF16, out_dt, st, pad, dil, tile, "rows_direct")
+    rows = run_place(x, w, S.BF16, out_dt, st, pad, dil, tile, "rows")
+    assert np.array_equal(got, rows)
+    x64, w64 = S.widen(x, S.BF16), S.widen(w, S.BF16)
+    if n * co * c * h * wd < 400000:
+        ref = OC.conv2d_loops(x64, w64, st, pad, dil)
+        bound = OC.conv2d_loops(np.abs(x64), np.abs(w64), st, pad, dil)
+        ok, worst, idx = OT.check(got, ref, bound, out_dt)
+        assert ok, f"worst ratio {worst} at {idx}"
+    check_against_oracle(got, x64, w64, st, pad, dil, out_dt)
+
+
+@pytest.mark.parametrize("acc", [1, 2])
+def test_direct_rows_integer_inputs_exact(acc):
+    x = S.integer_matrix(112, (2, 48, 30, 32), S.F16)
+    w = S.integer_matrix(113, (40, 48, 3, 3), S.F16)
+    got = run_place(x, w, S.F16, S.F32, (2, 2), (1, 1), (1, 1), 4, "rows_direct", acc=acc)
+    ref = OC.conv2d(S.widen(x, S.F16), S.widen(w, S.F16), (2, 2), (1, 1), (1, 1))
+    assert np.array_equal(got, ref)
+
+
+def test_direct_rows_w_and_batch_tiles_do_not_change_bits():
+    # Each W-tile's span starts at its own column (col0 mod 8 varies); batch
+    # tiles start at their own image.
+    x = S.random_matrix(114, (3, 16, 21, 48), S.BF16, "normal")
+    w = S.random_matrix(115, (40, 16, 3, 3), S.BF16, "normal")
+    st, pad, dil = (2, 1), (1, 1), (1, 1)
+    base = run_place(x, w, S.BF16, S.F32, st, pad, dil, 4, "rows_direct")
+    for tile_ow, tile_n in ((1, 0), (5, 2), (8, 1), (17, 3), (40, 0)):
+        got = run_place(x, w, S.BF16, S.F32, st, pad, dil, 4, "rows_direct", tile_ow=tile_ow,
+                        tile_n=tile_n)
+        assert np.array_equal(got, base), (tile_ow, tile_n)
+    check_against_oracle(base, S.widen(x, S.BF16), S.widen(w, S.BF16), st, pad, dil, S.F32)
+
+
+@pytest.mark.parametrize("st", [(1, 1), (1, 2)])
+def test_direct_rows_wide_spans(st):
+    # Widths past one span (several column blocks per row); at stride 1 a
+    # stage spans up to 249 columns, the transposers' 32 groups of 8.
+    x = S.random_matrix(116, (1, 8, 5, 1000), S.F16)
+    w = S.random_matrix(117, (12, 8, 3, 3), S.F16)
+    got = run_place(x, w, S.F16, S.F16, st, (1, 1), (1, 1), 2, "rows_direct", guard=32)
+    rows = run_place(x, w, S.F16, S.F16, st, (1, 1), (1, 1), 2, "rows", guard=32)
+    assert np.array_equal(got, rows)
+    check_against_oracle(got, S.widen(x, S.F16), S.widen(w, S.F16), st, (1, 1), (1, 1), S.F16)
+
+
+def test_direct_rows_workload_and_auto():
+    # The convolution workload: the direct form is what AUTO takes for it.
+    wl = S.WORKLOADS["conv_htiled"]
+    x_np, w_np = S.conv_inputs(wl)
+    args = ((wl.sh, wl.sw), (wl.ph, wl.pw), (wl.dh, wl.dw), wl.tile_oh)
+    got = run_place(x_np, w_np, wl.in_dtype, wl.out_dtype, *args, "rows_direct")
+    auto = run_place(x_np, w_np, wl.in_dtype, wl.out_dtype, *args, "auto")
+    assert np.array_equal(got, auto)
+    check_against_oracle(got, S.widen(x_np, wl.in_dtype), S.widen(w_np, wl.in_dtype), *args[:3],
+                         wl.out_dtype)
+
+
+def test_direct_rows_refused_where_it_does_not_apply():
+    w = torch.zeros((16, 16, 3, 3), dtype=torch.float16, device="cuda")
+    cfg = T.make_config(128, 256, 64, 4, 192, "tcgen05", 0, 1, conv_weights="rows_direct")
+    for shape, layout in (((1, 16, 8, 20), "nchw"),       # W not a multiple of 8
+                          ((1, 8, 16, 16), "nhwc")):      # not an NCHW input
+        x = torch.zeros(shape, dtype=torch.float16, device="cuda")
+        ws = T.conv_workspace(x, w, (1, 1), (1, 1), (1, 1), 4, layout=layout)
+        with pytest.raises(T.TilesError) as e:
+            T.conv2d_htiled(x, w, (1, 1), (1, 1), (1, 1), 4, workspace=ws, cfg=cfg, layout=layout)
+        assert e.value.status == -4

@@ -47,7 +47,7 @@ def device_query(ordinal: int = 0) -> _abi.Device:
 
 
 CONV_WEIGHTS = {"auto": _abi.CONV_W_AUTO, "smem": _abi.CONV_W_SMEM, "tmem": _abi.CONV_W_TMEM,
-                "rows": _abi.CONV_W_TMEM_ROWS}
+                "rows": _abi.CONV_W_TMEM_ROWS, "rows_direct": _abi.CONV_W_TMEM_ROWS_DIRECT}
 TAILS = {"auto": _abi.TAIL_AUTO, "whole": _abi.TAIL_WHOLE, "nhalf": _abi.TAIL_NHALF,
          "ksplit": _abi.TAIL_KSPLIT}
 

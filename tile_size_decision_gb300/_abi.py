@@ -56,7 +56,7 @@ class Config(C.Structure):
 
 
 TAIL_AUTO, TAIL_WHOLE, TAIL_NHALF, TAIL_KSPLIT = 0, 1, 2, 3
-CONV_W_AUTO, CONV_W_SMEM, CONV_W_TMEM, CONV_W_TMEM_ROWS = 0, 1, 2, 3
+CONV_W_AUTO, CONV_W_SMEM, CONV_W_TMEM, CONV_W_TMEM_ROWS, CONV_W_TMEM_ROWS_DIRECT = 0, 1, 2, 3, 4
 
 
 class Verdict(C.Structure):

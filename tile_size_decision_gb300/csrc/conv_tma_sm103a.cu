@@ -74,6 +74,18 @@ struct ConvTmaArgs {
     int32_t k_stages, n_planes, plane_bytes, pmax;
     int32_t tma_store;                    // rows form: the staged tile leaves by one TMA store
     int32_t tap_plane[8], tap_shift[8], plane_phase[8];
+    // Rows form over an NCHW input read in place (FORM 2): each stage's raw
+    // box, 64 channel rows of xw input columns (xw / 8 odd), lands in one of
+    // raw_stages slots of raw_b bytes from raw_off; phase_planes holds the
+    // plane of each stride phase (4 bits per phase, 15 = no tap reads it);
+    // plane p starts plane_rows0 >> 4p & 15 rows into its plane_bytes.
+    int32_t raw_off, raw_b, raw_stages, xw;
+    int32_t raw_early;                    // raw slots below the filter's start-up space
+    uint32_t plane_rows0;
+    uint32_t phase_planes;
+    // Offsets of the plane (or pixel box) ring and of the filter's start-up
+    // passes in shared memory.
+    int32_t ring_off, w_off;
     ConvHTile ht[kConvMaxHTiles];
     ConvWTile wt[kConvMaxWTiles];
 };
@@ -149,6 +161,10 @@ __device__ __forceinline__ int div_small(int a, int d, float inv_d) {
     if (q * d > a) --q;
     else if ((q + 1) * d <= a) ++q;
     return q;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16) {
@@ -437,6 +453,19 @@ constexpr int kWtEpilogueWarps = 8;
 constexpr int kWtEpilogueThreads = kWtEpilogueWarps * 32;
 constexpr int kWtTmemCols = 512;
 constexpr int kWtWeightBlockBytes = 128 * 128;   // 128 rows x 64 channels x 2 bytes
+// Rows form read straight from an NCHW input: kTrWarps more warps, after
+// the producer, the MMA issuer and the epilogue warps, build each stage's
+// stride-phase planes from the input rows.  They take the warps past the
+// epilogue's that do not share the MMA issuer's scheduler (warp % 4 != 1);
+// the others there stay idle.
+constexpr int kTrWarps = 12;
+constexpr int kTrFirstWarp = 2 + 8;          // after the producer, the MMA issuer, 8 epilogue warps
+constexpr int kWtDirectThreads =
+    (kTrFirstWarp + (kTrWarps - 1) + (kTrWarps - 1) / 3 + 1) * 32;
+static_assert(kTrFirstWarp % 4 == 2, "transposer warp mapping assumes warp 10 sits on scheduler 2");
+// Transposer items per warp and stage: a raw box of at most 256 columns is
+// 32 column groups x 2 channel halves.
+constexpr int kTrItems = (64 + kTrWarps - 1) / kTrWarps;
 
 struct WtBarriers {
     uint64_t full[kMaxStages];
@@ -469,22 +498,57 @@ __device__ __forceinline__ bool epilogue_bar_and(bool flag) {
     return r != 0;
 }
 
-// ROWS = false: one pixel box per (tap, 64 channels).  ROWS = true: one
+// Four 8 x 8 blocks of 16-bit elements from shared memory, transposed: lane
+// l gives the address of row l & 7 of block l >> 3 (16 bytes, 16-byte
+// aligned) and receives, in d[b], elements (2(l & 3), l >> 2) and
+// (2(l & 3) + 1, l >> 2) of block b, the first in the low half.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&d)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// Where one stage of the rows form reads its input: image, input row,
+// first channel and the first input column of the span (pmax * sw columns
+// from col0).
+struct RowStage { int img, ih, c0, col0; };
+
+__device__ __forceinline__ RowStage row_stage(int u, int kb, const ConvTmaArgs& a) {
+    const ConvUnit cu = decode_conv_unit(u, a);
+    const ConvHTile ht = a.ht[cu.ht];
+    const ConvWTile wt = a.wt[cu.wt];
+    const int r = kb / a.ch_blocks;
+    RowStage s;
+    s.img = a.img0 + cu.img;
+    s.ih = ht.in_start - ht.pt + cu.rb * a.nr * a.sh + r * a.dh;
+    s.c0 = (kb - r * a.ch_blocks) * 64;
+    s.col0 = wt.in_start - wt.pl + cu.cb * a.owc * a.sw;
+    return s;
+}
+
+// FORM 0: one pixel box per (tap, 64 channels).  FORM 1 (rows form): one
 // output row per tile and one stage per (kernel row, 64 channels), whose
 // stride phases of the input row serve every tap of that row: tap s's B
 // operand starts tap_shift[s] 128-byte rows into plane tap_plane[s] (a
 // K-major 128-byte-swizzled tile read from a whole-row offset is the same
-// tile shifted, the swizzle following the address bits).
-template <bool ROWS>
-__global__ void __launch_bounds__(kWtThreads, 1)
+// tile shifted, the swizzle following the address bits).  FORM 2: the rows
+// form over an NCHW input, its planes written by transposer warps from raw
+// NCHW boxes instead of loaded by TMA from an NHWC copy.
+template <int FORM>
+__global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
     conv_wtmem_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmY, const __grid_constant__ ConvTmaArgs args) {
+    constexpr bool ROWS = FORM != 0;
+    constexpr bool DIRECT = FORM == 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    // [stages x pixel box][staging tile][barriers]; at the start the filter
-    // passes use [0, w_slots x 16 KB) of the first two.
-    uint8_t* ring = base;
+    // FORM 0, 1: [stages x pixel box][staging tile][barriers], the filter
+    // passes in [0, w_slots x 16 KB) at the start.  FORM 2: [raw ring][plane
+    // ring][staging tile][barriers], the filter passes from raw slot
+    // raw_early on, so the first raw_early boxes load beside them.
+    uint8_t* ring = base + args.ring_off;
     uint8_t* staging = base + args.stg_off;
     WtBarriers* bar = reinterpret_cast<WtBarriers*>(base + args.bar_off);
     const int stages = args.stages;
@@ -496,8 +560,16 @@ __global__ void __launch_bounds__(kWtThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            ptx::mbar_init(&bar->full[s], 1);
+            // FORM 2: every transposer warp arrives once per stage.
+            ptx::mbar_init(&bar->full[s], DIRECT ? kTrWarps : 1);
             ptx::mbar_init(&bar->empty[s], 1);
+        }
+        if (DIRECT) {
+            // The raw ring's barriers follow the plane ring's.
+            for (int s = 0; s < args.raw_stages; ++s) {
+                ptx::mbar_init(&bar->full[stages + s], 1);
+                ptx::mbar_init(&bar->empty[stages + s], kTrWarps);
+            }
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&bar->acc_full[a], 1);
@@ -535,19 +607,64 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         if (lane == 0) {
             bool aborted = false;
             // ---------------- the filter, pass by pass ----------------
-            for (int p = 0; p < passes && has_work; ++p) {
+            auto filter_pass = [&](int p) {
                 if (p > 0 && !ptx::mbar_wait(&bar->wcons, (p - 1) & 1, abort, limit)) {
                     raise_error(args.err, abort, kErrProducer);
                     aborted = true;
-                    break;
+                    return;
                 }
                 const int kb0 = p * args.w_slots;
                 const int nkb = min(args.w_slots, args.k_blocks - kb0);
                 ptx::mbar_arrive_expect_tx(&bar->wfull, static_cast<uint32_t>(nkb * kWtWeightBlockBytes));
                 for (int i = 0; i < nkb; ++i)
-                    ptx::tma_load_3d(base + i * kWtWeightBlockBytes, &tmW, &bar->wfull,
+                    ptx::tma_load_3d(base + args.w_off + i * kWtWeightBlockBytes, &tmW, &bar->wfull,
                                      (kb0 + i) * 64, 0, 0);
-            }
+            };
+            if constexpr (DIRECT) {
+                // ---------------- TMA producer: each stage's raw NCHW box ----------------
+                // 64 channel rows of xw columns from the span's 8-column
+                // group (x 16-byte aligned); rows, columns and channels
+                // outside the input arrive as zeros.  The first raw_early
+                // boxes go out with the filter's first pass, the rest once
+                // the filter has left the slots after them.
+                uint32_t rs = 0, rphase = 0;
+                int issued = 0, u = blockIdx.x, kb = 0;
+                const uint32_t raw_tx = static_cast<uint32_t>(args.raw_b);
+                auto issue_raw = [&]() {
+                    if (!ptx::mbar_wait(&bar->empty[stages + rs], rphase ^ 1u, abort, limit)) {
+                        raise_error(args.err, abort, kErrProducer);
+                        aborted = true;
+                        return;
+                    }
+                    const RowStage st = row_stage(u, kb, args);
+                    uint64_t* rfull = &bar->full[stages + rs];
+                    ptx::mbar_arrive_expect_tx(rfull, raw_tx);
+                    tma_load_4d(base + args.raw_off + rs * args.raw_b, &tmX, rfull, st.col0 & ~7,
+                                st.ih, st.c0, st.img);
+                    ++issued;
+                    if (++rs == static_cast<uint32_t>(args.raw_stages)) { rs = 0; rphase ^= 1u; }
+                    if (++kb == args.k_stages) { kb = 0; u += gridDim.x; }
+                };
+                // The filter's loads go first: one TMA queue serves both, and
+                // a raw box from DRAM ahead of them would hold them up.
+                if (has_work) filter_pass(0);
+                while (!aborted && u < args.units && issued < args.raw_early) issue_raw();
+                for (int p = 1; p < passes && has_work && !aborted; ++p) filter_pass(p);
+                if (!aborted && has_work && !ptx::mbar_wait(&bar->wcons, (passes - 1) & 1, abort, limit)) {
+                    raise_error(args.err, abort, kErrProducer);
+                    aborted = true;
+                }
+                while (!aborted && u < args.units) issue_raw();
+                if (aborted) {
+                    settle_after_abort();
+                } else {
+                    for (int i = 0; i < (issued < args.raw_stages ? issued : args.raw_stages); ++i) {
+                        if (rs == 0) { rs = args.raw_stages - 1; rphase ^= 1u; } else { --rs; }
+                        ptx::mbar_wait(&bar->full[stages + rs], rphase, nullptr, limit);
+                    }
+                }
+            } else {
+            for (int p = 0; p < passes && has_work && !aborted; ++p) filter_pass(p);
             // The pixel boxes reuse that space once the last pass is copied.
             if (!aborted && has_work && !ptx::mbar_wait(&bar->wcons, (passes - 1) & 1, abort, limit)) {
                 raise_error(args.err, abort, kErrProducer);
@@ -599,6 +716,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                     ptx::mbar_wait(&bar->full[stage], phase, nullptr, limit);
                 }
             }
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -614,8 +732,10 @@ __global__ void __launch_bounds__(kWtThreads, 1)
 #pragma unroll
             for (int t = 0; t < 8; ++t)
                 tap_off[t] = ROWS && t < args.kw
-                                 ? static_cast<uint32_t>((args.tap_plane[t] * args.plane_bytes +
-                                                          args.tap_shift[t] * 128) >> 4)
+                                 ? static_cast<uint32_t>(
+                                       (args.tap_plane[t] * args.plane_bytes +
+                                        (static_cast<int>((args.plane_rows0 >> (4 * args.tap_plane[t])) & 15u) +
+                                         args.tap_shift[t]) * 128) >> 4)
                                  : 0u;
             const int kw = args.kw;
             const uint32_t tap_cols = static_cast<uint32_t>(args.ch_blocks * 32);
@@ -685,7 +805,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
             ptx::mma_commit_local<1>(&bar->drain);
             ptx::mbar_wait(&bar->drain, 0, nullptr, limit);
         }
-    } else {
+    } else if (warp < 2 + kWtEpilogueWarps) {
         const int quarter = warp & 3;
         const int half = (warp - 2) >> 2;
         const int et = threadIdx.x - 64;                // 0 .. 255
@@ -705,7 +825,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
             for (int i = half; i < nkb; i += 2) {
                 // Row co of a 128-byte-swizzled block: 16-byte chunk j sits
                 // at chunk j ^ (co & 7).
-                const uint8_t* row = base + i * kWtWeightBlockBytes + co * 128;
+                const uint8_t* row = base + args.w_off + i * kWtWeightBlockBytes + co * 128;
                 uint32_t v[32];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -755,6 +875,48 @@ __global__ void __launch_bounds__(kWtThreads, 1)
             // one round trip, after which the accumulator is released; the
             // conversion and the staging writes overlap the next tile's MMAs.
             const int ncols = col_end - col_begin;
+            if constexpr (DIRECT) {
+                // 32 columns at a time (the wider block leaves fewer
+                // registers per thread); the accumulator is released after
+                // the last chunk.
+#pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    uint32_t w[32];
+                    const int nc = min(32, ncols - c0);
+                    if (nc == 32) {
+                        ptx::tmem_ld_32cols(tacc + col_begin + c0, w);
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            if (8 * g + 8 <= nc)
+                                ptx::tmem_ld_8cols(tacc + col_begin + c0 + 8 * g, w[8 * g + 0],
+                                                   w[8 * g + 1], w[8 * g + 2], w[8 * g + 3],
+                                                   w[8 * g + 4], w[8 * g + 5], w[8 * g + 6],
+                                                   w[8 * g + 7]);
+                    }
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (8 * g + 8 > nc) continue;
+                        const int c = col_begin + c0 + 8 * g;
+                        if (ob == 2) {
+                            uint4 t;
+                            t.x = pack_half2(__uint_as_float(w[8 * g + 0]), __uint_as_float(w[8 * g + 1]), bf16_out);
+                            t.y = pack_half2(__uint_as_float(w[8 * g + 2]), __uint_as_float(w[8 * g + 3]), bf16_out);
+                            t.z = pack_half2(__uint_as_float(w[8 * g + 4]), __uint_as_float(w[8 * g + 5]), bf16_out);
+                            t.w = pack_half2(__uint_as_float(w[8 * g + 6]), __uint_as_float(w[8 * g + 7]), bf16_out);
+                            *reinterpret_cast<uint4*>(srow + c * 2) = t;
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(srow + c * 4);
+                            dst[0] = make_uint4(w[8 * g + 0], w[8 * g + 1], w[8 * g + 2], w[8 * g + 3]);
+                            dst[1] = make_uint4(w[8 * g + 4], w[8 * g + 5], w[8 * g + 6], w[8 * g + 7]);
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bar->acc_empty[acc]);
+            } else {
             uint32_t v[128];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -793,6 +955,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                     dst[0] = make_uint4(v[8 * g + 0], v[8 * g + 1], v[8 * g + 2], v[8 * g + 3]);
                     dst[1] = make_uint4(v[8 * g + 4], v[8 * g + 5], v[8 * g + 6], v[8 * g + 7]);
                 }
+            }
             }
             if (args.acc_bufs == 2) acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
@@ -854,6 +1017,113 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         // The last TMA store completes before the block (and its shared
         // memory) goes away.
         if (args.tma_store && et == 0) ptx::bulk_wait_all();
+    } else if constexpr (DIRECT) {
+        // ---------------- transposer warps (FORM 2) ----------------
+        // A raw box is 64 channel rows of xw input columns (row pitch 2 xw
+        // bytes, an odd multiple of 16, so the 8 rows of an 8 x 8 block sit
+        // in 8 bank groups).  A work item is one 8-column group and 32
+        // channels: one ldmatrix .x4 .trans reads its four 8 x 8 blocks
+        // transposed, leaving lane l with channels 2(l & 3), 2(l & 3) + 1 of
+        // column l >> 2 in each block; four 4-byte stores put them into the
+        // column's phase plane row, 16-byte chunk (channel group) ^ (row & 7)
+        // under the 128-byte swizzle.
+        // Transposer index: warps kTrFirstWarp + j, j % 4 == 3 idle (they
+        // share the MMA issuer's scheduler).
+        const int j = warp - kTrFirstWarp;
+        const int tw = (j & 3) == 3 ? -1 : j - (j >> 2);
+        if (tw < 0) goto transposers_done;
+        {
+        const int span = args.pmax * args.sw;
+        const int items = args.xw >> 2;            // xw / 8 column groups x 2 channel halves
+        const uint32_t pitch = 2u * static_cast<uint32_t>(args.xw);
+        // Item q of this warp is it = tw + q kTrWarps: channel half tw & 1
+        // and column group (tw >> 1) + q kTrWarps / 2, kColStep columns
+        // after the previous one.
+        constexpr int kColStep = 8 * (kTrWarps / 2);
+        const int half = tw & 1, g0 = tw >> 1;
+        // ldmatrix row of this lane: block l >> 3, channel row l & 7.
+        const uint32_t ld_off = static_cast<uint32_t>(half * 32 + (lane >> 3) * 8 + (lane & 7)) * pitch +
+                                16u * static_cast<uint32_t>(g0);
+        const int px = lane >> 2;                   // column within the group after the transpose
+        const int pair = (lane & 3) * 4;
+        // Strides dividing kColStep into a multiple of 8 rows keep a lane's
+        // phase plane and swizzle row (mod 8) across its items: rows advance
+        // by kColStep / sw per item.
+        const bool fast = kColStep % args.sw == 0 && (kColStep / args.sw) % 8 == 0;
+        const int row_step = fast ? kColStep / args.sw : 0;
+        uint32_t ps = 0, pphase = 0, rs = 0, rphase = 0;
+        // The planes reuse the filter's start-up space.
+        bool ok = !has_work || __all_sync(0xffffffffu, ptx::mbar_wait(&bar->wready, 0, abort, limit));
+        for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+            // Span column of raw column 0 (the box starts at the span's
+            // 8-column group), and of this lane's first item.
+            const int x_first = -(row_stage(u, 0, args).col0 & 7);
+            const int t0 = x_first + 8 * g0 + px;
+            int lane_off = 0, pl0 = 15, co[4] = {0, 0, 0, 0};
+            if (fast) {
+                const int phi = ((t0 % args.sw) + args.sw) % args.sw;
+                const int jr0 = (t0 - phi) / args.sw;
+                pl0 = static_cast<int>((args.phase_planes >> (4 * phi)) & 15u);
+                const int rr0 = static_cast<int>((args.plane_rows0 >> (4 * pl0)) & 15u) + jr0;
+                lane_off = pl0 * args.plane_bytes + rr0 * 128 + pair;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) co[m] = ((half * 4 + m) ^ (rr0 & 7)) << 4;
+            }
+            for (int kb = 0; kb < args.k_stages; ++kb) {
+                ok = __all_sync(0xffffffffu,
+                                ptx::mbar_wait(&bar->full[stages + rs], rphase, abort, limit)) &&
+                     __all_sync(0xffffffffu, ptx::mbar_wait(&bar->empty[ps], pphase ^ 1u, abort, limit));
+                if (!ok) break;
+                const uint32_t raw = ptx::smem_addr(base + args.raw_off + rs * args.raw_b) + ld_off;
+                uint8_t* slot = ring + ps * stage_bytes;
+                // All of this warp's items (at most kTrItems: items <= 64)
+                // are read first, so their loads overlap; the conditions
+                // are warp-uniform and the warp converged for ldmatrix.
+                uint32_t d[kTrItems][4];
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < kTrItems; ++q)
+                    if (tw + q * kTrWarps < items)
+                        ldmatrix_x4_trans(raw + 16u * static_cast<uint32_t>(q * (kTrWarps / 2)), d[q]);
+#pragma unroll
+                for (int q = 0; q < kTrItems; ++q) {
+                    if (tw + q * kTrWarps >= items) break;
+                    const int t = t0 + kColStep * q;          // span column of this lane's value
+                    if (t < 0 || t >= span) continue;
+                    int rr, pl;
+                    uint8_t* row;
+                    if (fast) {
+                        if (pl0 == 15) continue;
+                        pl = pl0;
+                        row = slot + lane_off + q * row_step * 128;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m)
+                            *reinterpret_cast<uint32_t*>(row + co[m]) = d[q][m];
+                    } else {
+                        const int jr = t / args.sw, phi = t - jr * args.sw;
+                        pl = static_cast<int>((args.phase_planes >> (4 * phi)) & 15u);
+                        if (pl == 15) continue;
+                        rr = static_cast<int>((args.plane_rows0 >> (4 * pl)) & 15u) + jr;
+                        row = slot + pl * args.plane_bytes + rr * 128 + pair;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m)
+                            *reinterpret_cast<uint32_t*>(row + (((half * 4 + m) ^ (rr & 7)) << 4)) = d[q][m];
+                    }
+                }
+                // The raw slot is read (its values are in registers) ...
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bar->empty[stages + rs]);
+                // ... and the planes go to the tensor cores (the async proxy).
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bar->full[ps]);
+                if (++ps == static_cast<uint32_t>(stages)) { ps = 0; pphase ^= 1u; }
+                if (++rs == static_cast<uint32_t>(args.raw_stages)) { rs = 0; rphase ^= 1u; }
+            }
+        }
+        if (!ok && lane == 0) raise_error(args.err, abort, kErrProducer);
+        }
+    transposers_done:;
     }
 
     ptx::tc_fence_before();
@@ -865,6 +1135,10 @@ __global__ void __launch_bounds__(kWtThreads, 1)
     }
 }
 
+// Items (64 channels x 32 columns of one row) per warp: all their loads are
+// in flight before the first transpose.
+constexpr int kPrepItemsPerWarp = 1;
+
 // NCHW -> NHWC for 16-bit elements with 16-byte accesses on both sides (C
 // and W multiples of 8, x 16-byte aligned), fused with the weight reorder.
 // A warp moves kPrepItemsPerWarp items of 64 channels x 32 columns of one
@@ -873,14 +1147,6 @@ __global__ void __launch_bounds__(kWtThreads, 1)
 // 8 channels.  For a fixed register a warp reads 8 runs of 64 bytes and
 // writes 4 runs of 128 bytes.  Blocks past the transpose reorder the
 // weights as reorder_weights_kernel does.
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
-    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
-}
-
-// Items (64 channels x 32 columns of one row) per warp: all their loads are
-// in flight before the first transpose.
-constexpr int kPrepItemsPerWarp = 1;
-
 __global__ void __launch_bounds__(256)
     conv_prep_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xt, int C, int H,
                      int W, int64_t items, unsigned transpose_blocks,
@@ -1126,11 +1392,16 @@ bool wtmem_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, i
 struct RowsPlan {
     WtPlan wp;
     int n_planes = 0, plane_bytes = 0, pmax = 0;
+    int raw_b = 0, xw = 0;           // direct form: raw box bytes and columns
     int tap_plane[8] = {}, tap_shift[8] = {}, plane_phase[8] = {};
 };
 
+// direct: the form over an NCHW input read in place, whose stages also hold
+// a raw box of 64 channel rows x xw columns (xw / 8 odd, at most 256, at
+// least the span pmax * sw plus the 7 columns of its 8-column group); at
+// most 4 plane and 4 raw stages.
 bool rows_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, int tile_ow,
-               int64_t k_blocks, int sms, int forced_acc, RowsPlan* out) {
+               int64_t k_blocks, int sms, int forced_acc, bool direct, RowsPlan* out) {
     if (d->c_out > 128 || d->kw > 8) return false;
     RowsPlan rp;
     int qmax = 0;
@@ -1156,14 +1427,22 @@ bool rows_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, in
     for (int owc = 16; owc <= 256; owc += 16) {
         const int pmax = owc + qmax;
         if (static_cast<int64_t>(pmax) * d->sw > 256) break;
+        int xw = 0;
+        if (direct) {
+            xw = (pmax * d->sw + 7 + 7) / 8 * 8;
+            if ((xw / 8) % 2 == 0) xw += 8;
+            if (xw > 256) break;
+        }
         int acc = 2 * owc + a_cols <= kWtTmemCols ? 2 : owc + a_cols <= kWtTmemCols ? 1 : 0;
         if (forced_acc) acc = (forced_acc * owc + a_cols <= kWtTmemCols) ? forced_acc : 0;
         if (!acc) continue;
-        const int plane_bytes = (pmax * 128 + 1023) / 1024 * 1024;
-        const int stage = rp.n_planes * plane_bytes;
+        // Direct form: a plane may start up to 7 rows into its space.
+        const int plane_bytes = ((pmax + (direct ? 7 : 0)) * 128 + 1023) / 1024 * 1024;
+        const int raw_b = 128 * xw;
+        const int stage = rp.n_planes * plane_bytes + raw_b;
         const int pitch = owc * ob + 16;
         const int stg = 128 * pitch;
-        const int stages = std::min(kMaxStages, (budget - stg) / stage);
+        const int stages = std::min(direct ? kMaxStages / 2 : kMaxStages, (budget - stg) / stage);
         if (stages < 2) continue;
         const int64_t units = static_cast<int64_t>(d->n) * n_ht * rows * n_wt *
                               ((wcols + owc - 1) / owc);
@@ -1179,11 +1458,15 @@ bool rows_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, in
             rp.wp.stages = stages;
             rp.wp.stg_pitch = pitch;
             rp.wp.stg_bytes = stg;
-            rp.wp.w_slots = (stages * stage + stg) / kWtWeightBlockBytes;
+            // The filter's start-up passes use everything from raw slot 1
+            // on (the direct form's first raw box loads beside them).
+            rp.wp.w_slots = (stages * stage + stg - (direct ? raw_b : 0)) / kWtWeightBlockBytes;
             rp.wp.smem = std::max(stages * stage + stg + kSmemBarrierBytes + kSmemAlignSlack,
                                   116 * 1024);
             rp.pmax = pmax;
             rp.plane_bytes = plane_bytes;
+            rp.raw_b = raw_b;
+            rp.xw = xw;
         }
     }
     if (best < 0) return false;
@@ -1198,7 +1481,7 @@ cudaError_t set_smem_attr(const void* fn, std::atomic<int>* cached, int smem) {
     if (e == cudaSuccess) cached->store(smem, std::memory_order_relaxed);
     return e;
 }
-std::atomic<int> g_smem_wtmem{0}, g_smem_rows{0}, g_smem_tma{0};
+std::atomic<int> g_smem_wtmem{0}, g_smem_rows{0}, g_smem_direct{0}, g_smem_tma{0};
 
 int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, int tile_ow,
                int tile_n, int64_t oh, int64_t ow, const ConvTmaGeometry& g, void* ws,
@@ -1209,10 +1492,12 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
                     (long long)g.ws_bytes);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) || (reinterpret_cast<uintptr_t>(d->x) & 15u))
         return fail(TILES_ERR_MISALIGNED, "workspace must be 256-byte and x 16-byte aligned");
-    if (weights_mode < TILES_CONV_W_AUTO || weights_mode > TILES_CONV_W_TMEM_ROWS)
-        return fail(TILES_ERR_INVALID_ARG, "conv_weights must be auto, smem, tmem or tmem_rows");
+    if (weights_mode < TILES_CONV_W_AUTO || weights_mode > TILES_CONV_W_TMEM_ROWS_DIRECT)
+        return fail(TILES_ERR_INVALID_ARG,
+                    "conv_weights must be auto, smem, tmem, tmem_rows or tmem_rows_direct");
     const int forced_acc = cfg ? cfg->acc_bufs : 0;
-    if ((weights_mode == TILES_CONV_W_TMEM || weights_mode == TILES_CONV_W_TMEM_ROWS) &&
+    if ((weights_mode == TILES_CONV_W_TMEM || weights_mode == TILES_CONV_W_TMEM_ROWS ||
+         weights_mode == TILES_CONV_W_TMEM_ROWS_DIRECT) &&
         (forced_acc < 0 || forced_acc > 2))
         return fail(TILES_ERR_INVALID_ARG, "acc_bufs must be 0 (auto), 1 or 2");
     int dev = 0, sms = 0;
@@ -1224,10 +1509,23 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     const int64_t k_blocks = static_cast<int64_t>(d->kh) * d->kw * g.ch_blocks;
     WtPlan wp;
     RowsPlan rp;
-    bool use_tmem = false, use_rows = false;
-    if (weights_mode == TILES_CONV_W_AUTO || weights_mode == TILES_CONV_W_TMEM_ROWS)
+    bool use_tmem = false, use_rows = false, use_direct = false;
+    // The rows form over an NCHW input read directly: 16-byte loads of 8
+    // columns (W a multiple of 8), and a stage's span, from its 8-column
+    // group, within the transposers' 32 groups.
+    if (d->x_layout == TILES_LAYOUT_NCHW && d->w % 8 == 0 &&
+        (weights_mode == TILES_CONV_W_AUTO || weights_mode == TILES_CONV_W_TMEM_ROWS_DIRECT))
+        use_direct = rows_plan(d, oh, ow, tile_oh, tile_ow, k_blocks, sms,
+                               weights_mode == TILES_CONV_W_TMEM_ROWS_DIRECT ? forced_acc : 0,
+                               true, &rp);
+    if (weights_mode == TILES_CONV_W_TMEM_ROWS_DIRECT && !use_direct)
+        return fail(TILES_ERR_INFEASIBLE,
+                    "the direct rows form needs an NCHW input with W a multiple of 8, the filter "
+                    "in tensor memory, kw <= 8 and an input row span of at most 241 columns");
+    use_rows = use_direct;
+    if (!use_rows && (weights_mode == TILES_CONV_W_AUTO || weights_mode == TILES_CONV_W_TMEM_ROWS))
         use_rows = rows_plan(d, oh, ow, tile_oh, tile_ow, k_blocks, sms,
-                             weights_mode == TILES_CONV_W_TMEM_ROWS ? forced_acc : 0, &rp);
+                             weights_mode == TILES_CONV_W_TMEM_ROWS ? forced_acc : 0, false, &rp);
     if (weights_mode == TILES_CONV_W_TMEM_ROWS && !use_rows)
         return fail(TILES_ERR_INFEASIBLE,
                     "the rows form needs the filter in tensor memory, kw <= 8 and an input row "
@@ -1248,8 +1546,8 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     char* wsb = static_cast<char*>(ws);
     uint16_t* wr = reinterpret_cast<uint16_t*>(wsb + g.weights_offset);
     const uint16_t* x_src = static_cast<const uint16_t*>(d->x);
-    uint16_t* xt = d->x_layout == TILES_LAYOUT_NCHW ? reinterpret_cast<uint16_t*>(wsb + g.x_offset)
-                                                     : nullptr;
+    uint16_t* xt = d->x_layout == TILES_LAYOUT_NCHW && !use_direct
+                       ? reinterpret_cast<uint16_t*>(wsb + g.x_offset) : nullptr;
     const uint16_t* xn = xt ? xt : x_src;
 
     auto fn = encode_fn_tma_conv();
@@ -1272,7 +1570,22 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         if (r != CUDA_SUCCESS)
             return fail(TILES_ERR_CUDA, "cuTensorMapEncodeTiled(weights) failed (%d)", (int)r);
     }
-    {
+    if (use_direct) {
+        // NCHW input: a stage's raw box is 64 channel rows of xw columns of
+        // one input row.
+        cuuint64_t dims[4] = {static_cast<cuuint64_t>(d->w), static_cast<cuuint64_t>(d->h),
+                              static_cast<cuuint64_t>(d->c), static_cast<cuuint64_t>(d->n)};
+        cuuint64_t strides[3] = {static_cast<cuuint64_t>(d->w) * 2,
+                                 static_cast<cuuint64_t>(d->h) * d->w * 2,
+                                 static_cast<cuuint64_t>(d->c) * d->h * d->w * 2};
+        cuuint32_t box[4] = {static_cast<cuuint32_t>(rp.xw), 1, 64, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult r = fn(&tx, dt, 4, const_cast<uint16_t*>(x_src), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(TILES_ERR_CUDA, "cuTensorMapEncodeTiled(input) failed (%d)", (int)r);
+    } else {
         cuuint64_t dims[4] = {static_cast<cuuint64_t>(d->c), static_cast<cuuint64_t>(d->w),
                               static_cast<cuuint64_t>(d->h), static_cast<cuuint64_t>(d->n)};
         cuuint64_t strides[3] = {static_cast<cuuint64_t>(d->c) * 2,
@@ -1355,6 +1668,12 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
             }
             a.stage_b = rp.n_planes * rp.plane_bytes;
             a.tx_bytes = static_cast<uint32_t>(rp.n_planes * rp.pmax * 128);
+            a.raw_b = rp.raw_b;
+            a.xw = rp.xw;
+            a.phase_planes = 0xffffffffu;
+            for (int p = 0; p < rp.n_planes; ++p)
+                a.phase_planes = (a.phase_planes & ~(15u << (4 * rp.plane_phase[p]))) |
+                                 (static_cast<uint32_t>(p) << (4 * rp.plane_phase[p]));
         } else {
             a.k_stages = static_cast<int32_t>(k_blocks);
             a.stage_b = a.npix * 128;
@@ -1366,17 +1685,42 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         }
         a.idesc = ptx::idesc_f16_f32acc(d->in_dtype == TILES_BF16, false, 128, a.npix);
         a.stages = wp.stages;
-        a.stg_off = wp.stages * a.stage_b;
+        // FORM 2: [raw ring][plane ring][staging]; else [ring][staging].
+        a.raw_stages = use_direct ? wp.stages : 0;
+        a.raw_off = 0;
+        a.ring_off = use_direct ? wp.stages * a.raw_b : 0;
+        a.raw_early = use_direct ? 1 : 0;
+        a.w_off = a.raw_early * a.raw_b;
+        // Direct form: each plane starts some rows into its space so that
+        // the columns one store instruction writes (8 consecutive span
+        // columns) fall in 8 different swizzle rows.  At stride 2 the two
+        // phase planes' rows coincide when the span's columns start even
+        // (the planes need 4 rows between them, mod 8) and are one apart
+        // when odd (5 rows); the start's parity is pw's, the same for every
+        // tile of the launch.  Other strides: plane p starts p rows in.
+        a.plane_rows0 = 0;
+        if (use_direct) {
+            if (d->sw == 2 && rp.n_planes == 2) {
+                const int skew = (d->pw % 2 == 0) ? 4 : 5;
+                for (int p = 0; p < 2; ++p)
+                    if (rp.plane_phase[p] == 1) a.plane_rows0 |= static_cast<uint32_t>(skew) << (4 * p);
+            } else {
+                for (int p = 0; p < rp.n_planes; ++p) a.plane_rows0 |= static_cast<uint32_t>(p) << (4 * p);
+            }
+        }
+        a.stg_off = a.ring_off + wp.stages * a.stage_b;
         // A TMA store reads the box densely: [channel][owc pixels].
         a.tma_store = tma_store ? 1 : 0;
         a.stg_pitch = tma_store ? owc * yb : wp.stg_pitch;
         a.bar_off = a.stg_off + wp.stg_bytes;
         a.w_slots = wp.w_slots;
         smem = wp.smem;
-        e = use_rows ? set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel<true>),
-                                     &g_smem_rows, smem)
-                     : set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel<false>),
-                                     &g_smem_wtmem, smem);
+        e = use_direct ? set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel<2>),
+                                       &g_smem_direct, smem)
+            : use_rows ? set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel<1>),
+                                       &g_smem_rows, smem)
+                       : set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel<0>),
+                                       &g_smem_wtmem, smem);
     } else {
         // Weights stay resident in shared memory when there is one output-
         // channel block and they leave room for at least 3 pixel stages;
@@ -1494,10 +1838,13 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
                 lc.stream = st;
                 lc.attrs = attr;
                 lc.numAttrs = 1;
-                if (use_tmem) {
+                if (use_direct) {
+                    lc.blockDim = dim3(kWtDirectThreads);
+                    e = cudaLaunchKernelEx(&lc, conv_wtmem_kernel<2>, tw, tx, ty, a);
+                } else if (use_tmem) {
                     lc.blockDim = dim3(kWtThreads);
-                    e = use_rows ? cudaLaunchKernelEx(&lc, conv_wtmem_kernel<true>, tw, tx, ty, a)
-                                 : cudaLaunchKernelEx(&lc, conv_wtmem_kernel<false>, tw, tx, ty, a);
+                    e = use_rows ? cudaLaunchKernelEx(&lc, conv_wtmem_kernel<1>, tw, tx, ty, a)
+                                 : cudaLaunchKernelEx(&lc, conv_wtmem_kernel<0>, tw, tx, ty, a);
                 } else {
                     lc.blockDim = dim3(kGemmThreads);
                     e = cudaLaunchKernelEx(&lc, conv_tma_kernel, tw, tx, a, stages, stage_bytes);

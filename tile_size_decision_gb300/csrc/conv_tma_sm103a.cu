@@ -459,6 +459,9 @@ constexpr int kWtWeightBlockBytes = 128 * 128;   // 128 rows x 64 channels x 2 b
 // epilogue's that do not share the MMA issuer's scheduler (warp % 4 != 1);
 // the others there stay idle.
 constexpr int kTrWarps = 12;
+// A warp's items keep its channel half and step 8 kTrWarps / 2 columns, a
+// multiple of 16 so that stride-2 rows advance by a multiple of 8.
+static_assert(kTrWarps % 4 == 0, "transposer count");
 constexpr int kTrFirstWarp = 2 + 8;          // after the producer, the MMA issuer, 8 epilogue warps
 constexpr int kWtDirectThreads =
     (kTrFirstWarp + (kTrWarps - 1) + (kTrWarps - 1) / 3 + 1) * 32;

@@ -285,28 +285,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        {
             // ---------------- MMA issuer ----------------
+            // The loop runs on the whole warp (warp-uniform state); one lane
+            // chosen by elect.sync issues the MMAs and commits.
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool weights_ready = !args.w_resident;
+            // The same lane issues every MMA and commit: a commit tracks the
+            // MMAs of the thread that issues it.
+            const bool issuer = ptx::elect_one_sync();
             for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
                 if (!weights_ready) {
-                    if (!ptx::mbar_wait(&bar->full[kMaxStages - 1], 0, abort, limit)) {
-                        raise_error(args.err, abort, kErrMma);
+                    if (!__all_sync(0xffffffffu,
+                                    ptx::mbar_wait(&bar->full[kMaxStages - 1], 0, abort, limit))) {
+                        if (lane == 0) raise_error(args.err, abort, kErrMma);
                         break;
                     }
                     weights_ready = true;
                 }
-                if (!ptx::mbar_wait(&bar->acc_empty[acc], acc_phase ^ 1u, abort, limit)) {
-                    raise_error(args.err, abort, kErrMma);
+                if (!__all_sync(0xffffffffu,
+                                ptx::mbar_wait(&bar->acc_empty[acc], acc_phase ^ 1u, abort, limit))) {
+                    if (lane == 0) raise_error(args.err, abort, kErrMma);
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + acc * kTmaConvMaxN;
                 bool ok = true;
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
-                    if (!ptx::mbar_wait(&bar->full[stage], phase, abort, limit)) {
-                        raise_error(args.err, abort, kErrMma);
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->full[stage], phase, abort, limit))) {
+                        if (lane == 0) raise_error(args.err, abort, kErrMma);
                         ok = false;
                         break;
                     }
@@ -314,24 +321,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t a0 = ptx::smem_addr(ring + stage * stage_bytes);
                     const uint32_t b0 = args.w_resident ? ptx::smem_addr(wres + kb * w_kblock_bytes)
                                                         : a0 + kTmaConvA;
+                    if (issuer) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // Both operands K-major: 16 channels = 32 bytes of a
-                        // 128-byte row; 8-row groups 1024 B apart.
-                        const uint64_t ad = ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                        ptx::mma_f16<1>(d, ad, bd, args.idesc, (kb | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // Both operands K-major: 16 channels = 32 bytes of a
+                            // 128-byte row; 8-row groups 1024 B apart.
+                            const uint64_t ad = ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                            const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                            ptx::mma_f16<1>(d, ad, bd, args.idesc, (kb | kk) != 0);
+                        }
+                        ptx::mma_commit<1>(&bar->empty[stage]);
                     }
-                    ptx::mma_commit<1>(&bar->empty[stage]);
+                    __syncwarp();
                     if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::mma_commit<1>(&bar->acc_full[acc]);
+                if (issuer) ptx::mma_commit<1>(&bar->acc_full[acc]);
+                __syncwarp();
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            ptx::mma_commit_local<1>(&bar->drain);
-            ptx::mbar_wait(&bar->drain, 0, nullptr, limit);
+            // Every MMA issued here completes before the block tears down.
+            if (issuer) {
+                ptx::mma_commit_local<1>(&bar->drain);
+                ptx::mbar_wait(&bar->drain, 0, nullptr, limit);
+            }
+            __syncwarp();
         }
     } else {
         // ---------------- epilogue (warps 2-5): one output pixel per thread ----------------
@@ -722,8 +737,10 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        {
             // ---------------- MMA issuer ----------------
+            // The loop runs on the whole warp (warp-uniform state); one lane
+            // chosen by elect.sync issues the MMAs and commits.
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             // Pixel rows K-major: 16 channels = 32 bytes of each 128-byte row,
             // 8-row groups 1024 B apart; stages and K steps move the
@@ -742,71 +759,84 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                                  : 0u;
             const int kw = args.kw;
             const uint32_t tap_cols = static_cast<uint32_t>(args.ch_blocks * 32);
-            bool ok = !has_work || ptx::mbar_wait(&bar->wready, 0, abort, limit);
-            if (!ok) raise_error(args.err, abort, kErrMma);
+            // The same lane issues every MMA and commit: a commit tracks the
+            // MMAs of the thread that issues it.
+            const bool issuer = ptx::elect_one_sync();
+            bool ok = __all_sync(0xffffffffu,
+                                 !has_work || ptx::mbar_wait(&bar->wready, 0, abort, limit));
+            if (!ok && lane == 0) raise_error(args.err, abort, kErrMma);
             ptx::tc_fence_after();
             for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-                if (!ptx::mbar_wait(&bar->acc_empty[acc], acc_phase ^ 1u, abort, limit)) {
-                    raise_error(args.err, abort, kErrMma);
+                if (!__all_sync(0xffffffffu,
+                                ptx::mbar_wait(&bar->acc_empty[acc], acc_phase ^ 1u, abort, limit))) {
+                    if (lane == 0) raise_error(args.err, abort, kErrMma);
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(args.npix);
                 for (int kb = 0; kb < args.k_stages; ++kb) {
-                    if (!ptx::mbar_wait(&bar->full[stage], phase, abort, limit)) {
-                        raise_error(args.err, abort, kErrMma);
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->full[stage], phase, abort, limit))) {
+                        if (lane == 0) raise_error(args.err, abort, kErrMma);
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     const uint64_t b_st = b_desc0 + ((stage * stage_bytes) >> 4);
-                    if constexpr (ROWS) {
-                        const int r = kb / args.ch_blocks;
-                        const int chb = kb - r * args.ch_blocks;
-                        // Filter columns of tap (r, 0); tap s adds s * tap_cols.
-                        const uint32_t a_r = tmem + static_cast<uint32_t>(
-                            args.a_col + (r * kw * args.ch_blocks + chb) * 32);
-                        const uint32_t first = kb != 0 ? 1u : 0u;   // 0: the tile's first MMA
-                        if (kw == 3) {
-                            // The common 3-tap row, fully unrolled: 12 MMAs
-                            // with offsets in registers and no branches.
+                    if (issuer) {
+                        if constexpr (ROWS) {
+                            const int r = kb / args.ch_blocks;
+                            const int chb = kb - r * args.ch_blocks;
+                            // Filter columns of tap (r, 0); tap s adds s * tap_cols.
+                            const uint32_t a_r = tmem + static_cast<uint32_t>(
+                                args.a_col + (r * kw * args.ch_blocks + chb) * 32);
+                            const uint32_t first = kb != 0 ? 1u : 0u;   // 0: the tile's first MMA
+                            if (kw == 3) {
+                                // The common 3-tap row, fully unrolled: 12 MMAs
+                                // with offsets in registers and no branches.
 #pragma unroll
-                            for (int t = 0; t < 3; ++t)
+                                for (int t = 0; t < 3; ++t)
 #pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    ptx::mma_f16_tmem_a(d, a_r + t * tap_cols + kk * 8,
-                                                        b_st + tap_off[t] + kk * (32 >> 4),
-                                                        args.idesc,
-                                                        (t | kk) != 0 ? 1u : first);
-                        } else {
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        ptx::mma_f16_tmem_a(d, a_r + t * tap_cols + kk * 8,
+                                                            b_st + tap_off[t] + kk * (32 >> 4),
+                                                            args.idesc,
+                                                            (t | kk) != 0 ? 1u : first);
+                            } else {
 #pragma unroll
-                            for (int t = 0; t < 8; ++t) {
-                                if (t >= kw) break;
-                                const uint64_t b_tap = b_st + tap_off[t];
-                                const uint32_t a0 = a_r + static_cast<uint32_t>(t) * tap_cols;
+                                for (int t = 0; t < 8; ++t) {
+                                    if (t >= kw) break;
+                                    const uint64_t b_tap = b_st + tap_off[t];
+                                    const uint32_t a0 = a_r + static_cast<uint32_t>(t) * tap_cols;
 #pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_tap + kk * (32 >> 4),
-                                                        args.idesc, (kb | t | kk) != 0);
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_tap + kk * (32 >> 4),
+                                                            args.idesc, (kb | t | kk) != 0);
+                                }
                             }
-                        }
-                    } else {
-                        const uint32_t a0 = tmem + static_cast<uint32_t>(args.a_col + kb * 32);
+                        } else {
+                            const uint32_t a0 = tmem + static_cast<uint32_t>(args.a_col + kb * 32);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)   // 16 channels: 8 TMEM columns of A
-                            ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_st + kk * (32 >> 4), args.idesc,
-                                                (kb | kk) != 0);
+                            for (int kk = 0; kk < 4; ++kk)   // 16 channels: 8 TMEM columns of A
+                                ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_st + kk * (32 >> 4), args.idesc,
+                                                    (kb | kk) != 0);
+                        }
+                        ptx::mma_commit<1>(&bar->empty[stage]);
                     }
-                    ptx::mma_commit<1>(&bar->empty[stage]);
+                    __syncwarp();
                     if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::mma_commit<1>(&bar->acc_full[acc]);
+                if (issuer) ptx::mma_commit<1>(&bar->acc_full[acc]);
+                __syncwarp();
                 if (args.acc_bufs == 2) acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            ptx::mma_commit_local<1>(&bar->drain);
-            ptx::mbar_wait(&bar->drain, 0, nullptr, limit);
+            // Every MMA issued here completes before the block tears down.
+            if (issuer) {
+                ptx::mma_commit_local<1>(&bar->drain);
+                ptx::mbar_wait(&bar->drain, 0, nullptr, limit);
+            }
+            __syncwarp();
         }
     } else if (warp < 2 + kWtEpilogueWarps) {
         const int quarter = warp & 3;

@@ -27,6 +27,17 @@ __device__ __forceinline__ uint32_t elect_lane0() {
     return (threadIdx.x & 31) == 0;
 }
 
+// Warp-collective: true in exactly one lane of the (fully converged) warp.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---- clusters ------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

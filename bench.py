@@ -271,8 +271,15 @@ def gemm_job(wl, dev, tiles, torch):
     j.host_out = torch.empty(wl.c_shape(), dtype=j.out.dtype).pin_memory()
     a_d, b_d = j.dev_in
 
-    # A workspace sized for the K-split last round (the default schedule).
-    j.ws = tiles.gemm_workspace(a_d, b_d, j.out)
+    verdict = tiles.plan(wl.m, wl.n, wl.k, b=wl.b, in_dtype=wl.in_dtype, out_dtype=wl.out_dtype,
+                         device=tiles.device_query(dev.index or 0))[0][0]
+    # A workspace with room for every last-round schedule the autotune
+    # times: the planner's own choice, and a K split of its tile (partials).
+    c = verdict.cfg
+    ksplit = tiles.make_config(c.bm, c.bn, c.bk, c.stages, c.threads, c.instr, c.acc_bufs,
+                               c.cta_group, tail="ksplit")
+    j.ws = max(tiles.gemm_workspace(a_d, b_d, j.out), tiles.gemm_workspace(a_d, b_d, j.out, ksplit),
+               key=lambda t: t.numel())
 
     def step(ws, stream):
         if wl.b > 1:
@@ -285,10 +292,7 @@ def gemm_job(wl, dev, tiles, torch):
     j.flops = wl.flops
     j.bound = "tensor"
     j.bytes = wl.b * (wl.m * wl.k + wl.k * wl.n) * 2 + wl.b * wl.m * wl.n * S.DTYPE_BYTES[wl.out_dtype]
-    verdict = tiles.plan(wl.m, wl.n, wl.k, b=wl.b, in_dtype=wl.in_dtype, out_dtype=wl.out_dtype,
-                         device=tiles.device_query(dev.index or 0))[0][0]
     sch = tiles.gemm_schedule(a_d, b_d, j.out, workspace=j.ws)
-    c = verdict.cfg
     j.config = {
         "workload": wl.name, "b": wl.b, "m": wl.m, "n": wl.n, "k": wl.k,
         "in_dtype": wl.in_dtype, "out_dtype": wl.out_dtype, "accumulate": "f32",

@@ -32,8 +32,10 @@ Rules
        fills at most half the groups) ceil(K/bk) * unit of the half-width
        tile; K parts s in 2..min(resident // rest, 8, K blocks):
        ceil(K/bk / s) * unit + (s-1) * reduce with reduce =
-       2 * ceil((bm/cg)*bn*4 / fill_bytes_per_clk) + 2048.  tail_split
-       reports s, -1 for N-halves, 0 for whole tiles.
+       2 * ceil((bm/cg)*bn*4 / PARTIAL_BYTES_PER_CLK) + 2048: a K part's
+       fp32 partial goes out and comes back at 32 bytes per clock per SM,
+       the rate measured for it on GB300 (not the operand fill rate).
+       tail_split reports s, -1 for N-halves, 0 for whole tiles.
   rank (est_clocks, round(C0), -bps, smem_total), stable over the variant
        order.
 """
@@ -177,6 +179,7 @@ MAX_TAIL_PARTS = 8
 
 
 HANDOFF_CLOCKS = 2048
+PARTIAL_BYTES_PER_CLK = 32
 
 
 def _stage_bytes(bm: int, bn: int, bk: int, cg: int, in_bytes: int = 2) -> int:
@@ -215,7 +218,7 @@ def tail_choice(v: GB300Verdict, dev: GB300Device, kblocks: int, resident: int):
         t = kblocks * _unit(dev, cfg.bm, cfg.bn // 2, cfg.bk, cg)
         if t < best[2]:
             best = ("nhalf", 0, t)
-    reduce = 2 * page.ceil_div((cfg.bm // cg) * cfg.bn * 4, dev.fill_bytes_per_clk) + HANDOFF_CLOCKS
+    reduce = 2 * page.ceil_div((cfg.bm // cg) * cfg.bn * 4, PARTIAL_BYTES_PER_CLK) + HANDOFF_CLOCKS
     for s in range(2, min(resident // rest, MAX_TAIL_PARTS, kblocks) + 1):
         t = page.ceil_div(kblocks, s) * unit + (s - 1) * reduce
         if t < best[2]:

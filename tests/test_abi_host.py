@@ -264,9 +264,11 @@ def test_gb300_choice_at_the_bench_shape(lib):
     # a third less operand traffic per SM, and the least C0.
     assert (best.cfg.bm, best.cfg.bn, best.cfg.stages, best.cfg.cta_group) == (256, 256, 7, 2)
     assert best.grid == 256 and best.waves == 4
-    # 256 tiles on 74 pairs: 3 whole rounds and 34 tiles left, each split
-    # along K into 74 // 34 = 2 parts.
-    assert best.tail_split == 2
+    # 256 tiles on 74 pairs: 3 whole rounds and 34 tiles left, which fill
+    # at most half the pairs, so they run as 68 N-half tiles: 64 K blocks
+    # of the half-width unit (384 clocks, fill-bound) = 24,576 clocks,
+    # against 32 * 512 + 2 * 4096 + 2048 = 26,624 for two K parts.
+    assert best.tail_split == -1
 
 
 # --------------------------------------------------------------------------- #

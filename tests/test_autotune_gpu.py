@@ -107,7 +107,11 @@ def test_tuned_ksplit_without_workspace_room_falls_back():
     a_np, b_np = inputs(m, n, k, dt, 60)
     a, b = to_cuda(a_np, dt), to_cuda(b_np, dt)
     c = empty_out((m, n), dt)
-    big = T.gemm_workspace(a, b, c)
+    # Room for the partial tiles of a K-split last round of the planner's tile.
+    f = T.plan(m, n, k, in_dtype=dt, out_dtype=dt, device=T.device_query(0))[0][0].cfg
+    ks = T.make_config(f.bm, f.bn, f.bk, f.stages, f.threads, f.instr, f.acc_bufs, f.cta_group,
+                       tail="ksplit")
+    big = T.gemm_workspace(a, b, c, ks)
     best, rows = T.gemm_autotune(a, b, c, top_k=1, reps=2, workspace=big)
     small = T.workspace()
     out = empty_out((m, n), dt)

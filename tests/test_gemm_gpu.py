@@ -266,10 +266,16 @@ def test_ksplit_tail_is_deterministic(ws):
     a, b = S.gemm_inputs(wl)
     ta, tb = to_cuda(a, wl.in_dtype), to_cuda(b, wl.in_dtype)
     c1 = empty_out(wl.c_shape(), wl.out_dtype)
-    w = T.gemm_workspace(ta, tb, c1)
-    assert T.gemm_schedule(ta, tb, c1, workspace=w).tail_mode == 2
-    T.gemm(ta, tb, out=c1, workspace=w)
-    c2 = T.gemm(ta, tb, out_dtype="f32", workspace=w)
+    # The planner's tile with its last round forced to K parts (the planner
+    # itself prefers N-halves here).
+    f = T.plan(wl.m, wl.n, wl.k, in_dtype=wl.in_dtype, out_dtype=wl.out_dtype,
+               device=T.device_query(0))[0][0].cfg
+    cfg = T.make_config(f.bm, f.bn, f.bk, f.stages, f.threads, f.instr, f.acc_bufs, f.cta_group,
+                        tail="ksplit")
+    w = T.gemm_workspace(ta, tb, c1, cfg)
+    assert T.gemm_schedule(ta, tb, c1, cfg=cfg, workspace=w).tail_mode == 2
+    T.gemm(ta, tb, out=c1, cfg=cfg, workspace=w)
+    c2 = T.gemm(ta, tb, out_dtype="f32", cfg=cfg, workspace=w)
     T.check(w)
     assert torch.equal(c1, c2)
 

@@ -229,9 +229,12 @@ int64_t gb300_unit_clocks(const tiles_device& dev, const tiles_config& cfg, int6
 
 int64_t gb300_reduce_clocks(const tiles_device& dev, const tiles_config& cfg) {
     // One fp32 partial tile per CTA written by a leading part and read back
-    // by the last part, plus the hand-off's fixed latency.
+    // by the last part, plus the hand-off's fixed latency.  The partials
+    // move at kPartialBytesPerClk, not at the operand fill rate: they are
+    // written while every SM stores at once into an L2 full of dirty lines.
+    (void)dev;
     const int cg = std::max(cfg.cta_group, 1);
-    return 2 * ceil_div((int64_t)(cfg.bm / cg) * cfg.bn * 4, std::max(dev.fill_bytes_per_clk, 1)) +
+    return 2 * ceil_div((int64_t)(cfg.bm / cg) * cfg.bn * 4, kPartialBytesPerClk) +
            kTailHandoffClocks;
 }
 

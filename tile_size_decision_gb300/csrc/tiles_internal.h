@@ -59,6 +59,11 @@ TailChoice gb300_tail_choice(const tiles_device& dev, const tiles_config& cfg, i
                              int64_t resident, int64_t k_blocks, int in_bytes, int forced);
 // Fixed clocks of a K-part hand-off (flag release, acquire, copy latency).
 constexpr int64_t kTailHandoffClocks = 2048;
+// Bytes per clock per SM at which a K part writes or reads its fp32
+// partial tile.  Measured on the 4096^3 GEMM after an L2-flushing write:
+// a CTA's 128 KB partial took ~5,300 clocks out (~25 B/clk) whether written
+// as 4-byte or 16-byte lane stores.
+constexpr int64_t kPartialBytesPerClk = 32;
 constexpr int kMaxTailParts = 8;
 void device_preset_h100(tiles_device* d);
 void device_preset_gb300(tiles_device* d);

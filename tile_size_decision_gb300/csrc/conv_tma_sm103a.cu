@@ -494,6 +494,7 @@ struct WtBarriers {
     uint64_t wfull;      // a pass of filter blocks landed in shared memory
     uint64_t wcons;      // the epilogue warps copied that pass to tensor memory
     uint64_t wready;     // the whole filter is in tensor memory
+    int32_t raw_col0[kMaxStages];   // FORM 2: span column origin of each raw slot's box
     uint32_t tmem_base;
     int abort;
 };
@@ -656,6 +657,9 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                     }
                     const RowStage st = row_stage(u, kb, args);
                     uint64_t* rfull = &bar->full[stages + rs];
+                    // The transposers read the box's column origin after
+                    // waiting on the slot's barrier (the arrive releases it).
+                    bar->raw_col0[rs] = st.col0;
                     ptx::mbar_arrive_expect_tx(rfull, raw_tx);
                     tma_load_4d(base + args.raw_off + rs * args.raw_b, &tmX, rfull, st.col0 & ~7,
                                 st.ih, st.c0, st.img);
@@ -1087,26 +1091,36 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
         uint32_t ps = 0, pphase = 0, rs = 0, rphase = 0;
         // The planes reuse the filter's start-up space.
         bool ok = !has_work || __all_sync(0xffffffffu, ptx::mbar_wait(&bar->wready, 0, abort, limit));
+        // Per-unit lane set-up, recomputed only when a box's column origin
+        // (written by the producer beside the box) changes: with one W tile
+        // every unit's boxes start at the same column.
+        int cached_col0 = INT32_MIN, t0 = 0, lane_off = 0, pl0 = 15, co[4] = {0, 0, 0, 0};
         for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-            // Span column of raw column 0 (the box starts at the span's
-            // 8-column group), and of this lane's first item.
-            const int x_first = -(row_stage(u, 0, args).col0 & 7);
-            const int t0 = x_first + 8 * g0 + px;
-            int lane_off = 0, pl0 = 15, co[4] = {0, 0, 0, 0};
-            if (fast) {
-                const int phi = ((t0 % args.sw) + args.sw) % args.sw;
-                const int jr0 = (t0 - phi) / args.sw;
-                pl0 = static_cast<int>((args.phase_planes >> (4 * phi)) & 15u);
-                const int rr0 = static_cast<int>((args.plane_rows0 >> (4 * pl0)) & 15u) + jr0;
-                lane_off = pl0 * args.plane_bytes + rr0 * 128 + pair;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) co[m] = ((half * 4 + m) ^ (rr0 & 7)) << 4;
-            }
             for (int kb = 0; kb < args.k_stages; ++kb) {
                 ok = __all_sync(0xffffffffu,
                                 ptx::mbar_wait(&bar->full[stages + rs], rphase, abort, limit)) &&
                      __all_sync(0xffffffffu, ptx::mbar_wait(&bar->empty[ps], pphase ^ 1u, abort, limit));
                 if (!ok) break;
+                if (kb == 0) {
+                    const int col0 = static_cast<volatile int32_t*>(bar->raw_col0)[rs];
+                    if (col0 != cached_col0) {
+                        cached_col0 = col0;
+                        // Span column of raw column 0 (the box starts at the
+                        // span's 8-column group), and of this lane's first item.
+                        const int x_first = -(col0 & 7);
+                        t0 = x_first + 8 * g0 + px;
+                        if (fast) {
+                            const int phi = ((t0 % args.sw) + args.sw) % args.sw;
+                            const int jr0 = (t0 - phi) / args.sw;
+                            pl0 = static_cast<int>((args.phase_planes >> (4 * phi)) & 15u);
+                            const int rr0 =
+                                static_cast<int>((args.plane_rows0 >> (4 * pl0)) & 15u) + jr0;
+                            lane_off = pl0 * args.plane_bytes + rr0 * 128 + pair;
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) co[m] = ((half * 4 + m) ^ (rr0 & 7)) << 4;
+                        }
+                    }
+                }
                 const uint32_t raw = ptx::smem_addr(base + args.raw_off + rs * args.raw_b) + ld_off;
                 uint8_t* slot = ring + ps * stage_bytes;
                 // All of this warp's items (at most kTrItems: items <= 64)

@@ -373,6 +373,43 @@ int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_co
 int tiles_conv2d_tiled(const tiles_conv_desc* desc, int tile_oh, int tile_ow, int tile_n,
                        const tiles_config* cfg, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- End to end from host memory ---------------------------------------
+ * The same operations with their operands starting, and their results
+ * ending, in host memory: the call a user with host data makes.  The source
+ * pages have no counterpart (they state the operation on resident operands);
+ * these calls add only the copies around the kernels above.
+ *
+ * The descriptor describes the caller's device buffers as for the device
+ * calls; each host buffer mirrors its device buffer (the same layout, pitches
+ * and batch strides).  Host buffers should be page-locked (cudaHostAlloc,
+ * cudaHostRegister): pageable memory still works, but its copies do not
+ * overlap anything.  The call enqueues, ordered after earlier work on
+ * `stream`:
+ *   - the operands that every piece needs (B of a single GEMM, the filter),
+ *   - then, piece by piece (chunks pieces: runs of batch items or images, or
+ *     for a single GEMM runs of rows of A and C rounded to whole tiles), the
+ *     piece's inputs, its kernels as soon as they have landed, and its
+ *     results back to the host as soon as the kernels are done.
+ * Host-to-device and device-to-host copies run on two copy streams the
+ * library creates on a host thread's first call on a device and keeps; the
+ * kernels run on `stream`, and work enqueued on `stream` after the call
+ * starts once every result is in host memory.  No device memory is
+ * allocated.  chunks is in 1 .. 16.  Calls that share device buffers and
+ * overlap (different streams) race.  On an error some pieces may already be
+ * enqueued; the status is that of the first failing step (tiles_last_error). */
+
+/* tiles_gemm_batched from host buffers a_host, b_host to c_host. */
+int tiles_gemm_host(const tiles_gemm_desc* desc, const tiles_config* cfg, const void* a_host,
+                    const void* b_host, void* c_host, int chunks, void* workspace,
+                    size_t ws_bytes, void* stream);
+
+/* tiles_conv2d_htiled from host buffers x_host, w_host to y_host; the pieces
+ * are runs of images.  The workspace must serve the whole batch (it then
+ * serves every piece). */
+int tiles_conv2d_host(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
+                      const void* x_host, const void* w_host, void* y_host, int chunks,
+                      void* workspace, size_t ws_bytes, void* stream);
+
 /* Workspace bytes the TMA producer needs for this convolution (256 when it
  * does not apply; 0 on invalid arguments). */
 size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh);

@@ -305,6 +305,30 @@ def test_gemm_validation(lib, kw, status):
     assert lib.tiles_last_error() != b""
 
 
+def test_host_calls_check_arguments_before_any_cuda_call(lib):
+    # Host-buffer calls reject missing buffers and piece counts outside
+    # 1..16 before touching a device.
+    d = _desc()
+    h = C.c_void_p(0x40000)
+    assert lib.tiles_gemm_host(C.byref(d), None, None, h, h, 4, None, 0, None) == _abi.ERR_INVALID_ARG
+    assert lib.tiles_gemm_host(None, None, h, h, h, 4, None, 0, None) == _abi.ERR_INVALID_ARG
+    for chunks in (0, 17):
+        assert lib.tiles_gemm_host(C.byref(d), None, h, h, h, chunks, None, 0, None) == \
+            _abi.ERR_INVALID_ARG
+        assert b"chunks" in lib.tiles_last_error()
+    cd = _abi.ConvDesc()
+    cd.n, cd.c, cd.h, cd.w, cd.c_out, cd.kh, cd.kw = 1, 8, 9, 9, 4, 3, 3
+    cd.sh = cd.sw = cd.dh = cd.dw = 1
+    cd.x, cd.wt, cd.y = 0x10000, 0x20000, 0x30000
+    assert lib.tiles_conv2d_host(C.byref(cd), 4, None, h, None, h, 2, None, 0, None) == \
+        _abi.ERR_INVALID_ARG
+    assert lib.tiles_conv2d_host(C.byref(cd), 4, None, h, h, h, 0, None, 0, None) == \
+        _abi.ERR_INVALID_ARG
+    cd.kh = 0
+    assert lib.tiles_conv2d_host(C.byref(cd), 4, None, h, h, h, 2, None, 0, None) == \
+        _abi.ERR_INVALID_ARG
+
+
 def test_plan_validation(lib):
     dev = T.device_preset("gb300")
     p = _abi.Problem()

@@ -19,6 +19,7 @@ __all__ = [
     "TilesError", "load", "version", "device_preset", "device_query", "evaluate",
     "finish_parallelism", "c0_bytes", "plan", "htile_rows", "workspace_bytes", "workspace",
     "gemm", "gemm_batched", "gemm_schedule", "gemm_workspace", "gemm_noalloc", "gemm_autotune",
+    "gemm_host", "conv2d_host",
     "tuned_lookup", "tuned_save", "tuned_load", "tuned_clear", "conv2d_htiled", "conv2d_tiled",
     "conv_workspace",
     "conv_out_shape", "check", "selftest_wait_timeout", "make_config",
@@ -256,6 +257,48 @@ def gemm_batched(a, b, out=None, out_dtype=None, cfg=None, workspace=None, strea
     _check(load().tiles_gemm_batched(C.byref(d), _cfg_ptr(cfg), ws, wsb, _stream_handle(stream)),
            "tiles_gemm_batched")
     return out
+
+
+def _mirror(host, dev, nm):
+    """A host tensor that mirrors a device tensor (same shape, dtype, strides)."""
+    if host.is_cuda or tuple(host.shape) != tuple(dev.shape) or host.dtype != dev.dtype \
+            or host.stride() != dev.stride():
+        raise ValueError(f"{nm}: the host tensor must mirror its device tensor "
+                         "(same shape, dtype and strides, in host memory)")
+
+
+def gemm_host(a_host, b_host, out_host, a_dev, b_dev, out_dev, cfg=None, workspace=None,
+              stream=None, chunks=4):
+    """out_host = a_host @ b_host (2-D, or 3-D batched) through the device
+    buffers a_dev, b_dev, out_dev: uploads, GEMMs and downloads in `chunks`
+    overlapping pieces (tiles_gemm_host).  Host tensors should be pinned."""
+    for h, dv, nm in ((a_host, a_dev, "a"), (b_host, b_dev, "b"), (out_host, out_dev, "out")):
+        _mirror(h, dv, nm)
+    d = _gemm_desc(*_batched3(a_dev, b_dev, out_dev), batched=True)
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().tiles_gemm_host(C.byref(d), _cfg_ptr(cfg), a_host.data_ptr(), b_host.data_ptr(),
+                                  out_host.data_ptr(), chunks, ws, wsb, _stream_handle(stream)),
+           "tiles_gemm_host")
+    return out_host
+
+
+def conv2d_host(x_host, w_host, y_host, x_dev, w_dev, y_dev, stride=(1, 1), pad=(0, 0),
+                dil=(1, 1), tile_oh=16, cfg=None, workspace=None, stream=None, layout="nchw",
+                chunks=4):
+    """y_host = conv2d(x_host, w_host) through the device buffers x_dev, w_dev,
+    y_dev: uploads, convolutions and downloads in `chunks` overlapping runs
+    of images (tiles_conv2d_host).  Host tensors should be pinned."""
+    for h, dv, nm in ((x_host, x_dev, "x"), (w_host, w_dev, "w"), (y_host, y_dev, "y")):
+        _mirror(h, dv, nm)
+    d = _conv_desc(x_dev, w_dev, stride, pad, dil, y_dev, layout)
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().tiles_conv2d_host(C.byref(d), tile_oh, _cfg_ptr(cfg), x_host.data_ptr(),
+                                    w_host.data_ptr(), y_host.data_ptr(), chunks, ws, wsb,
+                                    _stream_handle(stream)),
+           "tiles_conv2d_host")
+    return y_host
 
 
 def conv_out_hw(h, w, kh, kw, stride, pad, dil):

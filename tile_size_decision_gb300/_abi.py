@@ -154,6 +154,11 @@ SIGNATURES = {
                                       C.c_void_p, C.c_size_t, C.c_void_p]),
     "tiles_gemm_noalloc": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_void_p,
                                      C.c_int]),
+    "tiles_gemm_host": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_void_p, C.c_void_p,
+                                  C.c_void_p, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "tiles_conv2d_host": (C.c_int, [C.POINTER(ConvDesc), C.c_int, C.POINTER(Config), C.c_void_p,
+                                    C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_size_t,
+                                    C.c_void_p]),
     "tiles_conv2d_tiled": (C.c_int, [C.POINTER(ConvDesc), C.c_int, C.c_int, C.c_int,
                                      C.POINTER(Config), C.c_void_p, C.c_size_t, C.c_void_p]),
     "tiles_conv_workspace_bytes": (C.c_size_t, [C.POINTER(ConvDesc), C.c_int]),

@@ -45,6 +45,7 @@ def units():
         ("api.cu", "api.o", []),
         ("conv_sm103a.cu", "conv_sm103a.o", []),
         ("conv_tma_sm103a.cu", "conv_tma_sm103a.o", []),
+        ("host_pipeline.cu", "host_pipeline.o", []),
     ]
     for bn, cg in GEMM_VARIANTS:
         out.append(("gemm_sm103a.cu", f"gemm_bn{bn}_cg{cg}.o",

@@ -518,3 +518,32 @@ def test_direct_rows_refused_where_it_does_not_apply():
         with pytest.raises(T.TilesError) as e:
             T.conv2d_htiled(x, w, (1, 1), (1, 1), (1, 1), 4, workspace=ws, cfg=cfg, layout=layout)
         assert e.value.status == -4
+
+
+@pytest.mark.parametrize("case", [
+    # (n, c, h, w, co, stride, dtype, layout): 3x3 filters over 64 input
+    # channels (9 K blocks, which fit tensor memory), taken there straight
+    # from their OIHW rows; c_out below 128 leaves TMEM rows zero-filled.
+    (2, 64, 20, 24, 96, (1, 1), S.BF16, "nchw"),
+    (1, 64, 17, 16, 128, (2, 2), S.F16, "nchw"),
+    (2, 64, 12, 16, 40, (1, 1), S.F16, "nhwc"),
+    (1, 64, 9, 8, 128, (2, 2), S.BF16, "nhwc"),
+])
+def test_raw_oihw_filter_in_tensor_memory(case):
+    n, c, h, wd, co, st, dt, layout = case
+    x_np = S.random_matrix(91, (n, c, h, wd), dt)
+    w_np = S.random_matrix(92, (co, c, 3, 3), dt)
+    x = to_cuda(x_np, dt)
+    if layout == "nhwc":
+        x = x.permute(0, 2, 3, 1).contiguous()
+    w = to_cuda(w_np, dt)
+    oh, ow = T.conv_out_hw(h, wd, 3, 3, st, (1, 1), (1, 1))
+    y = torch.full((n, co, oh, ow), float("nan"), dtype=torch.float32, device="cuda")
+    wsp = T.conv_workspace(x, w, st, (1, 1), (1, 1), 4, layout=layout)
+    T.conv2d_htiled(x, w, st, (1, 1), (1, 1), 4, out=y, workspace=wsp, layout=layout)
+    T.check(wsp)
+    # The filter went to tensor memory from the caller's rows: nothing wrote
+    # the workspace's reordered-filter area (it follows the 256-byte header).
+    assert int(wsp[256:256 + co * 9 * c * 2].count_nonzero()) == 0
+    check_against_oracle(to_f64(y), S.widen(x_np, dt), S.widen(w_np, dt), st, (1, 1), (1, 1),
+                         S.F32)

@@ -73,6 +73,7 @@ struct ConvTmaArgs {
     // pixel tap_shift[s] on.  k_stages = kh * ch_blocks (else k_blocks).
     int32_t k_stages, n_planes, plane_bytes, pmax;
     int32_t tma_store;                    // rows form: the staged tile leaves by one TMA store
+    int32_t raw_filter;                   // filter in TMEM read from the caller's OIHW rows (3x3)
     int32_t tap_plane[8], tap_shift[8], plane_phase[8];
     // Rows form over an NCHW input read in place (FORM 2): each stage's raw
     // box, 64 channel rows of xw input columns (xw / 8 odd), lands in one of
@@ -478,6 +479,8 @@ constexpr int kTrWarps = 12;
 // multiple of 16 so that stride-2 rows advance by a multiple of 8.
 static_assert(kTrWarps % 4 == 0, "transposer count");
 constexpr int kTrFirstWarp = 2 + 8;          // after the producer, the MMA issuer, 8 epilogue warps
+// Boxes of 64 elements per 64 input channels of a 3x3 filter's OIHW row.
+constexpr int kRawFilterBoxes = 9;
 constexpr int kWtDirectThreads =
     (kTrFirstWarp + (kTrWarps - 1) + (kTrWarps - 1) / 3 + 1) * 32;
 static_assert(kTrFirstWarp % 4 == 2, "transposer warp mapping assumes warp 10 sits on scheduler 2");
@@ -572,7 +575,11 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
     WtBarriers* bar = reinterpret_cast<WtBarriers*>(base + args.bar_off);
     const int stages = args.stages;
     const uint32_t stage_bytes = static_cast<uint32_t>(args.stage_b);
-    const int passes = (args.k_blocks + args.w_slots - 1) / args.w_slots;
+    // Filter passes.  Reordered filter: w_slots K blocks per pass.  Raw
+    // filter (3x3, C a multiple of 64): one pass per 64 input channels, the
+    // 9 boxes of 64 elements of each OIHW row that hold them.
+    const int passes = args.raw_filter ? args.ch_blocks
+                                       : (args.k_blocks + args.w_slots - 1) / args.w_slots;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -632,8 +639,8 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                     aborted = true;
                     return;
                 }
-                const int kb0 = p * args.w_slots;
-                const int nkb = min(args.w_slots, args.k_blocks - kb0);
+                const int kb0 = args.raw_filter ? p * kRawFilterBoxes : p * args.w_slots;
+                const int nkb = args.raw_filter ? kRawFilterBoxes : min(args.w_slots, args.k_blocks - kb0);
                 ptx::mbar_arrive_expect_tx(&bar->wfull, static_cast<uint32_t>(nkb * kWtWeightBlockBytes));
                 for (int i = 0; i < nkb; ++i)
                     ptx::tma_load_3d(base + args.w_off + i * kWtWeightBlockBytes, &tmW, &bar->wfull,
@@ -856,6 +863,44 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                 if (lane == 0) raise_error(args.err, abort, kErrEpilogue);
                 ok = false;
                 break;
+            }
+            if (args.raw_filter) {
+                // Pass p holds input channels 64p .. 64p+63 of every OIHW row:
+                // element e = channel * 9 + tap of the pass, box e / 64,
+                // 16-byte chunk (e % 64) / 8 at chunk ^ (row & 7).  This
+                // thread builds row co's 32 channels half*32 .. +31, eight at
+                // a time: the 72 elements of 8 channels are 9 chunks, and each
+                // TMEM column (tap t, channels 2j, 2j+1) takes two halves of
+                // them (K order (tap, channel), two channels per column).
+                const uint8_t* rowb = base + args.w_off + co * 128;
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) {
+                    const int cl = half * 32 + k * 8;          // first channel of the chunk
+                    uint32_t L[36];
+#pragma unroll
+                    for (int q = 0; q < 9; ++q) {
+                        const int qq = (cl / 8) * 9 + q;
+                        const uint4 v = *reinterpret_cast<const uint4*>(
+                            rowb + (qq >> 3) * kWtWeightBlockBytes + (((qq & 7) ^ (co & 7)) << 4));
+                        L[4 * q] = v.x; L[4 * q + 1] = v.y; L[4 * q + 2] = v.z; L[4 * q + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int t = 0; t < kRawFilterBoxes; ++t) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int e0 = 18 * jj + t, e1 = e0 + 9;
+                            o[jj] = __byte_perm(L[e0 >> 1], L[e1 >> 1],
+                                                ((e0 & 1) ? 0x32u : 0x10u) | ((e1 & 1) ? 0x7600u : 0x5400u));
+                        }
+                        ptx::tmem_st_4cols(tmem + lane_base +
+                                               static_cast<uint32_t>(args.a_col + (t * args.ch_blocks + p) * 32 + cl / 2),
+                                           o);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bar->wcons);
+                continue;
             }
             const int kb0 = p * args.w_slots;
             const int nkb = min(args.w_slots, args.k_blocks - kb0);
@@ -1587,6 +1632,23 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     if (weights_mode == TILES_CONV_W_TMEM && !use_tmem)
         return fail(TILES_ERR_INFEASIBLE,
                     "the filter does not fit tensor memory (needs c_out <= 128 and kh*kw*ceil(c/64) <= 14)");
+    // A 3x3 filter over whole 64-channel blocks that goes to tensor memory
+    // (with no NHWC copy of the input to prepare) is read straight from the
+    // caller's OIHW rows: the kernel puts it in K order, one pass of 9 boxes
+    // per channel block, and there is no reorder launch.  The pass needs 9
+    // blocks of start-up space; a smaller plan pads its staging area.
+    const bool raw_shape = use_tmem && (d->x_layout != TILES_LAYOUT_NCHW || use_direct) &&
+                           d->kh * d->kw == kRawFilterBoxes && d->c % 64 == 0 &&
+                           d->c_out <= 128 && (reinterpret_cast<uintptr_t>(d->wt) & 15u) == 0;
+    if (raw_shape && wp.w_slots < kRawFilterBoxes) {
+        const int extra = (kRawFilterBoxes - wp.w_slots) * kWtWeightBlockBytes;
+        if (wp.smem + extra <= 227 * 1024) {
+            wp.stg_bytes += extra;
+            wp.smem += extra;
+            wp.w_slots = kRawFilterBoxes;
+        }
+    }
+    const bool raw_filter = raw_shape && wp.w_slots >= kRawFilterBoxes;
     const int owc = use_tmem ? wp.owc : g.owc;
     const int nr = use_tmem ? wp.nr : g.nr;
 
@@ -1604,14 +1666,16 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     CUtensorMap tw, tx;
     {
         // Weight rows [c_out][kh*kw*Cp]: K blocks of 64 channels x (the
-        // output-channel block, or 128 rows with zero fill for TMEM).
+        // output-channel block, or 128 rows with zero fill for TMEM).  The
+        // raw OIHW rows have the same length (Cp = C).
         const int64_t k = static_cast<int64_t>(d->kh) * d->kw * g.cp;
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(d->c_out), 1};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(k) * 2,
                                  static_cast<cuuint64_t>(k) * 2 * static_cast<cuuint64_t>(d->c_out)};
         cuuint32_t box[3] = {64, static_cast<cuuint32_t>(use_tmem ? 128 : g.bn), 1};
         cuuint32_t estr[3] = {1, 1, 1};
-        CUresult r = fn(&tw, dt, 3, wr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+        void* wbase = raw_filter ? const_cast<void*>(d->wt) : static_cast<void*>(wr);
+        CUresult r = fn(&tw, dt, 3, wbase, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS)
@@ -1758,6 +1822,7 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         a.stg_off = a.ring_off + wp.stages * a.stage_b;
         // A TMA store reads the box densely: [channel][owc pixels].
         a.tma_store = tma_store ? 1 : 0;
+        a.raw_filter = raw_filter ? 1 : 0;
         a.stg_pitch = tma_store ? owc * yb : wp.stg_pitch;
         a.bar_off = a.stg_off + wp.stg_bytes;
         a.w_slots = wp.w_slots;
@@ -1820,7 +1885,7 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
             else
                 nchw_to_nhwc_kernel<false><<<grid, 256, 0, st>>>(x_src, xt, d->c, d->h, d->w);
         }
-    } else {
+    } else if (!raw_filter) {
         reorder_weights_kernel<<<w_blocks, 256, 0, st>>>(wsrc, wr, d->c, g.cp, d->kh, d->kw,
                                                          w_total);
     }

@@ -364,6 +364,14 @@ __device__ __forceinline__ void tmem_ld_wait() {
 
 // Warp-collective store of 32 consecutive fp32 columns into the warp's 32
 // TMEM lanes (the inverse of tmem_ld_32cols).
+// Warp-collective store of 4 consecutive 32-bit columns of the warp's 32
+// TMEM lanes (lane i writes row lane base + i).
+__device__ __forceinline__ void tmem_st_4cols(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "

@@ -408,7 +408,8 @@ def gemm_schedule(a, b, out, cfg=None, workspace=None):
 
 
 def gemm_workspace(a, b, out, cfg=None):
-    """A zeroed workspace large enough for this GEMM's K-split last round."""
+    """A zeroed workspace large enough for this GEMM's schedule under cfg (the
+    partial tiles of a K-split last round, when that is the schedule)."""
     torch = _torch()
     d = _gemm_desc(*_batched3(a, b, out), batched=True)
     n = int(load().tiles_gemm_workspace_bytes(C.byref(d), _cfg_ptr(cfg)))

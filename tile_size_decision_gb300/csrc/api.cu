@@ -275,10 +275,12 @@ int gemm_prepare(const tiles_gemm_desc* d, const tiles_config* user_cfg, bool ba
     const tiles_config& cfg = gp->cfg;
     gp->tiles = d->batch * ((d->m + cfg.bm - 1) / cfg.bm) * ((d->n + cfg.bn - 1) / cfg.bn);
     if (gp->tiles > INT32_MAX / 2) return fail(TILES_ERR_TOO_LARGE, "too many output tiles");
-    // Wave-aware schedule (C4): rounds of the resident groups.  A last round
-    // that would fill at most half of them is split: along K into
-    // ksplit = resident / rest parts when the workspace holds the partial
-    // tiles, else into N-halves when those are whole B atoms.
+    // Wave-aware schedule (C4): rounds of the resident groups.  A partial
+    // last round runs as whole tiles, as N-halves (when it fills at most half
+    // of the groups and the halves are whole B atoms) or split along K
+    // (when the workspace holds the partial tiles): the cheapest under the
+    // planner's time model (gb300_tail_choice), or the one the configuration
+    // forces.
     gp->resident = max_groups(gp->ordinal, cfg.bn, cfg.cta_group, gp->dev.sm_count);
     gp->full_units = gp->units = gp->tiles;
     gp->tail_mode = kTailNone;

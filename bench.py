@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import csv
 import hashlib
+import re
 import io
 import json
 import os
@@ -106,13 +107,28 @@ WORKLOAD_SOURCES = {
 }
 
 
-def kernel_source_hash(workload: str) -> str:
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and with whitespace collapsed: an
+    edit to a comment leaves a recorded figure valid, a code change does not.
+    (String literals holding comment markers are not special-cased; the
+    hashed sources have none that matter.)"""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(workload: str, read=None) -> str:
+    """Hash of the code (comments dropped) of the sources a workload's kernels
+    and launch shapes come from; `read(name)` returns a source's text."""
     kind = "conv" if workload.startswith("conv") else "gemm"
-    h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tile_size_decision_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                return f.read()
+    h = hashlib.sha256()
     for name in sorted(SHARED_SOURCES + WORKLOAD_SOURCES[kind]):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        h.update(name.encode() + code_only(read(name)).encode())
     return h.hexdigest()[:16]
 
 

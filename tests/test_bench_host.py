@@ -1,0 +1,40 @@
+"""Host logic of bench.py that decides what a bench line reports (no GPU)."""
+
+import os
+
+import bench
+
+
+def test_code_only_drops_comments_and_collapses_whitespace():
+    src = "int a = 1; // one\n/* block\n comment */ int  b =\n 2;\n"
+    assert bench.code_only(src) == "int a = 1; int b = 2;"
+
+
+def test_source_hash_ignores_comment_edits_but_not_code_edits():
+    csrc = os.path.join(os.path.dirname(bench.__file__), "tile_size_decision_gb300", "csrc")
+
+    def read(name):
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            return f.read()
+
+    base = bench.kernel_source_hash("gemm_4096", read)
+    assert base == bench.kernel_source_hash("gemm_4096")
+    commented = lambda name: read(name) + ("\n// a note\n/* another */\n" if name == "api.cu" else "")
+    assert bench.kernel_source_hash("gemm_4096", commented) == base
+    edited = lambda name: read(name) + ("\nstatic int unused_edit = 1;\n" if name == "api.cu" else "")
+    assert bench.kernel_source_hash("gemm_4096", edited) != base
+    # The convolution's figure depends on its own sources, not the GEMM's API file.
+    assert bench.kernel_source_hash("conv_htiled", edited) == bench.kernel_source_hash("conv_htiled")
+
+
+def test_recorded_traffic_needs_a_matching_hash(tmp_path, monkeypatch):
+    rec = tmp_path / "profiles"
+    rec.mkdir()
+    (rec / "traffic_gemm_4096.txt").write_text(
+        "# note\nsource_hash = 0000000000000000\ndram_bytes_per_launch = 123\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda wl: "0000000000000000")
+    assert bench.recorded_traffic("gemm_4096") == 123
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda wl: "1111111111111111")
+    assert bench.recorded_traffic("gemm_4096") is None
+    assert bench.recorded_traffic("conv_htiled") is None

@@ -74,6 +74,9 @@ struct ConvTmaArgs {
     int32_t k_stages, n_planes, plane_bytes, pmax;
     int32_t tma_store;                    // rows form: the staged tile leaves by one TMA store
     int32_t raw_filter;                   // filter in TMEM read from the caller's OIHW rows (3x3)
+    int32_t contig;                       // a CTA runs a contiguous run of units (not a stride)
+    int32_t reuse;                        // FORM 2: units reuse the previous unit's last stage ...
+    int32_t reuse_period;                 // ... except every reuse_period-th (an image's first row)
     int32_t tap_plane[8], tap_shift[8], plane_phase[8];
     // Rows form over an NCHW input read in place (FORM 2): each stage's raw
     // box, 64 channel rows of xw input columns (xw / 8 odd), lands in one of
@@ -549,6 +552,33 @@ __device__ __forceinline__ RowStage row_stage(int u, int kb, const ConvTmaArgs& 
     return s;
 }
 
+// The units of a CTA.  With args.contig a contiguous run [first, end), so
+// that consecutive output rows, whose input rows overlap, stay on one CTA;
+// otherwise units blockIdx.x, + gridDim.x, ... up to args.units.
+struct UnitRange { int first, end, step; };
+
+__device__ __forceinline__ UnitRange unit_range(const ConvTmaArgs& a) {
+    if (a.contig) {
+        const int64_t u0 = static_cast<int64_t>(blockIdx.x) * a.units / gridDim.x;
+        const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * a.units / gridDim.x;
+        return UnitRange{static_cast<int>(u0), static_cast<int>(u1), 1};
+    }
+    return UnitRange{static_cast<int>(blockIdx.x), a.units, static_cast<int>(gridDim.x)};
+}
+
+// Whether unit u's first stage reads the same input row, image, channels and
+// columns as the previous unit's last stage, so that its stride-phase planes
+// are still in the ring and the stage is neither loaded nor transposed again
+// (stride 2 and a 3-row filter: output rows oh and oh+1 share input row
+// 2 oh + 1).  The host sets reuse only where the units of an image are its
+// output rows in order (one W tile, one column and output-channel block,
+// whole H tiles, one channel block, (kh-1)*dh == sh): then every unit but a
+// CTA's first and an image's first row qualifies.  Every role of the kernel
+// takes the same decision.
+__device__ __forceinline__ bool reuses_prev(int u, const UnitRange& ur, const ConvTmaArgs& a) {
+    return a.reuse && u != ur.first && u % a.reuse_period != 0;
+}
+
 // FORM 0: one pixel box per (tap, 64 channels).  FORM 1 (rows form): one
 // output row per tile and one stage per (kernel row, 64 channels), whose
 // stride phases of the input row serve every tap of that row: tap s's B
@@ -628,6 +658,7 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
     volatile int* abort = &bar->abort;
     const uint64_t limit = args.wait_limit_ns;
     const bool has_work = static_cast<int>(blockIdx.x) < args.units;
+    const UnitRange ur = unit_range(args);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -654,9 +685,11 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                 // boxes go out with the filter's first pass, the rest once
                 // the filter has left the slots after them.
                 uint32_t rs = 0, rphase = 0;
-                int issued = 0, u = blockIdx.x, kb = 0;
+                int issued = 0, u = ur.first, kb = 0;
                 const uint32_t raw_tx = static_cast<uint32_t>(args.raw_b);
                 auto issue_raw = [&]() {
+                    // A stage whose planes are reused needs no box.
+                    if (kb == 0 && reuses_prev(u, ur, args)) kb = 1;
                     if (!ptx::mbar_wait(&bar->empty[stages + rs], rphase ^ 1u, abort, limit)) {
                         raise_error(args.err, abort, kErrProducer);
                         aborted = true;
@@ -672,18 +705,18 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                                 st.ih, st.c0, st.img);
                     ++issued;
                     if (++rs == static_cast<uint32_t>(args.raw_stages)) { rs = 0; rphase ^= 1u; }
-                    if (++kb == args.k_stages) { kb = 0; u += gridDim.x; }
+                    if (++kb == args.k_stages) { kb = 0; u += ur.step; }
                 };
                 // The filter's loads go first: one TMA queue serves both, and
                 // a raw box from DRAM ahead of them would hold them up.
                 if (has_work) filter_pass(0);
-                while (!aborted && u < args.units && issued < args.raw_early) issue_raw();
+                while (!aborted && u < ur.end && issued < args.raw_early) issue_raw();
                 for (int p = 1; p < passes && has_work && !aborted; ++p) filter_pass(p);
                 if (!aborted && has_work && !ptx::mbar_wait(&bar->wcons, (passes - 1) & 1, abort, limit)) {
                     raise_error(args.err, abort, kErrProducer);
                     aborted = true;
                 }
-                while (!aborted && u < args.units) issue_raw();
+                while (!aborted && u < ur.end) issue_raw();
                 if (aborted) {
                     settle_after_abort();
                 } else {
@@ -702,7 +735,7 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
             // ---------------- TMA producer: one pixel box per K block ----------------
             uint32_t stage = 0, phase = 0;
             int issued = 0;
-            for (int u = blockIdx.x; u < args.units && !aborted; u += gridDim.x) {
+            for (int u = ur.first; u < ur.end && !aborted; u += ur.step) {
                 const ConvUnit cu = decode_conv_unit(u, args);
                 const ConvHTile ht = args.ht[cu.ht];
                 const ConvWTile wt = args.wt[cu.wt];
@@ -777,22 +810,33 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                                  !has_work || ptx::mbar_wait(&bar->wready, 0, abort, limit));
             if (!ok && lane == 0) raise_error(args.err, abort, kErrMma);
             ptx::tc_fence_after();
-            for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+            // A reused stage reads the previous stage's slot again; that
+            // slot is released only after the second use.
+            bool reuse_this = false;
+            uint32_t last_slot = 0;
+            for (int u = ur.first; ok && u < ur.end; u += ur.step) {
                 if (!__all_sync(0xffffffffu,
                                 ptx::mbar_wait(&bar->acc_empty[acc], acc_phase ^ 1u, abort, limit))) {
                     if (lane == 0) raise_error(args.err, abort, kErrMma);
                     break;
                 }
                 ptx::tc_fence_after();
+                const bool reuse_next = u + ur.step < ur.end && reuses_prev(u + ur.step, ur, args);
                 const uint32_t d = tmem + acc * static_cast<uint32_t>(args.npix);
                 for (int kb = 0; kb < args.k_stages; ++kb) {
-                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->full[stage], phase, abort, limit))) {
-                        if (lane == 0) raise_error(args.err, abort, kErrMma);
-                        ok = false;
-                        break;
+                    const bool reused = kb == 0 && reuse_this;
+                    const uint32_t slot = reused ? last_slot : stage;
+                    if (!reused) {
+                        if (!__all_sync(0xffffffffu,
+                                        ptx::mbar_wait(&bar->full[stage], phase, abort, limit))) {
+                            if (lane == 0) raise_error(args.err, abort, kErrMma);
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
                     }
-                    ptx::tc_fence_after();
-                    const uint64_t b_st = b_desc0 + ((stage * stage_bytes) >> 4);
+                    const bool keep = kb == args.k_stages - 1 && reuse_next;   // reused next
+                    const uint64_t b_st = b_desc0 + ((slot * stage_bytes) >> 4);
                     if (issuer) {
                         if constexpr (ROWS) {
                             const int r = kb / args.ch_blocks;
@@ -831,11 +875,15 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                                 ptx::mma_f16_tmem_a(d, a0 + kk * 8, b_st + kk * (32 >> 4), args.idesc,
                                                     (kb | kk) != 0);
                         }
-                        ptx::mma_commit<1>(&bar->empty[stage]);
+                        if (!keep) ptx::mma_commit<1>(&bar->empty[slot]);
                     }
                     __syncwarp();
-                    if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
+                    if (!reused) {
+                        last_slot = stage;
+                        if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
+                    }
                 }
+                reuse_this = reuse_next;
                 if (!ok) break;
                 if (issuer) ptx::mma_commit<1>(&bar->acc_full[acc]);
                 __syncwarp();
@@ -938,7 +986,7 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
         const float inv_nr = 1.0f / static_cast<float>(args.nr);
         const int ch_elems = 16 / ob;
         uint32_t acc = 0, acc_phase = 0;
-        for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+        for (int u = ur.first; ok && u < ur.end; u += ur.step) {
             const ConvUnit cu = decode_conv_unit(u, args);
             const bool okw = ptx::mbar_wait(&bar->acc_full[acc], acc_phase, abort, limit);
             // The previous tile's TMA store has read the staging tile
@@ -1140,13 +1188,16 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
         // (written by the producer beside the box) changes: with one W tile
         // every unit's boxes start at the same column.
         int cached_col0 = INT32_MIN, t0 = 0, lane_off = 0, pl0 = 15, co[4] = {0, 0, 0, 0};
-        for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-            for (int kb = 0; kb < args.k_stages; ++kb) {
+        for (int u = ur.first; ok && u < ur.end; u += ur.step) {
+            // A stage whose planes are reused is skipped here, as by the
+            // producer; the MMA warp reads the previous slot again.
+            const int kb_first = reuses_prev(u, ur, args) ? 1 : 0;
+            for (int kb = kb_first; kb < args.k_stages; ++kb) {
                 ok = __all_sync(0xffffffffu,
                                 ptx::mbar_wait(&bar->full[stages + rs], rphase, abort, limit)) &&
                      __all_sync(0xffffffffu, ptx::mbar_wait(&bar->empty[ps], pphase ^ 1u, abort, limit));
                 if (!ok) break;
-                if (kb == 0) {
+                if (kb == kb_first) {
                     const int col0 = static_cast<volatile int32_t*>(bar->raw_col0)[rs];
                     if (col0 != cached_col0) {
                         cached_col0 = col0;
@@ -1823,6 +1874,11 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         // A TMA store reads the box densely: [channel][owc pixels].
         a.tma_store = tma_store ? 1 : 0;
         a.raw_filter = raw_filter ? 1 : 0;
+        // The direct form runs each CTA on a contiguous run of output rows
+        // and, with one channel block per kernel row, lets a row's first
+        // stage reuse the planes of the previous row's last stage when they
+        // hold the same input row.
+        a.contig = use_direct ? 1 : 0;
         a.stg_pitch = tma_store ? owc * yb : wp.stg_pitch;
         a.bar_off = a.stg_off + wp.stg_bytes;
         a.w_slots = wp.w_slots;
@@ -1934,6 +1990,15 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
                     a.wt[i].unused = 0;
                 }
                 a.n_wtiles = wcount;
+                // Stage reuse (direct form, see reuses_prev): the launch's
+                // units of an image are its output rows in order.
+                bool full_htiles = true;
+                for (int i = 0; i < hcount; ++i) full_htiles = full_htiles && a.ht[i].rows == a.rblocks;
+                a.reuse = use_direct && nr == 1 && g.ch_blocks == 1 &&
+                                  (d->kh - 1) * d->dh == d->sh && wcount == 1 && a.cblocks == 1 &&
+                                  a.co_blocks == 1 && full_htiles
+                              ? 1 : 0;
+                a.reuse_period = hcount * a.rblocks;
                 const int64_t units = static_cast<int64_t>(n_imgs) * hcount * a.rblocks * wcount *
                                       a.cblocks * a.co_blocks;
                 if (units > INT32_MAX) return fail(TILES_ERR_TOO_LARGE, "too many tiles");

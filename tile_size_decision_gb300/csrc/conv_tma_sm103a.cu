@@ -1468,6 +1468,7 @@ bool conv_tma_geometry(const tiles_conv_desc* d, int64_t oh, int64_t ow, int til
 // Geometry and shared-memory layout of the weights-in-TMEM kernel.
 struct WtPlan {
     int owc = 0, nr = 0, acc_bufs = 0, stages = 0;
+    int raw_stages = 0;              // direct rows form: raw box slots (beside `stages` plane slots)
     int stg_pitch = 0, stg_bytes = 0, w_slots = 0, smem = 0;
 };
 
@@ -1539,10 +1540,12 @@ struct RowsPlan {
     int tap_plane[8] = {}, tap_shift[8] = {}, plane_phase[8] = {};
 };
 
-// direct: the form over an NCHW input read in place, whose stages also hold
-// a raw box of 64 channel rows x xw columns (xw / 8 odd, at most 256, at
-// least the span pmax * sw plus the 7 columns of its 8-column group); at
-// most 4 plane and 4 raw stages.
+// direct: the form over an NCHW input read in place, with a ring of raw
+// boxes of 64 channel rows x xw columns (xw / 8 odd, at most 256, at least
+// the span pmax * sw plus the 7 columns of its 8-column group) beside the
+// plane ring: 2 plane stages and as many raw boxes as fit, up to 6.  The raw
+// boxes come from DRAM, so their ring is the one whose depth hides latency;
+// the plane ring only hands transposed stages to the MMA warp.
 bool rows_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, int tile_ow,
                int64_t k_blocks, int sms, int forced_acc, bool direct, RowsPlan* out) {
     if (d->c_out > 128 || d->kw > 8) return false;
@@ -1582,11 +1585,19 @@ bool rows_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, in
         // Direct form: a plane may start up to 7 rows into its space.
         const int plane_bytes = ((pmax + (direct ? 7 : 0)) * 128 + 1023) / 1024 * 1024;
         const int raw_b = 128 * xw;
-        const int stage = rp.n_planes * plane_bytes + raw_b;
+        const int planes = rp.n_planes * plane_bytes;
         const int pitch = owc * ob + 16;
         const int stg = 128 * pitch;
-        const int stages = std::min(direct ? kMaxStages / 2 : kMaxStages, (budget - stg) / stage);
-        if (stages < 2) continue;
+        int stages = 0, raw_stages = 0;
+        if (direct) {
+            stages = 2;
+            raw_stages = std::min(kMaxStages - stages, (budget - stg - stages * planes) / raw_b);
+            if (raw_stages < 2) continue;
+        } else {
+            stages = std::min(kMaxStages, (budget - stg) / planes);
+            if (stages < 2) continue;
+        }
+        const int ring_bytes = raw_stages * raw_b + stages * planes;
         const int64_t units = static_cast<int64_t>(d->n) * n_ht * rows * n_wt *
                               ((wcols + owc - 1) / owc);
         const int64_t per_unit = stages_k * (std::max<int64_t>(d->kw * 4 * (owc / 2),
@@ -1599,12 +1610,13 @@ bool rows_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, in
             rp.wp.nr = 1;
             rp.wp.acc_bufs = acc;
             rp.wp.stages = stages;
+            rp.wp.raw_stages = raw_stages;
             rp.wp.stg_pitch = pitch;
             rp.wp.stg_bytes = stg;
             // The filter's start-up passes use everything from raw slot 1
             // on (the direct form's first raw box loads beside them).
-            rp.wp.w_slots = (stages * stage + stg - (direct ? raw_b : 0)) / kWtWeightBlockBytes;
-            rp.wp.smem = std::max(stages * stage + stg + kSmemBarrierBytes + kSmemAlignSlack,
+            rp.wp.w_slots = (ring_bytes + stg - (direct ? raw_b : 0)) / kWtWeightBlockBytes;
+            rp.wp.smem = std::max(ring_bytes + stg + kSmemBarrierBytes + kSmemAlignSlack,
                                   116 * 1024);
             rp.pmax = pmax;
             rp.plane_bytes = plane_bytes;
@@ -1848,9 +1860,9 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         a.idesc = ptx::idesc_f16_f32acc(d->in_dtype == TILES_BF16, false, 128, a.npix);
         a.stages = wp.stages;
         // FORM 2: [raw ring][plane ring][staging]; else [ring][staging].
-        a.raw_stages = use_direct ? wp.stages : 0;
+        a.raw_stages = use_direct ? wp.raw_stages : 0;
         a.raw_off = 0;
-        a.ring_off = use_direct ? wp.stages * a.raw_b : 0;
+        a.ring_off = use_direct ? wp.raw_stages * a.raw_b : 0;
         a.raw_early = use_direct ? 1 : 0;
         a.w_off = a.raw_early * a.raw_b;
         // Direct form: each plane starts some rows into its space so that

@@ -13,8 +13,11 @@ Rules
        16; the kernels' layout adds bk * in_bytes == 128 (one swizzle atom),
        (bn / cta_group) a multiple of 64, 192 threads, 1-2 accumulators,
        1-8 stages.  One violation count per failed condition.
-  C1   stages * ((bm/cg)*bk + bk*(bn/cg)) * in_bytes + 256 (barriers)
-       + 1024 (alignment slack) <= smem_per_block_max.
+  C1   stages * ((bm/cg)*bk + bk*(bn/cg)) * in_bytes + 16384 (the
+       epilogue's staging: four 32-row x 128-byte boxes, from which TMA
+       stores write C) + 256 (barriers) + 1024 (alignment slack)
+       <= smem_per_block_max.  The page's C1 counts the A/B tiles alone and
+       names the epilogue, barriers and padding it leaves out.
   C2   TMEM: acc_bufs * bn fp32 columns, allocated as a power of two >= 32,
        <= tmem_cols.
   occupancy  least of regs (kernel_regs_per_thread * threads), smem,
@@ -47,10 +50,11 @@ from dataclasses import dataclass, field
 from . import planner as page
 
 # Compiled variants (bm, bn, cta_group, stages), in enumeration order.
-VARIANTS = ((128, 64, 1, 8), (128, 128, 1, 7), (128, 192, 1, 5), (128, 256, 1, 4),
-            (256, 128, 2, 8), (256, 256, 2, 7))
+VARIANTS = ((128, 64, 1, 8), (128, 128, 1, 6), (128, 192, 1, 5), (128, 256, 1, 4),
+            (256, 128, 2, 8), (256, 256, 2, 6))
 
 THREADS = 192
+EPILOGUE_BYTES = 4 * 32 * 128
 BARRIER_BYTES = 256
 ALIGN_SLACK = 1024
 MAX_STAGES = 8
@@ -67,7 +71,7 @@ class GB300Device:
     tmem_cols: int = 512
     mma_flops_per_clk: int = 8192
     fill_bytes_per_clk: int = 64
-    kernel_regs_per_thread: int = 112
+    kernel_regs_per_thread: int = 152
     cta_pairs: int = 0          # co-resident 2-CTA clusters; 0 = sm_count // 2
 
 
@@ -132,7 +136,7 @@ def evaluate(cfg: GB300Config, dev: GB300Device, in_bytes: int = 2) -> GB300Verd
     if v.c3_violations:
         v.failures.append(page.C3)
     v.smem_per_stage = ((cfg.bm // cgs) * cfg.bk + cfg.bk * (cfg.bn // cgs)) * in_bytes
-    v.smem_total = v.smem_per_stage * cfg.stages + BARRIER_BYTES + ALIGN_SLACK
+    v.smem_total = v.smem_per_stage * cfg.stages + EPILOGUE_BYTES + BARRIER_BYTES + ALIGN_SLACK
     if v.smem_total > dev.smem_per_block_max:
         v.failures.append(page.C1)
     v.tmem_cols_alloc = _tmem_alloc(max(cfg.acc_bufs * cfg.bn, 1))

@@ -8,7 +8,7 @@ from tile_size_decision_gb300 import _abi
 
 HEADER = "tiles-tuned 1\n"
 # sm_count batch m n k in out | bm bn bk stages threads instr acc_bufs cta_group tail | us
-LINE_A = "152 1 4096 4096 4096 {f16} {f16} 256 256 64 7 192 3 2 2 3 85.600\n"
+LINE_A = "152 1 4096 4096 4096 {f16} {f16} 256 256 64 6 192 3 2 2 3 85.600\n"
 LINE_B = "148 16 2048 2048 1024 {bf16} {bf16} 128 256 64 4 192 3 2 1 1 101.250\n"
 
 
@@ -29,7 +29,7 @@ def test_load_then_lookup(tmp_path):
     p.write_text(HEADER + fmt(LINE_A) + "\n" + fmt(LINE_B))
     T.tuned_load(str(p))
     a = T.tuned_lookup(152, 1, 4096, 4096, 4096, S.F16, S.F16)
-    assert (a.bm, a.bn, a.bk, a.stages, a.cta_group, a.tail) == (256, 256, 64, 7, 2, 3)
+    assert (a.bm, a.bn, a.bk, a.stages, a.cta_group, a.tail) == (256, 256, 64, 6, 2, 3)
     b = T.tuned_lookup(148, 16, 2048, 2048, 1024, S.BF16, S.BF16)
     assert (b.bm, b.bn, b.stages, b.cta_group, b.tail) == (128, 256, 4, 1, 1)
     # Another SM count is another problem.

@@ -91,7 +91,7 @@ def test_sweep_matches_the_oracle(m, n, k, instr, sm, smem):
 def test_gb300_mode_ranks_the_pair_tile_first():
     res = run_json("--mode", "gb300", "--sm-count", "148")
     best = res["ranked"][0]
-    assert (best["bm"], best["bn"], best["stages"], best["cta_group"]) == (256, 256, 7, 2)
+    assert (best["bm"], best["bn"], best["stages"], best["cta_group"]) == (256, 256, 6, 2)
     assert best["grid"] == 256 and best["waves"] == 4 and best["tail_split"] == -1
     assert res["device"]["tmem_cols"] == 512
 

@@ -23,7 +23,7 @@ import tile_size_decision_gb300 as T  # noqa: E402
 from tests.gpu_util import to_cuda, to_f64, empty_out  # noqa: E402
 
 # Compiled variants: (bn, cta_group) -> stages.
-VARIANTS = {(64, 1): 8, (128, 1): 7, (192, 1): 5, (256, 1): 4, (128, 2): 8, (256, 2): 7}
+VARIANTS = {(64, 1): 8, (128, 1): 6, (192, 1): 5, (256, 1): 4, (128, 2): 8, (256, 2): 6}
 VARIANT_IDS = [f"bn{bn}_cg{cg}" for bn, cg in VARIANTS]
 
 
@@ -309,7 +309,7 @@ def test_forced_tail_schedules(tail):
     b_np = S.random_matrix(62, (k, n), S.BF16, "normal")
     a, b = to_cuda(a_np, S.BF16), to_cuda(b_np, S.BF16)
     c = empty_out((m, n), S.BF16)
-    cfg = T.make_config(256, 256, 64, 7, 192, "tcgen05", 2, 2, tail=tail)
+    cfg = T.make_config(256, 256, 64, 6, 192, "tcgen05", 2, 2, tail=tail)
     w = T.gemm_workspace(a, b, c, cfg)
     sch = T.gemm_schedule(a, b, c, cfg, w)
     assert sch.tail_mode == {"whole": 0, "nhalf": 1, "ksplit": 2}[tail]

@@ -80,7 +80,7 @@ def test_gemm_host_equals_the_device_call_piece_by_piece():
     c_h = torch.empty((m, n), dtype=torch.float32).pin_memory()
     a_d, b_d = a_h.cuda(), b_h.cuda()
     c_d = torch.empty((m, n), dtype=torch.float32, device="cuda")
-    cfg = T.make_config(256, 256, 64, 7, 192, "tcgen05", 2, 2, tail="whole")
+    cfg = T.make_config(256, 256, 64, 6, 192, "tcgen05", 2, 2, tail="whole")
     ws = T.workspace()
     T.gemm_host(a_h, b_h, c_h, torch.empty_like(a_d), torch.empty_like(b_d), c_d, cfg=cfg,
                 workspace=ws, chunks=4)

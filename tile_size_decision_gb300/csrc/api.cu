@@ -55,6 +55,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// The tensor map through which the GEMM epilogue's TMA stores write C: a
+// row-major [batch][m][n] array of the output type with row pitch `ldc` and
+// item pitch `sc` (elements), box {128 bytes of columns, 32 rows, 1}, the
+// 128-byte swizzle of the staging boxes.  False when C cannot take TMA
+// stores (base or pitches not 16-byte multiples, or the encoder refuses);
+// the epilogue then writes C from registers.
+bool encode_c_store(CUtensorMap* map, int dtype, void* base, uint64_t n, uint64_t m,
+                    uint64_t batch, uint64_t ldc, uint64_t sc) {
+    auto fn = encode_fn();
+    const uint64_t eb = dtype == TILES_F32 ? 4 : 2;
+    if (!fn || !aligned16(base) || (ldc * eb) % 16 != 0 || (sc * eb) % 16 != 0) return false;
+    const CUtensorMapDataType t = dtype == TILES_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : dtype == TILES_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {n, m, batch};
+    cuuint64_t strides[2] = {ldc * eb, sc * eb};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, t, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A 3-D tensor map over a row-major [d2][d1][d0] array of 16-bit elements
 // with row pitch `pitch1` and item pitch `pitch2` (elements), box
 // {box0, box1, 1}, 128-byte swizzle, zero fill out of range.
@@ -161,19 +184,19 @@ int max_groups(int ordinal, int bn, int cg, int sm_count) {
 }
 
 int launch_variant(int bn, int cg, const CUtensorMap& ta, const CUtensorMap& tb,
-                   const GemmArgs& args, int groups, cudaStream_t st) {
+                   const CUtensorMap& tc, const GemmArgs& args, int groups, cudaStream_t st) {
     if (cg == 1) {
         switch (bn) {
-            case 64: return launch_gemm_variant<64, 1>(ta, tb, args, groups, st);
-            case 128: return launch_gemm_variant<128, 1>(ta, tb, args, groups, st);
-            case 192: return launch_gemm_variant<192, 1>(ta, tb, args, groups, st);
-            case 256: return launch_gemm_variant<256, 1>(ta, tb, args, groups, st);
+            case 64: return launch_gemm_variant<64, 1>(ta, tb, tc, args, groups, st);
+            case 128: return launch_gemm_variant<128, 1>(ta, tb, tc, args, groups, st);
+            case 192: return launch_gemm_variant<192, 1>(ta, tb, tc, args, groups, st);
+            case 256: return launch_gemm_variant<256, 1>(ta, tb, tc, args, groups, st);
             default: break;
         }
     } else if (cg == 2) {
         switch (bn) {
-            case 128: return launch_gemm_variant<128, 2>(ta, tb, args, groups, st);
-            case 256: return launch_gemm_variant<256, 2>(ta, tb, args, groups, st);
+            case 128: return launch_gemm_variant<128, 2>(ta, tb, tc, args, groups, st);
+            case 256: return launch_gemm_variant<256, 2>(ta, tb, tc, args, groups, st);
             default: break;
         }
     }
@@ -351,6 +374,9 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
     if (s != TILES_OK) return s;
     s = encode_3d(&tb, d->b_dtype, d->b, d->n, d->k, batch, d->ldb, sb, 64, 64);
     if (s != TILES_OK) return s;
+    CUtensorMap tc{};
+    const int64_t sc = batch > 1 ? d->stride_c : d->m * d->ldc;
+    const bool tma_c = encode_c_store(&tc, d->c_dtype, d->c, d->n, d->m, batch, d->ldc, sc);
 
     GemmArgs args{};
     args.m = (int32_t)d->m; args.n = (int32_t)d->n; args.k = (int32_t)d->k;
@@ -375,11 +401,12 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
     args.ldc = d->ldc;
     args.stride_c = batch > 1 ? d->stride_c : 0;
     args.c_dtype = d->c_dtype;
+    args.tma_store = tma_c ? 1 : 0;
     args.idesc = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, cfg.bm, cfg.bn);
     args.idesc_half = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, cfg.bm, cfg.bn / 2);
     args.err = (ws && ws_bytes >= sizeof(int32_t)) ? static_cast<int32_t*>(ws) : nullptr;
     args.wait_limit_ns = kDefaultWaitLimitNs;
-    int e = launch_variant(cfg.bn, cfg.cta_group, ta, tb, args, (int)gp.groups,
+    int e = launch_variant(cfg.bn, cfg.cta_group, ta, tb, tc, args, (int)gp.groups,
                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(TILES_ERR_CUDA, "GEMM launch failed: %s",

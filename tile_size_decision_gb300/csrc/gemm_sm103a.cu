@@ -62,13 +62,14 @@ int gemm_variant_max_groups<BN, CG>(int sm_count) {
 
 template <>
 int launch_gemm_variant<BN, CG>(const CUtensorMap& ta, const CUtensorMap& tb,
-                                const GemmArgs& args, int groups, cudaStream_t stream) {
+                                const CUtensorMap& tc, const GemmArgs& args, int groups,
+                                cudaStream_t stream) {
     cudaError_t e = set_smem_attribute();
     if (e != cudaSuccess) return static_cast<int>(e);
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     fill_launch(&cfg, attr, groups, stream);
-    e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<BN, STAGES, CG>, ta, tb, args);
+    e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<BN, STAGES, CG>, ta, tb, tc, args);
     if (e != cudaSuccess) return static_cast<int>(e);
     return static_cast<int>(cudaGetLastError());
 }

@@ -26,8 +26,15 @@
 //   warp-uniform, and one lane chosen by elect.sync issues the TMA, MMA and
 //   commit instructions.  (The same loops run by a single lane made the
 //   4096^3 GEMM 2.4% slower with a CTA pair and 6% slower with one CTA.)
-//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, cast, store the
-//               rows they own (warp w reads TMEM lanes 32*(w%4)..+31).
+//   warps 2-5   epilogue: warp w owns TMEM lanes 32*(w%4)..+31, i.e. 32
+//               rows of the tile.  It reads them with tcgen05.ld, casts to
+//               the output type and writes each 128-byte-wide column box
+//               (32 fp32 or 64 16-bit columns) into its own swizzled 4 KB
+//               staging box in shared memory, which one TMA store copies
+//               to C, clipped at M and N.  Each lane's 16-byte writes land
+//               in distinct banks, and the store leaves the L1 path free;
+//               a C whose rows are not 16-byte multiples is written from
+//               the registers instead.
 //
 // Work is scheduled persistently: CTA group g takes units g, g+groups, ...
 // The units are the output tiles, except that when the last round would
@@ -74,6 +81,7 @@ struct GemmArgs {
     void* c;
     int64_t ldc, stride_c;     // elements
     int32_t c_dtype;           // tiles_dtype
+    int32_t tma_store;         // 1: C leaves through TMA stores of staged boxes
     uint32_t idesc;            // tcgen05 instruction descriptor, N = BN
     uint32_t idesc_half;       // the same with N = BN / 2
     int32_t* err;              // workspace error word, may be null
@@ -103,7 +111,11 @@ struct GemmLayout {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;          // per CTA
     static constexpr int TX_BYTES = STAGE_BYTES * CG;              // on the leader's barrier
     static constexpr int OPERAND_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int SMEM_BYTES = OPERAND_BYTES + kSmemBarrierBytes + kSmemAlignSlack;
+    // One staging box per epilogue warp: 32 rows x 128 bytes.
+    static constexpr int EPI_BOX_BYTES = 32 * 128;
+    static constexpr int STAGING_BYTES = 4 * EPI_BOX_BYTES;
+    static constexpr int SMEM_BYTES =
+        OPERAND_BYTES + STAGING_BYTES + kSmemBarrierBytes + kSmemAlignSlack;
     static constexpr int ACC_COLS = 2 * BN;
     static constexpr int TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64
                                    : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
@@ -114,6 +126,8 @@ struct GemmLayout {
     // The last K part of a split tile stages one partial per epilogue warp
     // (32 rows x BN fp32) in the idle operand stages.
     static_assert(4 * 32 * BN * 4 <= OPERAND_BYTES, "partial staging must fit the stages");
+    static_assert(STAGING_BYTES == kSmemEpilogueBytes, "the planner counts this staging");
+    static_assert(OPERAND_BYTES % 1024 == 0, "staging boxes sit on the 128-byte swizzle's 1 KB atoms");
 };
 
 struct TileCoord { int b, mi, ni; };
@@ -262,10 +276,34 @@ __device__ __forceinline__ void store_row_chunk(void* row, int64_t col0, int64_t
     }
 }
 
+// Two fp32 accumulators as one packed pair of the 16-bit output type.
+__device__ __forceinline__ uint32_t pack_f16x2(uint32_t lo, uint32_t hi) {
+    __half2 t = __floats2half2_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+
+// Write one 128-byte row (w[0..31]) of a 32-row staging box in the 128-byte
+// swizzled layout a SWIZZLE_128B tensor map reads: 16-byte piece q of row r
+// sits at piece position q ^ (r % 8).  With one row per lane, the eight
+// lanes of each quarter-warp store phase hit eight different bank groups.
+__device__ __forceinline__ void stage_box_row(uint32_t box, int row, const uint32_t (&w)[32]) {
+    const uint32_t r = box + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        ptx::st_shared_v4(r + (static_cast<uint32_t>(q ^ (row & 7)) << 4), w[4 * q], w[4 * q + 1],
+                          w[4 * q + 2], w[4 * q + 3]);
+}
+
 template <int BN, int STAGES, int CG>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     using L = GemmLayout<BN, STAGES, CG>;
     extern __shared__ uint8_t smem_raw[];
     // Operand tiles start on a 1024-byte boundary: the 128-byte swizzle is a
@@ -276,7 +314,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* smA = base;
     uint8_t* smB = base + STAGES * L::A_BYTES;
-    PipeBarriers* bar = reinterpret_cast<PipeBarriers*>(base + L::OPERAND_BYTES);
+    uint8_t* staging = base + L::OPERAND_BYTES;
+    PipeBarriers* bar = reinterpret_cast<PipeBarriers*>(staging + L::STAGING_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -301,6 +340,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tmA);
         ptx::tma_prefetch_desc(&tmB);
+        if (args.tma_store) ptx::tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         ptx::tmem_alloc<CG>(&bar->tmem_base, L::TMEM_COLS);
@@ -433,6 +473,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int quarter = warp & 3;               // TMEM lanes this warp may read
         const int row_in_tile = quarter * 32 + lane;
         const int out_bytes = args.c_dtype == TILES_F32 ? 4 : 2;
+        uint8_t* box_ptr = staging + quarter * L::EPI_BOX_BYTES;
+        const uint32_t box = ptx::smem_addr(box_ptr);
         uint32_t acc = 0, acc_phase = 0;
         for (int u = group; u < args.units; u += groups) {
             const UnitCoord uc = decode_unit<BN>(u, args);
@@ -523,8 +565,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     __syncwarp();
                 }
             } else {
+                int c = 0;                                  // next 32-column TMEM chunk
+                if (args.tma_store) {
+                    // Whole 128-byte boxes: 32 fp32 or 64 16-bit columns.
+                    const int per_box = out_bytes == 4 ? 1 : 2;
+                    const int boxes = uc.width / (32 * per_box);
+                    const int box_row0 = uc.mi * L::BM + static_cast<int>(rank) * 128 + quarter * 32;
 #pragma unroll 1
-                for (int c = 0; c < uc.width / 32; ++c) {
+                    for (int j = 0; j < boxes; ++j, c += per_box) {
+                        uint32_t w[32];
+                        if (per_box == 1) {
+                            ptx::tmem_ld_32cols(tacc + c * 32, w);
+                            ptx::tmem_ld_wait();
+                        } else {
+                            uint32_t v0[32], v1[32];
+                            ptx::tmem_ld_32cols(tacc + c * 32, v0);
+                            ptx::tmem_ld_32cols(tacc + c * 32 + 32, v1);
+                            ptx::tmem_ld_wait();
+                            if (args.c_dtype == TILES_F16) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    w[i] = pack_f16x2(v0[2 * i], v0[2 * i + 1]);
+                                    w[16 + i] = pack_f16x2(v1[2 * i], v1[2 * i + 1]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+                                    w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+                                }
+                            }
+                        }
+                        // The previous box's store has finished reading the
+                        // staging box (lane 0 issued it and tracks its group).
+                        if (lane == 0) ptx::bulk_wait_read_all();
+                        __syncwarp();
+                        stage_box_row(box, lane, w);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        const int x = uc.n0 + c * 32;
+                        if (lane == 0 && x < args.n && box_row0 < args.m) {
+                            ptx::tma_store_3d(&tmC, box_ptr, x, box_row0, uc.b);
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                }
+#pragma unroll 1
+                for (; c < uc.width / 32; ++c) {
                     uint32_t v[32];
                     ptx::tmem_ld_32cols(tacc + c * 32, v);
                     ptx::tmem_ld_wait();
@@ -544,6 +631,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
+        // C is written, and the staging boxes are free, once the stores end.
+        if (lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -559,8 +649,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // gemm_sm103a.cu).  `groups` is the number of persistent CTA groups.
 // Returns a cudaError_t value.
 template <int BN, int CG>
-int launch_gemm_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                        int groups, cudaStream_t stream);
+int launch_gemm_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                        const GemmArgs& args, int groups, cudaStream_t stream);
 
 // Persistent CTA groups that fit on the device at once for a variant.
 template <int BN, int CG>
@@ -569,11 +659,11 @@ int gemm_variant_max_groups(int sm_count);
 // Stages compiled for each (BN, CG) (the planner's kGemmVariants agree).
 template <int BN, int CG> struct GemmStages;
 template <> struct GemmStages<64, 1>  { static constexpr int value = 8; };
-template <> struct GemmStages<128, 1> { static constexpr int value = 7; };
+template <> struct GemmStages<128, 1> { static constexpr int value = 6; };
 template <> struct GemmStages<192, 1> { static constexpr int value = 5; };
 template <> struct GemmStages<256, 1> { static constexpr int value = 4; };
 template <> struct GemmStages<128, 2> { static constexpr int value = 8; };
-template <> struct GemmStages<256, 2> { static constexpr int value = 7; };
+template <> struct GemmStages<256, 2> { static constexpr int value = 6; };
 
 __global__ void selftest_wait_kernel(int32_t* err, uint64_t limit_ns);
 

@@ -93,10 +93,11 @@ void evaluate_page(const tiles_device& dev, const tiles_config& cfg, int elem_by
 
 // GB300 kernel variants compiled into this library (bm, bn, cta_group,
 // stages), in enumeration order.  bk is one 128-byte swizzle atom of the
-// input type; the stage count is the deepest pipeline that fits 227 KB.
+// input type; the stage count is the deepest pipeline that fits 227 KB next
+// to the epilogue's staging boxes.
 const KernelVariant kGemmVariants[] = {
-    {128, 64, 1, 8}, {128, 128, 1, 7}, {128, 192, 1, 5}, {128, 256, 1, 4},
-    {256, 128, 2, 8}, {256, 256, 2, 7},
+    {128, 64, 1, 8}, {128, 128, 1, 6}, {128, 192, 1, 5}, {128, 256, 1, 4},
+    {256, 128, 2, 8}, {256, 256, 2, 6},
 };
 const int kNumGemmVariants = sizeof(kGemmVariants) / sizeof(kGemmVariants[0]);
 
@@ -104,7 +105,7 @@ int64_t gb300_smem_bytes(const tiles_config& cfg, int in_bytes, int64_t* per_sta
     const int cg = std::max(cfg.cta_group, 1);
     int64_t stage = ((int64_t)(cfg.bm / cg) * cfg.bk + (int64_t)cfg.bk * (cfg.bn / cg)) * in_bytes;
     if (per_stage) *per_stage = stage;
-    return stage * cfg.stages + kSmemBarrierBytes + kSmemAlignSlack;
+    return stage * cfg.stages + kSmemEpilogueBytes + kSmemBarrierBytes + kSmemAlignSlack;
 }
 
 static int pow2_at_least(int x) {
@@ -133,8 +134,9 @@ void evaluate_gb300(const tiles_device& dev, const tiles_config& cfg, int in_byt
     if (cfg.stages < 1 || cfg.stages > kMaxStages) ++c3;
     v->c3_violations = c3;
     if (c3) v->failures |= TILES_FAIL_C3;
-    // C1: pipeline stages plus barriers and the 1 KB alignment slack of the
-    // swizzled operand tiles, within the opt-in per-block limit.
+    // C1: pipeline stages plus the epilogue's staging boxes, the barriers
+    // and the 1 KB alignment slack of the swizzled operand tiles, within the
+    // opt-in per-block limit.
     tiles_config c = cfg;
     c.cta_group = cgs;
     v->smem_total = gb300_smem_bytes(c, in_bytes, &v->smem_per_stage);

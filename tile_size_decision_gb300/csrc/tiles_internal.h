@@ -12,14 +12,17 @@ namespace tiles {
 // MMA issuer and TMEM owner, warps 2-5 epilogue.
 constexpr int kGemmThreads = 192;
 // Registers per thread of the GEMM kernels as built (ptxas reports up to
-// 110, which the per-warp granule of 256 rounds to 112); the planner's
-// occupancy uses this figure.
-constexpr int kGemmRegsPerThread = 112;
+// 152, a multiple of the per-warp granule of 256); the planner's occupancy
+// uses this figure.
+constexpr int kGemmRegsPerThread = 152;
 // Shared memory beyond the operand stages: mbarriers, the TMEM address slot,
 // an abort flag (kSmemBarrierBytes) and the slack that lets the operand
 // tiles start on a 1024-byte boundary, as the 128-byte swizzle requires.
 constexpr int kSmemBarrierBytes = 256;
 constexpr int kSmemAlignSlack = 1024;
+// The epilogue's staging boxes: one 32-row x 128-byte box per epilogue warp,
+// from which TMA stores copy the output tile to C.
+constexpr int kSmemEpilogueBytes = 4 * 32 * 128;
 constexpr int kMaxStages = 8;
 // Default L2 -> shared-memory fill rate per SM per clock used by the GB300
 // time model (bytes).  A model parameter calibrated on the 128x256 one-CTA

@@ -453,16 +453,17 @@ def run_ours(args, rank, world, local_rank):
     job_ws = getattr(job, "ws", ws)
     if getattr(job, "autotune", None) and args.autotune > 0:
         job.config["autotune"] = job.autotune(args.autotune)
-    for _ in range(args.warmup):
-        flush.zero_()
-        job.step(ws, stream)
-    tiles.check(job_ws, stream)
-
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
+    # The warm-up steps run right before the timed ones, after the sampler's
+    # start-up pause, so that the timed steps start from a busy GPU.
+    for _ in range(args.warmup):
+        flush.zero_()
+        job.step(ws, stream)
+    tiles.check(job_ws, stream)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()

@@ -20,7 +20,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import tile_size_decision_gb300 as T  # noqa: E402
-from tests.gpu_util import to_cuda, to_f64, empty_out  # noqa: E402
+from tests.gpu_util import TORCH_DT, to_cuda, to_f64, empty_out  # noqa: E402
 
 # Compiled variants: (bn, cta_group) -> stages.
 VARIANTS = {(64, 1): 8, (128, 1): 6, (192, 1): 5, (256, 1): 4, (128, 2): 8, (256, 2): 6}
@@ -130,6 +130,51 @@ def test_ragged_every_variant_with_canaries(ws, v):
     host = to_f64(big)
     assert np.all(host[m:, :] == 12345.0) and np.all(host[:, n:] == 12345.0)
     assert_close(host[:m, :n], S.widen(a, S.F16), S.widen(b, S.F16), S.F32)
+
+
+@pytest.mark.parametrize("v", list(VARIANTS), ids=VARIANT_IDS)
+@pytest.mark.parametrize("out_dt", [S.F16, S.BF16])
+def test_ragged_16bit_output_stays_inside_m_and_n(ws, v, out_dt):
+    # 16-bit C leaves through 64-column TMA store boxes of 32 rows; the
+    # tensor map over C clips them at M and N, so the canary band past N
+    # (inside the row pitch) and the rows past M stay untouched.
+    bn, cg = v
+    m, n, k = 333 * cg, 2 * bn + 40, 200
+    in_dt = S.BF16 if out_dt == S.BF16 else S.F16
+    a = S.random_matrix(33, (m, k), in_dt, "normal")
+    b = S.random_matrix(34, (k, n), in_dt, "normal")
+    canary = 1536.0                      # exact in fp16 and bf16
+    big = torch.full((m + 3, n + 24), canary, dtype=TORCH_DT[out_dt], device="cuda")
+    c = big[:m, :n]
+    T.gemm(to_cuda(a, in_dt, -(-k // 8) * 8), to_cuda(b, in_dt, -(-n // 8) * 8), out=c,
+           cfg=variant(v), workspace=ws)
+    T.check(ws)
+    host = to_f64(big)
+    assert np.all(host[m:, :] == canary) and np.all(host[:, n:] == canary)
+    assert_close(host[:m, :n], S.widen(a, in_dt), S.widen(b, in_dt), out_dt)
+
+
+@pytest.mark.parametrize("v", [(128, 1), (256, 2), (192, 1)], ids=["bn128_cg1", "bn256_cg2",
+                                                                   "bn192_cg1"])
+@pytest.mark.parametrize("out_dt", [S.F32, S.F16, S.BF16])
+def test_batched_output_gaps_stay_untouched(ws, v, out_dt):
+    # C's items sit in a larger buffer: each item's rows past M and columns
+    # past N, and the rows between items, belong to nobody.  The 3-D tensor
+    # map over C (item pitch = the buffer's) must keep every store inside
+    # its own item's M x N.
+    bn, cg = v
+    bsz, m, n, k = 3, 130 * cg + 7, bn + 72, 128
+    in_dt = S.BF16 if out_dt == S.BF16 else S.F16
+    a = S.random_matrix(43, (bsz, m, k), in_dt, "normal")
+    b = S.random_matrix(44, (bsz, k, n), in_dt, "normal")
+    canary = 1536.0
+    big = torch.full((bsz, m + 9, n + 40), canary, dtype=TORCH_DT[out_dt], device="cuda")
+    c = big[:, :m, :n]
+    T.gemm_batched(to_cuda(a, in_dt), to_cuda(b, in_dt), out=c, cfg=variant(v), workspace=ws)
+    T.check(ws)
+    host = to_f64(big)
+    assert np.all(host[:, m:, :] == canary) and np.all(host[:, :, n:] == canary)
+    assert_close(host[:, :m, :n], S.widen(a, in_dt), S.widen(b, in_dt), out_dt)
 
 
 @pytest.mark.parametrize("v", [None] + list(VARIANTS), ids=["planned"] + VARIANT_IDS)

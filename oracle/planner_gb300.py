@@ -71,7 +71,7 @@ class GB300Device:
     tmem_cols: int = 512
     mma_flops_per_clk: int = 8192
     fill_bytes_per_clk: int = 64
-    kernel_regs_per_thread: int = 152
+    kernel_regs_per_thread: int = 168
     cta_pairs: int = 0          # co-resident 2-CTA clusters; 0 = sm_count // 2
 
 

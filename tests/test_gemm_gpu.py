@@ -306,6 +306,35 @@ def test_tail_rounds_split(ws, v, rest, tail):
         assert_close(to_f64(c), S.widen(a_np, S.F16), S.widen(b_np, S.F16), S.F32)
 
 
+@pytest.mark.parametrize("v", [(256, 2), (256, 1), (128, 1)], ids=["bn256_cg2", "bn256_cg1",
+                                                                   "bn128_cg1"])
+@pytest.mark.parametrize("out_dt", [S.F16, S.BF16])
+def test_ksplit_tail_16bit_output(ws, v, out_dt):
+    # The last K part adds the partials and casts: a 16-bit C leaves in
+    # 64-column boxes, two TMEM chunks each.  N and M are ragged, and the
+    # canary band past N inside the row pitch stays untouched.
+    bn, cg = v
+    g = _groups(cg)
+    m, n, k = 128 * cg * (g + 1) - 37, bn - 40, 1000
+    in_dt = S.BF16 if out_dt == S.BF16 else S.F16
+    a_np = S.random_matrix(53, (m, k), in_dt, "normal")
+    b_np = S.random_matrix(54, (k, n), in_dt, "normal")
+    a = to_cuda(a_np, in_dt, -(-k // 8) * 8)
+    b = to_cuda(b_np, in_dt, -(-n // 8) * 8)
+    canary = 1536.0
+    big = torch.full((m, n + 16), canary, dtype=TORCH_DT[out_dt], device="cuda")
+    c = big[:, :n]
+    cfg = T.make_config(128 * cg, bn, 64, VARIANTS[v], 192, "tcgen05", 2, cg, tail="ksplit")
+    w = T.gemm_workspace(a, b, c, cfg)
+    sch = T.gemm_schedule(a, b, c, cfg, w)
+    assert sch.tail_mode == 2 and sch.ksplit >= 2
+    T.gemm(a, b, out=c, cfg=cfg, workspace=w)
+    T.check(w)
+    host = to_f64(big)
+    assert np.all(host[:, n:] == canary)
+    assert_close(host[:, :n], S.widen(a_np, in_dt), S.widen(b_np, in_dt), out_dt)
+
+
 def test_ksplit_tail_is_deterministic(ws):
     wl = S.WORKLOADS["gemm_ragged"]
     a, b = S.gemm_inputs(wl)

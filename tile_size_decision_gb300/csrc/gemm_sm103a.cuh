@@ -287,6 +287,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi, bool f16) {
+    if (f16) {
+        __half2 t = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&t);
+    }
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+
 // Write one 128-byte row (w[0..31]) of a 32-row staging box in the 128-byte
 // swizzled layout a SWIZZLE_128B tensor map reads: 16-byte piece q of row r
 // sits at piece position q ^ (r % 8).  With one row per lane, the eight
@@ -475,6 +484,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int out_bytes = args.c_dtype == TILES_F32 ? 4 : 2;
         uint8_t* box_ptr = staging + quarter * L::EPI_BOX_BYTES;
         const uint32_t box = ptx::smem_addr(box_ptr);
+        // One 128-byte-wide box of the warp's 32 rows (w: this lane's row)
+        // goes to C at column x through the staging box.  Lane 0 issues
+        // every store, so its bulk groups track them all.
+        auto store_box = [&](const uint32_t (&w)[32], int x, int row0, int b) {
+            // The previous box's store has finished reading the staging box.
+            if (lane == 0) ptx::bulk_wait_read_all();
+            __syncwarp();
+            stage_box_row(box, lane, w);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && x < args.n && row0 < args.m) {
+                ptx::tma_store_3d(&tmC, box_ptr, x, row0, b);
+                ptx::bulk_commit_group();
+            }
+        };
+        // Whole 128-byte boxes: 32 fp32 or 64 16-bit columns.
+        const int per_box = out_bytes == 4 ? 1 : 2;
         uint32_t acc = 0, acc_phase = 0;
         for (int u = group; u < args.units; u += groups) {
             const UnitCoord uc = decode_unit<BN>(u, args);
@@ -485,6 +511,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             ptx::tc_fence_after();
             const int64_t row = static_cast<int64_t>(uc.mi) * L::BM + rank * 128 + row_in_tile;
+            const int box_row0 = uc.mi * L::BM + static_cast<int>(rank) * 128 + quarter * 32;
             const bool row_ok = row < args.m;
             char* crow = static_cast<char*>(args.c) +
                          (static_cast<int64_t>(uc.b) * args.stride_c + row * args.ldc) * out_bytes;
@@ -545,21 +572,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ptx::cp_async_wait_all();
                     __syncwarp();
                     const bool last = j == args.ksplit - 2;
+                    if (last && args.tma_store) {
+                        // The last partial's sums leave box by box.
+                        const bool f16 = args.c_dtype == TILES_F16;
 #pragma unroll 1
-                    for (int c = 0; c < BN / 32; ++c) {
-                        uint32_t v[32];
-                        ptx::tmem_ld_32cols(tacc + c * 32, v);
-                        ptx::tmem_ld_wait();
+                        for (int c = 0; c < BN / 32; c += per_box) {
+                            uint32_t w[32];
+                            const float* p0 = stage_buf + c * 32 * 32 + lane;   // column c*32+i at p0[32*i]
+                            if (per_box == 1) {
+                                ptx::tmem_ld_32cols(tacc + c * 32, w);
+                                ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) +
-                                                   stage_buf[(c * 32 + i) * 32 + lane]);
-                        if (!last) {
-                            ptx::tmem_st_32cols(tacc + c * 32, v);
-                            ptx::tmem_st_wait();
-                        } else if (row_ok) {
-                            store_row_chunk(crow, static_cast<int64_t>(uc.n0) + c * 32, args.n, v,
-                                            args.c_dtype);
+                                for (int i = 0; i < 32; ++i)
+                                    w[i] = __float_as_uint(__uint_as_float(w[i]) + p0[32 * i]);
+                            } else {
+                                uint32_t v0[32], v1[32];
+                                ptx::tmem_ld_32cols(tacc + c * 32, v0);
+                                ptx::tmem_ld_32cols(tacc + c * 32 + 32, v1);
+                                ptx::tmem_ld_wait();
+                                const float* p1 = p0 + 32 * 32;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    w[i] = pack_pair(__uint_as_float(v0[2 * i]) + p0[32 * (2 * i)],
+                                                     __uint_as_float(v0[2 * i + 1]) + p0[32 * (2 * i + 1)],
+                                                     f16);
+                                    w[16 + i] = pack_pair(__uint_as_float(v1[2 * i]) + p1[32 * (2 * i)],
+                                                          __uint_as_float(v1[2 * i + 1]) + p1[32 * (2 * i + 1)],
+                                                          f16);
+                                }
+                            }
+                            store_box(w, uc.n0 + c * 32, box_row0, uc.b);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int c = 0; c < BN / 32; ++c) {
+                            uint32_t v[32];
+                            ptx::tmem_ld_32cols(tacc + c * 32, v);
+                            ptx::tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = __float_as_uint(__uint_as_float(v[i]) +
+                                                       stage_buf[(c * 32 + i) * 32 + lane]);
+                            if (!last) {
+                                ptx::tmem_st_32cols(tacc + c * 32, v);
+                                ptx::tmem_st_wait();
+                            } else if (row_ok) {
+                                store_row_chunk(crow, static_cast<int64_t>(uc.n0) + c * 32, args.n, v,
+                                                args.c_dtype);
+                            }
                         }
                     }
                     __syncwarp();
@@ -567,10 +627,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             } else {
                 int c = 0;                                  // next 32-column TMEM chunk
                 if (args.tma_store) {
-                    // Whole 128-byte boxes: 32 fp32 or 64 16-bit columns.
-                    const int per_box = out_bytes == 4 ? 1 : 2;
                     const int boxes = uc.width / (32 * per_box);
-                    const int box_row0 = uc.mi * L::BM + static_cast<int>(rank) * 128 + quarter * 32;
 #pragma unroll 1
                     for (int j = 0; j < boxes; ++j, c += per_box) {
                         uint32_t w[32];
@@ -596,18 +653,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                 }
                             }
                         }
-                        // The previous box's store has finished reading the
-                        // staging box (lane 0 issued it and tracks its group).
-                        if (lane == 0) ptx::bulk_wait_read_all();
-                        __syncwarp();
-                        stage_box_row(box, lane, w);
-                        ptx::fence_proxy_async_smem();
-                        __syncwarp();
-                        const int x = uc.n0 + c * 32;
-                        if (lane == 0 && x < args.n && box_row0 < args.m) {
-                            ptx::tma_store_3d(&tmC, box_ptr, x, box_row0, uc.b);
-                            ptx::bulk_commit_group();
-                        }
+                        store_box(w, uc.n0 + c * 32, box_row0, uc.b);
                     }
                 }
 #pragma unroll 1

@@ -656,6 +656,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         store_box(w, uc.n0 + c * 32, box_row0, uc.b);
                     }
                 }
+                // Register stores: the whole unit when C has no store map,
+                // else the 32 columns a 16-bit box could not take (no
+                // compiled unit width leaves any).
 #pragma unroll 1
                 for (; c < uc.width / 32; ++c) {
                     uint32_t v[32];

@@ -257,6 +257,31 @@ def test_gb300_evaluate_random_configs(lib):
         assert gb300_fields_native(v)[:-3] == gb300_fields_oracle(ref)[:-3], cfg
 
 
+# Dynamic shared memory the 256x256 CTA-pair GEMM kernel asked for at launch,
+# as ncu reported it (launch__shared_mem_per_block_dynamic, 214.272 KB) in
+# the 4096^3 capture.
+MEASURED_SMEM_256x256_PAIR = 214272
+
+
+def test_gb300_c1_is_the_kernels_shared_memory(lib):
+    # C1's total for the bench kernel equals what its launch requested, and
+    # every compiled stage count is the deepest one that fits 227 KB (or
+    # the 8-stage barrier array): one stage more fails C1.
+    dev = T.device_preset("gb300")
+    odev = OG.GB300Device(fill_bytes_per_clk=dev.fill_bytes_per_clk,
+                          kernel_regs_per_thread=dev.kernel_regs_per_thread)
+    for bm, bn, cg, st in OG.VARIANTS:
+        cfg = OG.GB300Config(bm, bn, 64, st, cta_group=cg)
+        ref = OG.evaluate(cfg, odev, 2)
+        v = T.evaluate(dev, T.make_config(bm, bn, 64, st, 192, "tcgen05", 2, cg), 2, 4)
+        assert v.smem_total == ref.smem_total and not ref.failures, (bm, bn, cg)
+        if (bm, bn, cg) == (256, 256, 2):
+            assert v.smem_total == MEASURED_SMEM_256x256_PAIR
+        if st < OG.MAX_STAGES:
+            deeper = OG.evaluate(OG.GB300Config(bm, bn, 64, st + 1, cta_group=cg), odev, 2)
+            assert "C1" in deeper.failures, (bm, bn, cg, st)
+
+
 def test_gb300_choice_at_the_bench_shape(lib):
     dev = T.device_preset("gb300")
     best = T.plan(4096, 4096, 4096, in_dtype="f16", device=dev)[0][0]

@@ -8,6 +8,8 @@ items (more pieces asked for than items), runs of images, and one piece; two
 calls in a row reuse the library's copy streams and events.
 """
 
+import threading
+
 import numpy as np
 import pytest
 
@@ -144,3 +146,41 @@ def test_host_calls_order_after_earlier_work_on_the_stream():
     ok, worst, idx = OT.check(host_f64(c_h), OG.gemm(a64, b64), OG.gemm_bound(a64, b64), S.F32)
     assert ok, f"worst ratio {worst} at {idx}"
     assert torch.equal(after.cpu(), c_h)
+
+
+def test_host_calls_from_threads_that_exit():
+    # Each host thread has its own copy streams and events, released when
+    # the thread exits.  Three threads call at once, each on its own stream
+    # and buffers, and exit; then this thread calls.  Every result matches.
+    m, n, k = 768, 512, 256
+    a_np = S.random_matrix(77, (m, k), S.F16)
+    b_np = S.random_matrix(78, (k, n), S.F16)
+    a_h, b_h = pinned(a_np, S.F16), pinned(b_np, S.F16)
+    a64, b64 = S.widen(a_np, S.F16), S.widen(b_np, S.F16)
+    ref, bound = OG.gemm(a64, b64), OG.gemm_bound(a64, b64)
+    outs, errors = [], []
+
+    def call(idx):
+        try:
+            c_h = torch.full((m, n), float("nan"), dtype=torch.float32).pin_memory()
+            a_d = torch.empty((m, k), dtype=torch.float16, device="cuda")
+            b_d = torch.empty((k, n), dtype=torch.float16, device="cuda")
+            c_d = torch.empty((m, n), dtype=torch.float32, device="cuda")
+            s = torch.cuda.Stream()
+            T.gemm_host(a_h, b_h, c_h, a_d, b_d, c_d, stream=s, chunks=2 + idx)
+            s.synchronize()
+            outs.append(c_h)
+        except Exception as e:          # reported below, in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=call, args=(i,)) for i in range(3)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    call(3)
+    assert not errors, errors
+    assert len(outs) == 4
+    for c_h in outs:
+        ok, worst, idx = OT.check(host_f64(c_h), ref, bound, S.F32)
+        assert ok, f"worst ratio {worst} at {idx}"

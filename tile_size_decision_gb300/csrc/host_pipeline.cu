@@ -25,11 +25,30 @@ constexpr int kMaxPieces = 16;
 constexpr int kMaxPipeDevices = 64;
 
 // The copy streams and events of one host thread on one device.  Per thread,
-// so that two threads' calls never re-record each other's events.
+// so that two threads' calls never re-record each other's events; released
+// when the thread exits.  Destroying a stream with work still queued on it
+// is allowed: the work completes and the stream is released afterwards.
 struct CopyPipe {
-    bool ready;
-    cudaStream_t up, down;
-    cudaEvent_t start, done, landed[kMaxPieces], computed[kMaxPieces];
+    bool ready = false;
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr, landed[kMaxPieces] = {}, computed[kMaxPieces] = {};
+
+    CopyPipe() = default;
+    CopyPipe(const CopyPipe&) = delete;
+    CopyPipe& operator=(const CopyPipe&) = delete;
+    ~CopyPipe() {
+        // Errors are ignored: at process exit the runtime may already be
+        // shutting down, and nothing can be reported from here.
+        auto drop_event = [](cudaEvent_t e) { if (e) cudaEventDestroy(e); };
+        drop_event(start);
+        drop_event(done);
+        for (int i = 0; i < kMaxPieces; ++i) {
+            drop_event(landed[i]);
+            drop_event(computed[i]);
+        }
+        if (up) cudaStreamDestroy(up);
+        if (down) cudaStreamDestroy(down);
+    }
 };
 
 thread_local CopyPipe t_pipes[kMaxPipeDevices];
@@ -46,10 +65,12 @@ int pipe_for_current_device(CopyPipe** out) {
         return fail(TILES_ERR_INVALID_ARG, "device ordinal %d beyond %d", dev, kMaxPipeDevices);
     CopyPipe& p = t_pipes[dev];
     if (!p.ready) {
-        e = cudaStreamCreateWithFlags(&p.up, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.down, cudaStreamNonBlocking);
+        // Each handle is recorded as soon as it exists, so a failure part
+        // way leaves nothing that the destructor does not release.
+        if (!p.up) e = cudaStreamCreateWithFlags(&p.up, cudaStreamNonBlocking);
+        if (e == cudaSuccess && !p.down) e = cudaStreamCreateWithFlags(&p.down, cudaStreamNonBlocking);
         auto make = [&](cudaEvent_t* ev) {
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+            if (e == cudaSuccess && !*ev) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
         };
         make(&p.start);
         make(&p.done);

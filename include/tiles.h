@@ -391,12 +391,15 @@ int tiles_conv2d_tiled(const tiles_conv_desc* desc, int tile_oh, int tile_ow, in
  *     piece's inputs, its kernels as soon as they have landed, and its
  *     results back to the host as soon as the kernels are done.
  * Host-to-device and device-to-host copies run on two copy streams the
- * library creates on a host thread's first call on a device and keeps; the
- * kernels run on `stream`, and work enqueued on `stream` after the call
- * starts once every result is in host memory.  No device memory is
- * allocated.  chunks is in 1 .. 16.  Calls that share device buffers and
- * overlap (different streams) race.  On an error some pieces may already be
- * enqueued; the status is that of the first failing step (tiles_last_error). */
+ * library creates on a host thread's first call on a device and releases
+ * when that thread exits; the kernels run on `stream`, and work enqueued on
+ * `stream` after the call starts once every result is in host memory.  No
+ * device memory is allocated.  chunks is in 1 .. 16.  Calls that share
+ * device buffers and overlap (different streams) race.  On an error some
+ * pieces may already be enqueued, on the copy streams as well, and `stream`
+ * is then not ordered after them: synchronize the device before reusing or
+ * freeing the buffers.  The status is that of the first failing step
+ * (tiles_last_error). */
 
 /* tiles_gemm_batched from host buffers a_host, b_host to c_host. */
 int tiles_gemm_host(const tiles_gemm_desc* desc, const tiles_config* cfg, const void* a_host,

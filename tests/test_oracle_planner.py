@@ -20,7 +20,7 @@ from oracle import planner as P
 from oracle import gemm as G
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "planner_pages.json")
-PAGES = "/root/reference/PAPER.md"   # read-only mount of the source pages
+PAGES_DIR = "/root/reference"   # read-only mount of the source pages
 
 
 @pytest.fixture(scope="module")
@@ -161,11 +161,22 @@ def test_binding_order_prefers_regs_on_ties():
 # Differential run of the page's own script
 # --------------------------------------------------------------------------- #
 
-def _script_path(tmp_path_factory):
-    if not os.path.exists(PAGES):
+def _pages_lines():
+    """Lines of the mounted page text that prints the planner script."""
+    if not os.path.isdir(PAGES_DIR):
         pytest.skip("source pages not mounted")
-    with open(PAGES, encoding="utf-8") as f:
-        lines = f.read().split("\n")
+    for name in sorted(os.listdir(PAGES_DIR)):
+        if not name.endswith(".md"):
+            continue
+        with open(os.path.join(PAGES_DIR, name), encoding="utf-8") as f:
+            lines = f.read().split("\n")
+        if any(l.startswith("#!/usr/bin/env python3") for l in lines):
+            return lines
+    pytest.skip("no mounted page prints the planner script")
+
+
+def _script_path(tmp_path_factory):
+    lines = _pages_lines()
     start = next(i for i, l in enumerate(lines) if l.startswith("#!/usr/bin/env python3"))
     end = next(i for i in range(start, len(lines)) if "raise SystemExit(main())" in lines[i])
     d = tmp_path_factory.mktemp("page_script")

@@ -19,6 +19,20 @@ host cores on a bounded row sample.  ``--impl reference`` times that oracle
 alone (the deliberately slow CPU program the pages' method is checked
 against).  With N > 1 ranks each GPU runs an independent replica (the GEMM
 has no exchange step).
+
+The default single-GPU run of the 4096^3 headline adds, after the headline's
+timed steps:
+  timing     the step timed at least 50 times with L2 flushed and 50 times
+             L2-warm (mean, median, minimum);
+  sustained  about 2.5 s of back-to-back launches between one pair of
+             events, with the SM clock sampled inside that window: TFLOP/s
+             against the measured sustained bf16 peak, and the cycles per
+             launch at the clock it ran at;
+  workloads  the other four seeded workloads (gemm_512, gemm_batched,
+             gemm_ragged, conv_htiled), each measured like the headline
+             (at least 50 flushed and 50 warm steps) with its roofline, its
+             recorded DRAM traffic, its clock record and the oracle timed on
+             a bounded sample of it.
 """
 
 from __future__ import annotations
@@ -59,6 +73,13 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-cpu-seconds", type=float, default=3.0,
+                    help="CPU time budget of the oracle sample of each further workload")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="gemm_4096 only: skip the 50-iteration timings, the sustained leg and "
+                         "the other four workloads")
+    ap.add_argument("--sustained-seconds", type=float, default=2.5,
+                    help="length of the sustained back-to-back leg")
     ap.add_argument("--e2e-chunks", type=int, default=4, metavar="P",
                     help="pieces of the end-to-end call (uploads, kernels, downloads overlap)")
     ap.add_argument("--autotune", type=int, default=4, metavar="K",
@@ -223,14 +244,20 @@ def oracle_conv_sample(wl, budget_s: float, x=None, w=None):
 # --------------------------------------------------------------------------- #
 
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of the SM clock, its maximum, the power and the
+    throttle reasons, every 100 ms, each stamped with the host clock so that
+    a summary can keep the samples of one time window."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
         self.file = None
+        self.rows = []
 
     def start(self):
         try:
@@ -242,17 +269,37 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        """Stop sampling and keep the parsed rows."""
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.file.seek(0)
-        rows = [r for r in csv.reader(io.StringIO(self.file.read())) if len(r) >= 9]
-        if not rows:
-            return None
+        self.rows = parse_clock_rows(self.file.read())
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, its maximum and the throttle reasons of the
+        samples taken in [t0, t1] (host time.time(); all samples when no
+        window is given)."""
+        return summarize_clocks(self.rows, t0, t1)
+
+
+def parse_clock_rows(text: str):
+    """Rows of the sampler's CSV as dicts: t (host seconds since the epoch),
+    sm, max (MHz), power (W), reasons (the active throttle reasons)."""
+    rows = []
+    for r in csv.reader(io.StringIO(text)):
+        if len(r) < 10:
+            continue
+        try:
+            t = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            frac = r[0].strip().split(".")
+            t += float("0." + frac[1]) if len(frac) > 1 and frac[1].isdigit() else 0.0
+        except (ValueError, IndexError):
+            t = None
 
         def num(x):
             try:
@@ -260,14 +307,26 @@ class ClockSampler:
             except ValueError:
                 return None
 
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[j] for r in rows for j in range(4)
-                          if r[5 + j].strip().lower() == "active"})
-        return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+        reasons = [ClockSampler.REASONS[j] for j in range(4)
+                   if r[6 + j].strip().lower() == "active"]
+        rows.append({"t": t, "sm": num(r[2]), "max": num(r[3]), "power": num(r[4]),
+                     "reasons": reasons})
+    return rows
+
+
+def summarize_clocks(rows, t0=None, t1=None):
+    if t0 is not None:
+        rows = [r for r in rows if r["t"] is not None and t0 <= r["t"] <= t1]
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    sm = [r["sm"] for r in rows if r["sm"] is not None]
+    mx = [r["max"] for r in rows if r["max"] is not None]
+    pw = [r["power"] for r in rows if r["power"] is not None]
+    return {"sm_mhz": float(np.median(sm)) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted({x for r in rows for x in r["reasons"]}),
+            "samples": len(rows),
+            "power_w_median": float(np.median(pw)) if pw else None}
 
 
 # --------------------------------------------------------------------------- #
@@ -433,6 +492,140 @@ def host_tensor(x, dt, torch):
     return t.pin_memory()
 
 
+def timed_steps(job, stream, flush, steps, warm=False):
+    """Milliseconds of each of `steps` steps, each bracketed by CUDA events
+    on `stream`; before each step L2 is flushed (a 256 MB write outside the
+    events) unless `warm`.  Also returns the host-clock window (time.time())
+    that the steps ran in."""
+    import torch
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(steps):
+        if not warm:
+            flush.zero_()
+        starts[i].record(stream)
+        job.step(None, stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], (t0, t1)
+
+
+def roofline(job, ms, peaks, src, workload):
+    """The roofline object of one workload's kernel at `ms` per step."""
+    achieved = job.flops / (ms * 1e-3) / 1e12
+    if job.bound == "tensor":
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{src} bf16 burst (fp16 shares the bf16 tensor rate)",
+                "frac_of_nominal_2250": round(achieved / 2250.0, 4)}
+    else:
+        gbs = job.bytes / (ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(gbs / peak, 4), "peak_source": f"{src} HBM copy bandwidth",
+                "algorithmic_bytes": job.bytes,
+                "timed_over": f"the whole step ({job.launches} launch(es): "
+                              + ("the filter reorder, then " if job.reorder_launches else "")
+                              + "the convolution)"}
+    roof["traffic"] = recorded_traffic(workload)
+    return roof
+
+
+def ms_stats(ms):
+    return {"iterations": len(ms), "mean_ms": round(float(np.mean(ms)), 5),
+            "median_ms": round(float(np.median(ms)), 5), "min_ms": round(float(np.min(ms)), 5)}
+
+
+def sustained_leg(job, stream, seconds, gpu_index, peaks, src):
+    """Back-to-back launches of the step (no flush) between one pair of CUDA
+    events for about `seconds`, with the clocks sampled inside that window:
+    the throughput under the power cap and the clock-normalised time."""
+    import torch
+
+    probe, _ = timed_steps(job, stream, None, 20, warm=True)
+    n = max(50, int(seconds * 1e3 / max(float(np.median(probe)), 1e-3)))
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)
+    s_ev = torch.cuda.Event(enable_timing=True)
+    e_ev = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    s_ev.record(stream)
+    for _ in range(n):
+        job.step(None, stream)
+    e_ev.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    total_ms = s_ev.elapsed_time(e_ev)
+    us = 1e3 * total_ms / n
+    tflops = job.flops * n / (total_ms * 1e-3) / 1e12
+    clk = sampler.summary(t0, t1)
+    out = {"launches": n, "seconds": round(total_ms / 1e3, 3), "us_per_launch": round(us, 3),
+           "tflops": round(tflops, 2),
+           "frac_of_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
+           "frac_of_burst": round(tflops / peaks["bf16_tflops"], 4),
+           "peak_source": f"{src} bf16 sustained (a seconds-long loop under the power cap)",
+           "clocks": clk}
+    if clk["sm_mhz"]:
+        # Time x clock: the cycles one launch takes at the clock it ran at.
+        out["kcycles_per_launch"] = round(us * clk["sm_mhz"] / 1e3, 1)
+        if clk["sm_max_mhz"]:
+            out["tflops_at_max_clock"] = round(tflops * clk["sm_max_mhz"] / clk["sm_mhz"], 1)
+    return out
+
+
+def make_job(name, dev, tiles, torch):
+    wl = S.WORKLOADS[name]
+    return (conv_job if isinstance(wl, S.ConvWorkload) else gemm_job)(wl, dev, tiles, torch), wl
+
+
+def workload_entry(name, args, dev, tiles, torch, stream, flush, peaks, src, gpu_index):
+    """One non-headline workload measured like the headline: warm-up, then
+    at least 50 flushed steps and as many L2-warm ones, its roofline, and the
+    oracle timed on a bounded sample of it."""
+    job, wl = make_job(name, dev, tiles, torch)
+    entry = {"config": job.config}
+    if getattr(job, "autotune", None) and args.autotune > 0:
+        entry["config"]["autotune"] = job.autotune(args.autotune)
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        flush.zero_()
+        job.step(None, stream)
+    tiles.check(job.ws, stream)
+    n = max(args.steps, 50)
+    ms, (t0, t1) = timed_steps(job, stream, flush, n)
+    warm, _ = timed_steps(job, stream, flush, n, warm=True)
+    sampler.stop()
+    tiles.check(job.ws, stream)
+    mean = float(np.mean(ms))
+    entry.update({
+        "value": round(job.flops / (mean * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "ms_per_step": round(mean, 5), "flushed": ms_stats(ms),
+        "l2_warm": dict(ms_stats(warm), tflops_median=round(
+            job.flops / (float(np.median(warm)) * 1e-3) / 1e12, 2)),
+        "roofline": roofline(job, mean, peaks, src, name),
+        "gpu_launches": n * job.launches,
+        "clocks": dict(sampler.summary(t0, t1), whole_leg=sampler.summary()),
+    })
+    if not args.no_cpu_baseline:
+        tf, secs, _, desc = job.oracle(args.extra_cpu_seconds)
+        entry["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": blas_threads(),
+                                 "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    return entry
+
+
+EXTRA_WORKLOADS = ("gemm_512", "gemm_batched", "gemm_ragged", "conv_htiled")
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -444,17 +637,13 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     tiles.load()
-    wl = S.WORKLOADS[args.workload]
-    job = (conv_job if isinstance(wl, S.ConvWorkload) else gemm_job)(wl, dev, tiles, torch)
-    ws = tiles.workspace(dev)
+    job, wl = make_job(args.workload, dev, tiles, torch)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    peaks, src = load_peaks()
 
-    job_ws = getattr(job, "ws", ws)
     if getattr(job, "autotune", None) and args.autotune > 0:
         job.config["autotune"] = job.autotune(args.autotune)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -462,25 +651,23 @@ def run_ours(args, rank, world, local_rank):
     # start-up pause, so that the timed steps start from a busy GPU.
     for _ in range(args.warmup):
         flush.zero_()
-        job.step(ws, stream)
-    tiles.check(job_ws, stream)
+        job.step(None, stream)
+    tiles.check(job.ws, stream)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        job.step(ws, stream)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    kernel_ms, (t0, t1) = timed_steps(job, stream, flush, args.steps)
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - t_wall
-    clocks = sampler.stop()
-    tiles.check(job_ws, stream)
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    sampler.stop()
+    tiles.check(job.ws, stream)
     ms = float(np.mean(kernel_ms))
+    # The headline's clock record: every sample from the warm-up to the end
+    # of the timed steps (the timed region itself lasts milliseconds; the
+    # sustained leg below samples a seconds-long window under load).
+    clocks = dict(sampler.summary(), samples_in_timed_window=sampler.summary(t0, t1)["samples"])
 
     # End to end through the library's host-buffer call (pinned host buffers):
     # every step uploads the inputs and downloads the result.
@@ -494,7 +681,7 @@ def run_ours(args, rank, world, local_rank):
         job.e2e_step(stream, args.e2e_chunks)
         e_ends[i].record(stream)
     torch.cuda.synchronize()
-    tiles.check(job_ws, stream)
+    tiles.check(job.ws, stream)
     e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(e_starts, e_ends)]))
 
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, world, dev)
@@ -520,33 +707,49 @@ def run_ours(args, rank, world, local_rank):
             "tflops": round(job.flops / (lib_mean * 1e-3) / 1e12, 2),
             "note": "torch.matmul on the same device tensors; context, not a baseline"}}
 
+    # What the line reports of the headline job (the job is released before
+    # the other workloads run).
+    head = {"dtype": job.dtype, "config": job.config, "roofline": roofline(job, ms, peaks, src,
+                                                                            args.workload),
+            "h2d": int(sum(t.numel() * t.element_size() for t in job.host_in)),
+            "d2h": int(job.host_out.numel() * job.host_out.element_size()),
+            "launches": job.launches}
+
+    # The same step timed at least 50 times, L2 flushed and L2 warm, and a
+    # sustained, clock-sampled leg of back-to-back launches.
+    extras = world == 1 and args.workload == "gemm_4096" and not args.no_extras
+    timing = sustained = None
+    if extras:
+        n = max(args.steps, 50)
+        fl, _ = timed_steps(job, stream, flush, n)
+        wm, _ = timed_steps(job, stream, flush, n, warm=True)
+        tiles.check(job.ws, stream)
+        timing = {"flushed": dict(ms_stats(fl), tflops_median=round(
+                      job.flops / (float(np.median(fl)) * 1e-3) / 1e12, 2)),
+                  "l2_warm": dict(ms_stats(wm), tflops_median=round(
+                      job.flops / (float(np.median(wm)) * 1e-3) / 1e12, 2))}
+        sustained = sustained_leg(job, stream, args.sustained_seconds, local_rank, peaks, src)
+        tiles.check(job.ws, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, secs, _, desc = job.oracle(args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": desc, "seconds": round(secs, 2)}
 
+    workloads = None
+    if extras:
+        del job
+        torch.cuda.empty_cache()
+        workloads = {}
+        for name in EXTRA_WORKLOADS:
+            workloads[name] = workload_entry(name, args, dev, tiles, torch, stream, flush, peaks,
+                                             src, local_rank)
+            torch.cuda.empty_cache()
+
     if rank == 0:
-        peaks, src = load_peaks()
-        achieved = job.flops / (ms * 1e-3) / 1e12
-        value = job_throughput(world, job.flops, ms * 1e-3) / 1e12
-        e2e = job_throughput(world, job.flops, e2e_ms * 1e-3) / 1e12
-        if job.bound == "tensor":
-            peak = peaks["bf16_tflops"]
-            roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "peak_source": f"{src} bf16 burst (fp16 shares the bf16 tensor rate)",
-                    "frac_of_nominal_2250": round(achieved / 2250.0, 4)}
-        else:
-            gbs = job.bytes / (ms * 1e-3) / 1e9
-            peak = peaks["hbm_gbs"]
-            roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(gbs / peak, 4), "peak_source": f"{src} HBM copy bandwidth",
-                    "algorithmic_bytes": job.bytes,
-                    "timed_over": f"the whole step ({job.launches} launch(es): "
-                                  + ("the filter reorder, then " if job.reorder_launches else "")
-                                  + "the convolution)"}
-        roof["traffic"] = recorded_traffic(args.workload)
+        value = job_throughput(world, wl.flops, ms * 1e-3) / 1e12
+        e2e = job_throughput(world, wl.flops, e2e_ms * 1e-3) / 1e12
         line = {
             "metric": "GEMM TFLOP/s at 4096^3 fp16 and % of GB300 dense tensor peak (1 GPU)",
             "value": round(value, 2),
@@ -558,26 +761,32 @@ def run_ours(args, rank, world, local_rank):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": job.dtype,
+            "dtype": head["dtype"],
             "data": "synthetic",
             "impl": "ours",
-            "config": dict(job.config,
+            "config": dict(head["config"],
                            l2="flushed between timed steps (256 MB write, outside the kernel events)",
                            parallelism=f"replicas x{world}"),
-            "roofline": roof,
+            "roofline": head["roofline"],
             "e2e": {"value": round(e2e, 2), "unit": "TFLOP/s",
                     "call": "tiles_gemm_host" if args.workload.startswith("gemm") else "tiles_conv2d_host",
                     "pieces": args.e2e_chunks,
-                    "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in job.host_in)),
-                    "d2h_bytes_per_step": int(job.host_out.numel() * job.host_out.element_size()),
+                    "h2d_bytes_per_step": head["h2d"],
+                    "d2h_bytes_per_step": head["d2h"],
                     "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": args.steps * job.launches,
+            "gpu_launches": args.steps * head["launches"],
             "clocks": clocks,
             "wall_s_timed_region": round(wall, 4),
             "kernel_ms_min": round(min(kernel_ms), 5),
             "kernel_ms_median": round(float(np.median(kernel_ms)), 5),
             "cpu_baseline": cpu,
         }
+        if timing is not None:
+            line["timing"] = timing
+        if sustained is not None:
+            line["sustained"] = sustained
+        if workloads is not None:
+            line["workloads"] = workloads
         if context is not None:
             line["context"] = context
         if args.workload != "gemm_4096":

@@ -29,9 +29,11 @@
  *     use, of at least tiles_workspace_bytes() bytes.  Kernels record a
  *     bounded-wait timeout in its first word; tiles_check() reads and clears
  *     it.  A GEMM given tiles_gemm_workspace_bytes() bytes also uses it for
- *     the partial tiles of a last round split along K.  A NULL workspace
- *     disables the timeout report (the kernel still returns).  One
- *     workspace serves one launch at a time.
+ *     the partial tiles of a last round split along K.  The kernel calls
+ *     (GEMM, convolution, and their host-buffer forms) reject a NULL or
+ *     smaller workspace with TILES_ERR_INVALID_ARG, so that no expired wait
+ *     goes unreported; tiles_gemm_noalloc is the one kernel call that takes
+ *     none (it has its own).  One workspace serves one launch at a time.
  */
 #ifndef TILES_H
 #define TILES_H
@@ -106,7 +108,12 @@ typedef struct {
     int32_t kernel_regs_per_thread;   /* register budget of the GB300 kernels */
     int32_t cta_pairs;                /* GB300: CTA pairs (2-CTA clusters) resident at once;
                                          0 = sm_count / 2 */
-    int32_t reserved[3];
+    int32_t partial_bytes_per_clk;    /* GB300 time model: bytes per clock per SM at which a
+                                         K part of a split last round writes or reads its
+                                         fp32 partial tile (0 counts as 1) */
+    int32_t handoff_clocks;           /* GB300 time model: fixed clocks of one K-part
+                                         hand-off (flag release, acquire, latency) */
+    int32_t reserved[1];
 } tiles_device;
 
 /* One tile configuration (the page's Config record plus GB300 fields). */
@@ -324,6 +331,42 @@ int tiles_gemm(const tiles_gemm_desc* desc, const tiles_config* cfg, void* works
 int tiles_gemm_schedule(const tiles_gemm_desc* desc, const tiles_config* cfg, size_t ws_bytes,
                         tiles_schedule* out);
 
+/* ---- The compiled GEMM kernels as the hardware sees them ----------------
+ * The GB300 planner's C1, C2 and occupancy figures (README of
+ * tile_decision.py, "已知局限": the constraints are bounds that the real
+ * kernel has to confirm) restated as what the CUDA runtime reports for each
+ * compiled kernel variant. */
+typedef struct {
+    tiles_config cfg;                 /* bm, bn, bk, stages, threads, instr, acc_bufs,
+                                         cta_group of the variant (tail 0) */
+    int32_t regs_per_thread;          /* cudaFuncAttributes::numRegs */
+    int32_t local_bytes_per_thread;   /* cudaFuncAttributes::localSizeBytes (spills) */
+    int32_t static_smem_bytes;        /* cudaFuncAttributes::sharedSizeBytes */
+    int32_t dynamic_smem_bytes;       /* dynamic shared memory every launch requests */
+    int32_t max_dynamic_smem_bytes;   /* cudaFuncAttributes::maxDynamicSharedSizeBytes once
+                                         the library has opted the kernel in */
+    int32_t blocks_per_sm;            /* cudaOccupancyMaxActiveBlocksPerMultiprocessor at
+                                         that dynamic shared memory */
+    int32_t resident_groups;          /* CTA groups resident at once: blocks_per_sm * SMs
+                                         for one CTA per tile, cudaOccupancyMaxActiveClusters
+                                         for CTA pairs */
+    int32_t reserved[5];
+} tiles_variant_info;
+
+/* Number of compiled GEMM kernel variants.  Host only. */
+int tiles_gemm_variant_count(void);
+
+/* The configuration of compiled variant `index` (0 <= index < count), in
+ * the planner's enumeration order.  Host only: no GPU needed.
+ * INVALID_ARG for a bad index or NULL. */
+int tiles_gemm_variant(int index, tiles_config* out);
+
+/* What the CUDA runtime reports for compiled variant `index` on the current
+ * device (register count, shared memory, occupancy).  Opts the kernel into
+ * its dynamic shared memory as a launch would; launches nothing.
+ * INVALID_ARG for a bad index, CUDA when a runtime query fails. */
+int tiles_gemm_variant_info(int index, tiles_variant_info* out);
+
 /* Workspace bytes that let this GEMM split its last round along K (256 when
  * it needs no split; 0 on invalid arguments, see tiles_last_error).  A
  * smaller workspace is accepted by the GEMM calls and changes only the
@@ -342,11 +385,14 @@ int tiles_gemm_batched(const tiles_gemm_desc* desc, const tiles_config* cfg, voi
  *
  * Two producers build the im2col operand:
  *  - TMA (default when it applies: c % 8 == 0 and strides <= 8; needs
- *    tiles_conv_workspace_bytes() of workspace): the
- *    weights are reordered to [c_out][r][s][c padded to 64] and an NCHW
- *    input is transposed to NHWC in the workspace, then per filter tap and
- *    64 channels the operand is one strided TMA box of the NHWC input, the
- *    pads arriving as zero fill;
+ *    tiles_conv_workspace_bytes() of workspace): TMA boxes of the input
+ *    rows feed the MMA, the pads arriving as zero fill.  An NCHW input is
+ *    read in place by the direct rows form (TILES_CONV_W_TMEM_ROWS_DIRECT:
+ *    warps of the kernel transpose each stage's box into the operand); the
+ *    forms that need NHWC rows transpose an NCHW input into the workspace
+ *    first.  The filter is reordered to [c_out][r][s][c padded to 64] in the
+ *    workspace, except a 3x3 filter over 64 channels bound for tensor
+ *    memory, which the kernel builds from its OIHW rows;
  *  - gather (NCHW input only; c*kh*kw a multiple of 8): four warps gather
  *    the operand from global memory into shared memory.
  * With the TMA producer the filter sits in tensor memory as the MMA's A
@@ -413,6 +459,13 @@ int tiles_conv2d_host(const tiles_conv_desc* desc, int tile_oh, const tiles_conf
                       const void* x_host, const void* w_host, void* y_host, int chunks,
                       void* workspace, size_t ws_bytes, void* stream);
 
+/* Output height and width of the convolution `desc` describes (only its
+ * n/c/h/w, kernel, stride, pad and dilation fields are read):
+ * oh = (h + 2*ph - (kh-1)*dh - 1) / sh + 1, and ow likewise, the output of
+ * the direct convolution the H-tiles partition.  INVALID_ARG when a size is
+ * out of range or no window fits. */
+int tiles_conv_out_hw(const tiles_conv_desc* desc, int32_t* oh, int32_t* ow);
+
 /* Workspace bytes the TMA producer needs for this convolution (256 when it
  * does not apply; 0 on invalid arguments). */
 size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh);
@@ -424,12 +477,17 @@ size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh);
  * memory, paths that must not allocate).  Its scratch is a 256-byte static
  * device array in the library, held by every GPU that loads the library until
  * the process exits; the call allocates nothing and calls no allocating
- * routine.  The GEMM needs exactly that much (its timeout error word); a need
- * beyond it is rejected with TILES_ERR_TOO_LARGE.  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  All calls
- * share the array: a timeout recorded by a call stays until a call with
- * wait != 0 reads and clears it, and calls that overlap on the GPU race on it.
+ * routine.  The GEMM needs exactly that much (its timeout error word): the
+ * last round of tiles never splits along K here (it runs as whole tiles or
+ * N-halves), and a cfg that forces a K split, whose partial tiles would need
+ * more, is rejected with TILES_ERR_TOO_LARGE.  A call made outside stream
+ * capture looks up the array's device address (cudaGetSymbolAddress) with
+ * the current device (so that it follows a device reset, after which the
+ * array loads at a new address); a call during stream capture uses the
+ * address the last call outside capture found on that device, so make one
+ * call on each device before any capture.  All calls share the array: a
+ * timeout recorded by a call stays until a call with wait != 0 reads and
+ * clears it, and calls that overlap on the GPU race on it.
  * wait == 0: asynchronous on `stream`, returns the launch status.
  * wait != 0: also synchronises `stream` and returns TILES_ERR_TIMEOUT if a
  * bounded wait expired in a call since the last read. */
@@ -493,6 +551,22 @@ int tiles_check(void* workspace, void* stream);
  * wait expires and records a timeout in the workspace.  Returns the launch
  * status; tiles_check then reports TILES_ERR_TIMEOUT. */
 int tiles_selftest_wait_timeout(void* workspace, int64_t limit_ns, void* stream);
+
+/* Test hook for the kernels' own bounded waits (the production kernels,
+ * not a separate one).  Arms, for the calling thread's next GEMM launch
+ * (tiles_gemm, tiles_gemm_batched, tiles_gemm_noalloc) or next TMA
+ * convolution launch (tiles_conv2d_htiled / _tiled with the TMA producer), a
+ * planted fault: the first CTA group's TMA producer skips the loads and the
+ * arrival of its `stage`-th pipeline stage (counted from 0 over the loads it
+ * issues), so the stage's consumer waits on a barrier that never completes;
+ * every wait of that launch gives up after limit_ns nanoseconds.  The
+ * kernel then records the expiry in the workspace's error word (or the
+ * no-alloc scratch), lets its other roles stop, waits for its own copies
+ * and MMAs in flight, frees its tensor memory and returns; tiles_check
+ * reports TILES_ERR_TIMEOUT and the context stays usable.  The other CTA
+ * groups of the launch run normally.  The launch consumes the fault; stage
+ * < 0 disarms it.  INVALID_ARG unless 0 < limit_ns <= 1e10. */
+int tiles_selftest_drop_stage(int stage, int64_t limit_ns);
 
 #ifdef __cplusplus
 }

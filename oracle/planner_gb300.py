@@ -1,46 +1,60 @@
 """GB300 mode of the tile planner (oracle; test infrastructure only).
 
-Parity unpinned: no page fixes these rules.  They extend the page's
-constraint order (tile_decision.py: C3 -> C1 -> C2 -> occupancy -> C4 -> C0)
-to the sm_103a kernels of this library, and this module restates them
-independently of the C++ planner so the two can be compared bit for bit.
-The parts that reduce to the page (C0, the fill formula, the binding order)
-are pinned through the page-mode tests.
+This library's extension of the page's constraints (README of
+"04-tile-size-decision": C3 instruction shape, C1 capacity, C2 registers,
+C4 waves and last-wave fill, C0 traffic) to its sm_103a kernels, written
+independently of the C++ planner so that the two can be compared bit for
+bit.  No page fixes these rules; the README's known-limitations section says
+what fixes them instead: C1 and C2 are bounds that the real kernel has to
+confirm.  So the kernel-dependent numbers are inputs here, never literals:
+
+  * the compiled tiles (bm, bn, cta_group) come from the library's variant
+    list; the pipeline depth of each is derived, not listed: the deepest
+    stage count (at most MAX_STAGES) that passes C1;
+  * the kernels' register figure, the co-resident CTA pairs, the operand
+    fill rate and the K-split hand-off rate and latency are fields of the
+    device record, which callers fill from the runtime (GPU tests) or from
+    the library's preset (host tests).
+
+What pins them: GPU tests compare C1's total with the dynamic shared memory
+the runtime reports for each compiled kernel, the register figure with its
+register count, the resident groups with the runtime's occupancy (blocks per
+SM, co-resident clusters), and the ranking with measured launch times; host
+tests compare the time estimate with a brute-force simulation of the
+persistent schedule.  The pieces shared with the page (C0, the fill
+formula, the binding order) are pinned through the page-mode tests.
 
 Rules
   C3   tcgen05.mma kind::f16: 128 rows per CTA (bm = 128 * cta_group,
        cta_group 1 or 2), bn a multiple of 16 in [16, 256], bk a multiple of
        16; the kernels' layout adds bk * in_bytes == 128 (one swizzle atom),
        (bn / cta_group) a multiple of 64, 192 threads, 1-2 accumulators,
-       1-8 stages.  One violation count per failed condition.
-  C1   stages * ((bm/cg)*bk + bk*(bn/cg)) * in_bytes + 16384 (the
-       epilogue's staging: four 32-row x 128-byte boxes, from which TMA
-       stores write C) + 256 (barriers) + 1024 (alignment slack)
-       <= smem_per_block_max.  The page's C1 counts the A/B tiles alone and
-       names the epilogue, barriers and padding it leaves out.
+       1-MAX_STAGES stages.  One violation per failed condition.
+  C1   stages * ((bm + bn) / cg) * bk * in_bytes + the epilogue's staging
+       (four 32-row x 128-byte boxes) + the barrier block + 1 KB of
+       alignment slack <= smem_per_block_max.  The page's C1 counts the A/B
+       tiles alone and names what it leaves out.
   C2   TMEM: acc_bufs * bn fp32 columns, allocated as a power of two >= 32,
        <= tmem_cols.
-  occupancy  least of regs (kernel_regs_per_thread * threads), smem,
-       threads, TMEM; binding order regs, smem, threads, tmem.
-  C4   grid = b * ceil(M/bm) * ceil(N/bn); resident = max(bps * slots, 1)
-       with slots = sm_count for one CTA per tile and the co-resident CTA
-       pairs (cta_pairs, else sm_count // 2) for pairs; waves; fill as on the
-       page.
+  residency  least of regs (kernel_regs_per_thread * threads), smem,
+       threads, TMEM blocks per SM; ties go to regs, smem, threads, tmem.
+  C4   tiles = b * ceil(M/bm) * ceil(N/bn); resident groups = blocks per
+       SM times the SMs (one CTA per tile) or the co-resident CTA pairs
+       (cta_pairs, else sm_count // 2); waves; fill as on the page.
   C0   the page's expression with b, in_bytes, out_bytes.
-  time est_clocks = (grid // resident) * ceil(K/bk) * unit + the last
-       round's cost, unit = max(mma, fill), mma = (bm/cg)*bn*bk*2 //
-       mma_flops_per_clk, fill = ceil(smem_per_stage / fill_bytes_per_clk).
-       The last round (when grid % resident > 0) takes the cheapest of:
-       whole tiles ceil(K/bk) * unit; N-halves (if whole B atoms and the rest
-       fills at most half the groups) ceil(K/bk) * unit of the half-width
-       tile; K parts s in 2..min(resident // rest, 8, K blocks):
-       ceil(K/bk / s) * unit + (s-1) * reduce with reduce =
-       2 * ceil((bm/cg)*bn*4 / PARTIAL_BYTES_PER_CLK) + 2048: a K part's
-       fp32 partial goes out and comes back at 32 bytes per clock per SM,
-       the rate measured for it on GB300 (not the operand fill rate).
-       tail_split reports s, -1 for N-halves, 0 for whole tiles.
-  rank (est_clocks, round(C0), -bps, smem_total), stable over the variant
-       order.
+  time est_clocks = whole rounds * K blocks * unit + the last round's cost,
+       unit = max(mma, fill) with mma = (bm/cg)*bn*bk*2 // mma_flops_per_clk
+       and fill = ceil(stage bytes / fill_bytes_per_clk).  The last round
+       (when tiles % resident > 0) takes the cheapest of: whole tiles;
+       N-halves (whole B atoms, and the rest fills at most half the groups)
+       at the half-width tile's unit; K parts s = 2 .. min(resident // rest,
+       MAX_TAIL_PARTS, K blocks) at ceil(K blocks / s) * unit + (s - 1) *
+       reduce, reduce = 2 * ceil((bm/cg)*bn*4 / partial_bytes_per_clk) +
+       handoff_clocks (a part's fp32 partial goes out and comes back).
+       Ties keep that order and the fewer parts.  tail_split reports s, -1
+       for N-halves, 0 for whole tiles.
+  rank (est_clocks, round(C0), -blocks per SM, smem_total), stable over the
+       variant order.
 """
 
 from __future__ import annotations
@@ -49,19 +63,24 @@ from dataclasses import dataclass, field
 
 from . import planner as page
 
-# Compiled variants (bm, bn, cta_group, stages), in enumeration order.
-VARIANTS = ((128, 64, 1, 8), (128, 128, 1, 6), (128, 192, 1, 5), (128, 256, 1, 4),
-            (256, 128, 2, 8), (256, 256, 2, 6))
-
-THREADS = 192
-EPILOGUE_BYTES = 4 * 32 * 128
-BARRIER_BYTES = 256
-ALIGN_SLACK = 1024
+THREADS = 192                  # warp-specialised block: producer, MMA, 4 epilogue warps
+EPILOGUE_BYTES = 4 * 32 * 128  # one 32-row x 128-byte staging box per epilogue warp
+BARRIER_BYTES = 256            # mbarriers, the TMEM address slot, the abort flag
+ALIGN_SLACK = 1024             # operand tiles start on a 1024-byte swizzle atom
 MAX_STAGES = 8
+MAX_TAIL_PARTS = 8
 
 
 @dataclass(frozen=True)
 class GB300Device:
+    """Hardware and kernel facts.  The kernel-dependent fields have no
+    defaults: a caller supplies them from an observation or a preset."""
+
+    kernel_regs_per_thread: int
+    fill_bytes_per_clk: int
+    partial_bytes_per_clk: int
+    handoff_clocks: int
+    cta_pairs: int = 0          # co-resident 2-CTA clusters; 0 = sm_count // 2
     smem_per_sm: int = 228 * 1024
     smem_per_block_max: int = 227 * 1024
     regs_per_sm: int = 65536
@@ -70,9 +89,6 @@ class GB300Device:
     sm_count: int = 148
     tmem_cols: int = 512
     mma_flops_per_clk: int = 8192
-    fill_bytes_per_clk: int = 64
-    kernel_regs_per_thread: int = 168
-    cta_pairs: int = 0          # co-resident 2-CTA clusters; 0 = sm_count // 2
 
 
 @dataclass(frozen=True)
@@ -118,25 +134,35 @@ def _tmem_alloc(cols: int) -> int:
     return p
 
 
+def stage_bytes(bm: int, bn: int, bk: int, cg: int, in_bytes: int = 2) -> int:
+    """One pipeline stage of one CTA: its bm/cg rows of A and bn/cg columns
+    of B, bk deep."""
+    return (bm // cg + bn // cg) * bk * in_bytes
+
+
+def c1_total(bm: int, bn: int, bk: int, cg: int, stages: int, in_bytes: int = 2) -> int:
+    return stage_bytes(bm, bn, bk, cg, in_bytes) * stages + EPILOGUE_BYTES + BARRIER_BYTES \
+        + ALIGN_SLACK
+
+
 def evaluate(cfg: GB300Config, dev: GB300Device, in_bytes: int = 2) -> GB300Verdict:
     v = GB300Verdict(cfg=cfg)
-    cg = cfg.cta_group
-    bad = [cg not in (1, 2)]
-    cgs = cg if cg in (1, 2) else 1
-    bad += [
-        cfg.bm != 128 * cgs,
-        cfg.bn % 16 != 0 or cfg.bn < 16 or cfg.bn > 256,
-        cfg.bk % 16 != 0 or cfg.bk * in_bytes != 128,
-        (cfg.bn // cgs) % 64 != 0,
-        cfg.threads != THREADS,
-        not 1 <= cfg.acc_bufs <= 2,
-        not 1 <= cfg.stages <= MAX_STAGES,
-    ]
-    v.c3_violations = sum(bad)
+    cg = cfg.cta_group if cfg.cta_group in (1, 2) else 1
+    conditions = (
+        cfg.cta_group in (1, 2),
+        cfg.bm == 128 * cg,
+        cfg.bn % 16 == 0 and 16 <= cfg.bn <= 256,
+        cfg.bk % 16 == 0 and cfg.bk * in_bytes == 128,
+        (cfg.bn // cg) % 64 == 0,
+        cfg.threads == THREADS,
+        1 <= cfg.acc_bufs <= 2,
+        1 <= cfg.stages <= MAX_STAGES,
+    )
+    v.c3_violations = sum(not ok for ok in conditions)
     if v.c3_violations:
         v.failures.append(page.C3)
-    v.smem_per_stage = ((cfg.bm // cgs) * cfg.bk + cfg.bk * (cfg.bn // cgs)) * in_bytes
-    v.smem_total = v.smem_per_stage * cfg.stages + EPILOGUE_BYTES + BARRIER_BYTES + ALIGN_SLACK
+    v.smem_per_stage = stage_bytes(cfg.bm, cfg.bn, cfg.bk, cg, in_bytes)
+    v.smem_total = c1_total(cfg.bm, cfg.bn, cfg.bk, cg, cfg.stages, in_bytes)
     if v.smem_total > dev.smem_per_block_max:
         v.failures.append(page.C1)
     v.tmem_cols_alloc = _tmem_alloc(max(cfg.acc_bufs * cfg.bn, 1))
@@ -144,19 +170,33 @@ def evaluate(cfg: GB300Config, dev: GB300Device, in_bytes: int = 2) -> GB300Verd
         v.failures.append(page.C2)
     v.regs_per_thread = dev.kernel_regs_per_thread
     v.regs_per_block = dev.kernel_regs_per_thread * cfg.threads
-    v.blocks_by_regs = dev.regs_per_sm // max(v.regs_per_block, 1)
-    v.blocks_by_smem = dev.smem_per_sm // max(v.smem_total, 1)
-    v.blocks_by_threads = dev.max_threads_per_sm // max(cfg.threads, 1)
-    v.blocks_by_tmem = dev.tmem_cols // max(v.tmem_cols_alloc, 1)
-    counts = (("regs", v.blocks_by_regs), ("smem", v.blocks_by_smem),
-              ("threads", v.blocks_by_threads), ("tmem", v.blocks_by_tmem))
-    least = min(c for _, c in counts)
-    v.blocks_per_sm = max(min(least, dev.max_blocks_per_sm), 0)
+    supply_demand = (
+        ("regs", dev.regs_per_sm, v.regs_per_block),
+        ("smem", dev.smem_per_sm, v.smem_total),
+        ("threads", dev.max_threads_per_sm, cfg.threads),
+        ("tmem", dev.tmem_cols, v.tmem_cols_alloc),
+    )
+    fits = {name: supply // max(demand, 1) for name, supply, demand in supply_demand}
+    v.blocks_by_regs, v.blocks_by_smem = fits["regs"], fits["smem"]
+    v.blocks_by_threads, v.blocks_by_tmem = fits["threads"], fits["tmem"]
+    scarcest = min(fits.values())
+    v.blocks_per_sm = max(min(scarcest, dev.max_blocks_per_sm), 0)
     if v.blocks_per_sm == 0:
         v.failures.append(page.OCC)
     else:
-        v.binding = next(name for name, c in counts if c == least)
+        v.binding = next(name for name, _, _ in supply_demand if fits[name] == scarcest)
     return v
+
+
+def deepest_stages(bm: int, bn: int, cg: int, dev: GB300Device, in_bytes: int = 2) -> int:
+    """The pipeline depth of a compiled tile: the most stages (up to
+    MAX_STAGES) that still pass C1; 0 when not even one does."""
+    bk = 128 // in_bytes
+    best = 0
+    for st in range(1, MAX_STAGES + 1):
+        if c1_total(bm, bn, bk, cg, st, in_bytes) <= dev.smem_per_block_max:
+            best = st
+    return best
 
 
 def resident_groups(v: GB300Verdict, dev: GB300Device) -> int:
@@ -179,21 +219,19 @@ def finish_parallelism(v: GB300Verdict, dev: GB300Device, b: int, m: int, n: int
         v.warnings.append(page.W_IDLE)
 
 
-MAX_TAIL_PARTS = 8
-
-
-HANDOFF_CLOCKS = 2048
-PARTIAL_BYTES_PER_CLK = 32
-
-
-def _stage_bytes(bm: int, bn: int, bk: int, cg: int, in_bytes: int = 2) -> int:
-    return ((bm // cg) * bk + bk * (bn // cg)) * in_bytes
-
-
-def _unit(dev: GB300Device, bm: int, bn: int, bk: int, cg: int) -> int:
+def unit_clocks(dev: GB300Device, bm: int, bn: int, bk: int, cg: int) -> int:
+    """Clocks of one K block of one tile: the MMA's or the operand fill's,
+    whichever is longer."""
     mma = (bm // cg) * bn * bk * 2 // dev.mma_flops_per_clk
-    fill = page.ceil_div(_stage_bytes(bm, bn, bk, cg), dev.fill_bytes_per_clk)
+    fill = page.ceil_div(stage_bytes(bm, bn, bk, cg), dev.fill_bytes_per_clk)
     return max(mma, fill)
+
+
+def reduce_clocks(dev: GB300Device, bm: int, bn: int, cg: int) -> int:
+    """Clocks one extra K part adds to the last part: its fp32 partial tile
+    per CTA written and read back, plus the hand-off's fixed latency."""
+    return 2 * page.ceil_div((bm // cg) * bn * 4, max(dev.partial_bytes_per_clk, 1)) \
+        + dev.handoff_clocks
 
 
 def nhalf_applies(cfg: GB300Config, grid: int, resident: int) -> bool:
@@ -213,16 +251,16 @@ def tail_choice(v: GB300Verdict, dev: GB300Device, kblocks: int, resident: int):
     fewer parts)."""
     cfg = v.cfg
     cg = max(cfg.cta_group, 1)
-    unit = _unit(dev, cfg.bm, cfg.bn, cfg.bk, cg)
+    unit = unit_clocks(dev, cfg.bm, cfg.bn, cfg.bk, cg)
     best = ("whole", 0, kblocks * unit)
     rest = v.grid % resident
     if rest == 0:
         return best
     if nhalf_applies(cfg, v.grid, resident):
-        t = kblocks * _unit(dev, cfg.bm, cfg.bn // 2, cfg.bk, cg)
+        t = kblocks * unit_clocks(dev, cfg.bm, cfg.bn // 2, cfg.bk, cg)
         if t < best[2]:
             best = ("nhalf", 0, t)
-    reduce = 2 * page.ceil_div((cfg.bm // cg) * cfg.bn * 4, PARTIAL_BYTES_PER_CLK) + HANDOFF_CLOCKS
+    reduce = reduce_clocks(dev, cfg.bm, cfg.bn, cg)
     for s in range(2, min(resident // rest, MAX_TAIL_PARTS, kblocks) + 1):
         t = page.ceil_div(kblocks, s) * unit + (s - 1) * reduce
         if t < best[2]:
@@ -234,7 +272,7 @@ def est_clocks(v: GB300Verdict, dev: GB300Device, k: int) -> int:
     cfg = v.cfg
     cg = max(cfg.cta_group, 1)
     kblocks = page.ceil_div(k, cfg.bk)
-    unit = _unit(dev, cfg.bm, cfg.bn, cfg.bk, cg)
+    unit = unit_clocks(dev, cfg.bm, cfg.bn, cfg.bk, cg)
     resident = resident_groups(v, dev)
     mode, parts, clocks = tail_choice(v, dev, kblocks, resident)
     v.tail_split = parts if mode == "ksplit" else (-1 if mode == "nhalf" else 0)
@@ -242,16 +280,24 @@ def est_clocks(v: GB300Verdict, dev: GB300Device, k: int) -> int:
     return (v.grid // resident) * kblocks * unit + (clocks if rest else 0)
 
 
-def plan(b: int, m: int, n: int, k: int, dev: GB300Device, in_bytes: int = 2,
+def compiled_configs(tiles, dev: GB300Device, in_bytes: int = 2) -> list:
+    """Configurations of the compiled tiles (bm, bn, cta_group), each at
+    its deepest stage count."""
+    bk = 128 // in_bytes
+    return [GB300Config(bm, bn, bk, deepest_stages(bm, bn, cg, dev, in_bytes), cta_group=cg)
+            for bm, bn, cg in tiles]
+
+
+def plan(b: int, m: int, n: int, k: int, dev: GB300Device, tiles, in_bytes: int = 2,
          out_bytes: int = 2) -> list:
+    """Feasible verdicts of the compiled tiles, best first."""
     kept = []
-    for bm, bn, cg, stages in VARIANTS:
-        cfg = GB300Config(bm, bn, 128 // in_bytes, stages, cta_group=cg)
+    for cfg in compiled_configs(tiles, dev, in_bytes):
         v = evaluate(cfg, dev, in_bytes)
         if v.failures:
             continue
         finish_parallelism(v, dev, b, m, n)
-        v.c0_bytes = page.c0_bytes(m, n, k, bm, bn, in_bytes, out_bytes, b)
+        v.c0_bytes = page.c0_bytes(m, n, k, cfg.bm, cfg.bn, in_bytes, out_bytes, b)
         v.est_clocks = est_clocks(v, dev, k)
         kept.append(v)
     kept.sort(key=lambda v: (v.est_clocks, round(v.c0_bytes), -v.blocks_per_sm, v.smem_total))

@@ -20,6 +20,7 @@ from tile_size_decision_gb300 import _abi
 from oracle import conv as OC
 from oracle import planner as OP
 from oracle import planner_gb300 as OG
+from tests.planner_util import compiled_tiles, oracle_device
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tiles.h")
@@ -170,6 +171,23 @@ def test_htile_rows_match_oracle(lib):
                                     r.in_start, r.in_end, r.in_span, r.pt, r.pb, r.halo)
 
 
+def test_conv_out_hw_matches_oracle(lib):
+    d = _abi.ConvDesc()
+    oh, ow = C.c_int32(0), C.c_int32(0)
+    for h, k, s, p, dil in [(224, 3, 2, 1, 1), (9, 3, 2, 1, 1), (5, 5, 1, 2, 2), (7, 1, 3, 0, 1),
+                            (1, 1, 1, 0, 1), (17, 5, 4, 3, 2)]:
+        d.n, d.c, d.h, d.w, d.c_out, d.kh, d.kw = 1, 1, h, h + 3, 1, k, k
+        d.sh, d.sw, d.ph, d.pw, d.dh, d.dw = s, s, p, p, dil, dil
+        assert lib.tiles_conv_out_hw(C.byref(d), C.byref(oh), C.byref(ow)) == _abi.OK
+        assert (oh.value, ow.value) == (OC.out_size(h, k, s, p, p, dil),
+                                        OC.out_size(h + 3, k, s, p, p, dil))
+        assert T.conv_out_hw(h, h + 3, k, k, (s, s), (p, p), (dil, dil)) == (oh.value, ow.value)
+    d.h, d.kh, d.ph, d.dh = 2, 5, 0, 1          # no window fits
+    assert lib.tiles_conv_out_hw(C.byref(d), C.byref(oh), C.byref(ow)) == _abi.ERR_INVALID_ARG
+    d.h, d.sh = 9, 0
+    assert lib.tiles_conv_out_hw(C.byref(d), C.byref(oh), C.byref(ow)) == _abi.ERR_INVALID_ARG
+
+
 # --------------------------------------------------------------------------- #
 # Planner parity, GB300 mode
 # --------------------------------------------------------------------------- #
@@ -215,9 +233,7 @@ def test_gb300_plan_with_measured_pairs(lib, pairs):
     dev.sm_count = 152
     dev.cta_pairs = pairs
     native, nf = T.plan(4096, 4096, 4096, in_dtype="f16", device=dev)
-    odev = OG.GB300Device(sm_count=152, fill_bytes_per_clk=dev.fill_bytes_per_clk,
-                          kernel_regs_per_thread=dev.kernel_regs_per_thread, cta_pairs=pairs)
-    ref = OG.plan(1, 4096, 4096, 4096, odev, 2, 2)
+    ref = OG.plan(1, 4096, 4096, 4096, oracle_device(dev), compiled_tiles(T), 2, 2)
     assert [gb300_fields_native(v) for v in native] == [gb300_fields_oracle(v) for v in ref]
 
 
@@ -227,19 +243,43 @@ def test_gb300_plan_matches_oracle(lib, case):
     dev = T.device_preset("gb300")
     dev.sm_count = sm
     native, nf = T.plan(m, n, k, b=b, in_dtype=di, out_dtype=do, mode="gb300", device=dev)
-    odev = OG.GB300Device(sm_count=sm, fill_bytes_per_clk=dev.fill_bytes_per_clk,
-                          kernel_regs_per_thread=dev.kernel_regs_per_thread,
-                          cta_pairs=dev.cta_pairs)
-    ref = OG.plan(b, m, n, k, odev, 2, 4 if do == "f32" else 2)
-    assert nf == len(ref) == len(OG.VARIANTS)
+    ref = OG.plan(b, m, n, k, oracle_device(dev), compiled_tiles(T), 2, 4 if do == "f32" else 2)
+    assert nf == len(ref) == len(T.gemm_variants())
     assert [gb300_fields_native(v) for v in native] == [gb300_fields_oracle(v) for v in ref]
+
+
+@pytest.mark.parametrize("field,values", [
+    ("kernel_regs_per_thread", (96, 168, 176, 256)),
+    ("fill_bytes_per_clk", (16, 48, 64, 128)),
+    ("partial_bytes_per_clk", (0, 8, 32, 256)),
+    ("handoff_clocks", (0, 512, 2048, 20000)),
+])
+def test_gb300_plan_follows_every_model_input(lib, field, values):
+    # The kernel-dependent numbers are inputs of both planners: varying any
+    # one of them (on shapes whose last round admits every schedule) keeps
+    # the two in step, and each changes some ranking or estimate.
+    shapes = [(1, 4096, 4096, 4096), (16, 2048, 2048, 1024), (1, 5000, 3000, 4096),
+              (1, 3000, 2000, 1536), (1, 512, 512, 512)]
+    seen = set()
+    for val in values:
+        dev = T.device_preset("gb300")
+        dev.sm_count = 152
+        setattr(dev, field, val)
+        out = []
+        for b, m, n, k in shapes:
+            native, _ = T.plan(m, n, k, b=b, in_dtype="bf16", device=dev)
+            ref = OG.plan(b, m, n, k, oracle_device(dev), compiled_tiles(T), 2, 2)
+            got = [gb300_fields_native(v) for v in native]
+            assert got == [gb300_fields_oracle(v) for v in ref], (field, val, m, n, k)
+            out.append(tuple(got))
+        seen.add(tuple(out))
+    assert len(seen) > 1, f"{field} changes nothing"
 
 
 def test_gb300_evaluate_random_configs(lib):
     rng = random.Random(99)
     dev = T.device_preset("gb300")
-    odev = OG.GB300Device(fill_bytes_per_clk=dev.fill_bytes_per_clk,
-                          kernel_regs_per_thread=dev.kernel_regs_per_thread)
+    odev = oracle_device(dev)
     for _ in range(1500):
         cfg = OG.GB300Config(rng.choice([64, 128, 256, 384]), rng.choice([16, 48, 64, 128, 192,
                                                                            256, 320, 512]),
@@ -263,23 +303,97 @@ def test_gb300_evaluate_random_configs(lib):
 MEASURED_SMEM_256x256_PAIR = 214272
 
 
-def test_gb300_c1_is_the_kernels_shared_memory(lib):
-    # C1's total for the bench kernel equals what its launch requested, and
-    # every compiled stage count is the deepest one that fits 227 KB (or
-    # the 8-stage barrier array): one stage more fails C1.
+def test_compiled_variants_are_the_deepest_pipelines_that_fit(lib):
+    # The library's compiled variants, as configurations: every stage count
+    # is the one the oracle derives from C1 (the deepest that fits 227 KB,
+    # or the 8-stage barrier array), and C1's total for the bench kernel
+    # equals what its launch requested as ncu observed it.
     dev = T.device_preset("gb300")
-    odev = OG.GB300Device(fill_bytes_per_clk=dev.fill_bytes_per_clk,
-                          kernel_regs_per_thread=dev.kernel_regs_per_thread)
-    for bm, bn, cg, st in OG.VARIANTS:
-        cfg = OG.GB300Config(bm, bn, 64, st, cta_group=cg)
-        ref = OG.evaluate(cfg, odev, 2)
-        v = T.evaluate(dev, T.make_config(bm, bn, 64, st, 192, "tcgen05", 2, cg), 2, 4)
-        assert v.smem_total == ref.smem_total and not ref.failures, (bm, bn, cg)
-        if (bm, bn, cg) == (256, 256, 2):
+    odev = oracle_device(dev)
+    variants = T.gemm_variants()
+    assert len(variants) == lib.tiles_gemm_variant_count() >= 1
+    for c in variants:
+        assert (c.bk, c.threads, c.acc_bufs, c.instr, c.tail) == (64, 192, 2, _abi.INSTR_TCGEN05, 0)
+        assert c.stages == OG.deepest_stages(c.bm, c.bn, c.cta_group, odev), (c.bm, c.bn)
+        ref = OG.evaluate(OG.GB300Config(c.bm, c.bn, 64, c.stages, cta_group=c.cta_group), odev)
+        v = T.evaluate(dev, c, 2, 4)
+        assert v.smem_total == ref.smem_total and not ref.failures and not v.failures
+        if (c.bm, c.bn, c.cta_group) == (256, 256, 2):
             assert v.smem_total == MEASURED_SMEM_256x256_PAIR
-        if st < OG.MAX_STAGES:
-            deeper = OG.evaluate(OG.GB300Config(bm, bn, 64, st + 1, cta_group=cg), odev, 2)
-            assert "C1" in deeper.failures, (bm, bn, cg, st)
+        if c.stages < OG.MAX_STAGES:
+            deeper = OG.evaluate(OG.GB300Config(c.bm, c.bn, 64, c.stages + 1, cta_group=c.cta_group),
+                                 odev)
+            assert "C1" in deeper.failures
+    out = _abi.Config()
+    assert lib.tiles_gemm_variant(len(variants), C.byref(out)) == _abi.ERR_INVALID_ARG
+    assert lib.tiles_gemm_variant(-1, C.byref(out)) == _abi.ERR_INVALID_ARG
+
+
+def simulated_makespan(v, dev, k):
+    """Clocks of the persistent schedule worked out unit by unit: units are
+    the whole tiles, then the last round's tiles in their schedule (whole,
+    two N-halves each, or s K parts each covering K blocks [p*kb//s,
+    (p+1)*kb//s)); CTA group g runs units g, g + G, ... in turn (G = the
+    smaller of the units and the resident groups); a unit costs its K
+    blocks times the clocks of one K block at its width, and the last K part
+    of a split tile, once its own K blocks are done, waits for its leading
+    parts to be done and then adds one partial read-back per leading part."""
+    cfg = v.cfg
+    cg = cfg.cta_group
+    kb = -(-k // cfg.bk)
+    resident = OG.resident_groups(v, dev)
+    rest = v.grid % resident
+    mode, parts, _ = OG.tail_choice(v, dev, kb, resident)
+    full_unit = OG.unit_clocks(dev, cfg.bm, cfg.bn, cfg.bk, cg)
+    units = [(kb * full_unit, None, 0)] * (v.grid - rest)       # (cost, tile, part)
+    for t in range(rest):
+        if mode == "nhalf":
+            half = OG.unit_clocks(dev, cfg.bm, cfg.bn // 2, cfg.bk, cg)
+            units += [(kb * half, None, 0)] * 2
+        elif mode == "ksplit":
+            for p in range(parts):
+                blocks = (p + 1) * kb // parts - p * kb // parts
+                units.append((blocks * full_unit, t, p))
+        else:
+            units.append((kb * full_unit, None, 0))
+    groups = min(len(units), resident)
+    clock = [0] * groups
+    done = {}
+    reduce = OG.reduce_clocks(dev, cfg.bm, cfg.bn, cg)
+    for u, (cost, tile, part) in enumerate(units):
+        g = u % groups
+        finish = clock[g] + cost
+        if tile is not None and part == parts - 1:
+            finish = max([finish] + [done[(tile, p)] for p in range(parts - 1)])
+            finish += (parts - 1) * reduce
+        clock[g] = finish
+        if tile is not None:
+            done[(tile, part)] = clock[g]
+    return max(clock)
+
+
+@pytest.mark.parametrize("sm,pairs", [(148, 0), (152, 76), (152, 74), (160, 0)])
+def test_gb300_estimate_is_the_simulated_schedule(lib, sm, pairs):
+    # The time estimate's round arithmetic against a unit-by-unit simulation
+    # of the persistent schedule, over shapes whose last rounds take every
+    # schedule (whole tiles, N-halves, 2-8 K parts) on every compiled tile.
+    dev = T.device_preset("gb300")
+    dev.sm_count, dev.cta_pairs = sm, pairs
+    odev = oracle_device(dev)
+    rng = random.Random(sm * 1000 + pairs)
+    shapes = [(1, 4096, 4096, 4096), (16, 2048, 2048, 1024), (1, 5000, 3000, 4096),
+              (1, 512, 512, 512), (1, 3000, 2000, 1536), (1, 256, 256, 16384)]
+    shapes += [(rng.randint(1, 4), rng.randint(1, 6000), rng.randint(1, 6000),
+                rng.randint(1, 9000)) for _ in range(60)]
+    modes = set()
+    for b, m, n, k in shapes:
+        for cfg in OG.compiled_configs(compiled_tiles(T), odev):
+            v = OG.evaluate(cfg, odev)
+            OG.finish_parallelism(v, odev, b, m, n)
+            est = OG.est_clocks(v, odev, k)
+            assert est == simulated_makespan(v, odev, k), (b, m, n, k, cfg)
+            modes.add(min(v.tail_split, 2))
+    assert modes == {-1, 0, 2}, modes
 
 
 def test_gb300_choice_at_the_bench_shape(lib):

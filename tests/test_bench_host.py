@@ -38,3 +38,16 @@ def test_recorded_traffic_needs_a_matching_hash(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda wl: "1111111111111111")
     assert bench.recorded_traffic("gemm_4096") is None
     assert bench.recorded_traffic("conv_htiled") is None
+
+
+def test_clock_summary_keeps_only_the_samples_of_its_window():
+    lines = [f"2026/12/02 14:41:0{i}.250, 0, {2000 - 100 * i}, 2070, 1000, 0x0, Not Active, "
+             f"Not Active, {'Active' if i == 3 else 'Not Active'}, Not Active" for i in range(5)]
+    rows = bench.parse_clock_rows("\n".join(lines) + "\nmalformed,row\n")
+    assert len(rows) == 5
+    t = [r["t"] for r in rows]
+    assert all(b - a == 1.0 for a, b in zip(t, t[1:]))
+    s = bench.summarize_clocks(rows, t[1], t[2])
+    assert (s["samples"], s["sm_mhz"], s["sm_max_mhz"], s["reasons"]) == (2, 1850.0, 2070.0, [])
+    assert bench.summarize_clocks(rows)["reasons"] == ["sw_thermal_slowdown"]
+    assert bench.summarize_clocks(rows, t[4] + 1, t[4] + 2)["samples"] == 0

@@ -104,3 +104,18 @@ def test_text_output_mentions_every_row():
     assert lines[0].startswith("hardware: 132 SMs")
     rows = [ln.split() for ln in lines if ln.split() and ln.split()[0].isdigit()]
     assert sum(1 for r in rows if len(r) > 10) == 5
+
+
+def test_gb300_diagnose_defaults_are_the_compiled_bench_kernel():
+    # With no flags but the mode, --diagnose checks the 256x256 CTA-pair
+    # tile at the depth it was compiled with, which passes every constraint.
+    T.load()
+    res = run_json("--mode", "gb300", "--diagnose")
+    v = res["diagnosis"]
+    assert (v["bm"], v["bn"], v["cta_group"]) == (256, 256, 2)
+    compiled = {(c.bm, c.bn, c.cta_group): c.stages for c in T.gemm_variants()}
+    assert v["stages"] == compiled[(256, 256, 2)]
+    assert v["failures"] == [] and v["blocks_per_sm"] == 1
+    # One stage deeper no longer fits (C1), and the shared memory is reported.
+    deeper = run_json("--mode", "gb300", "--diagnose", "--stages", str(v["stages"] + 1))
+    assert "C1" in deeper["diagnosis"]["failures"]

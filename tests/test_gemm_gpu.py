@@ -419,6 +419,5 @@ def test_many_tiny_batch_items(ws):
     c = empty_out((batch, m, n), S.F32)
     T.gemm_batched(to_cuda(a, S.F16), to_cuda(b, S.F16), out=c, workspace=ws)
     T.check(ws)
-    got = to_f64(c)
-    for i in (0, 1, 499, 998, 999):
-        assert_close(got[i], S.widen(a[i], S.F16), S.widen(b[i], S.F16), S.F32)
+    # Every item against the oracle (a batched float64 matmul).
+    assert_close(to_f64(c), S.widen(a, S.F16), S.widen(b, S.F16), S.F32)

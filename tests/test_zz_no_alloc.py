@@ -4,9 +4,10 @@ Such callers (code running inside an allocator or driver callback, under a
 runtime that owns all device memory, or on a path that must not allocate)
 cannot hand the library a workspace.  The entry point uses the library's
 static device scratch instead.  These tests call it through the C ABI twice in
-a row and compare each result with the workspace-taking entry point
-(tiles_gemm_batched) under the parity tolerance of the other GPU tests.  The
-file is named so that pytest collects it last.
+a row and compare each result with the float64 oracle under the parity
+tolerance of the other GPU tests, and with the workspace-taking entry point
+(tiles_gemm_batched, the same kernel and schedule) bit for bit.  The file is
+named so that pytest collects it last.
 """
 
 import ctypes as C
@@ -55,22 +56,23 @@ def test_noalloc_matches_workspace_gemm_on_two_calls(case):
     handle = C.c_void_p(stream.cuda_stream)
 
     ws = T.workspace()
-    ref = empty_out((bsz, m, n), dt_out)
-    d_ref = desc_for(a, b, ref, dt_in, dt_out)
-    assert lib.tiles_gemm_batched(C.byref(d_ref), None, ws.data_ptr(), ws.numel(), handle) == 0
+    same = empty_out((bsz, m, n), dt_out)
+    d_ws = desc_for(a, b, same, dt_in, dt_out)
+    assert lib.tiles_gemm_batched(C.byref(d_ws), None, ws.data_ptr(), ws.numel(), handle) == 0
     assert lib.tiles_check(ws.data_ptr(), handle) == 0
-    ref64 = to_f64(ref)
+    same64 = to_f64(same)
 
     a64, b64 = S.widen(a_np, dt_in), S.widen(b_np, dt_in)
-    bound = OG.gemm_bound(a64, b64)
+    ref, bound = OG.gemm(a64, b64), OG.gemm_bound(a64, b64)
     for call in range(2):
         out = empty_out((bsz, m, n), dt_out)
         d = desc_for(a, b, out, dt_in, dt_out)
         status = lib.tiles_gemm_noalloc(C.byref(d), None, handle, 1)
         assert status == 0, lib.tiles_last_error().decode()
         got = to_f64(out)
-        ok, worst, idx = OT.check(got, ref64, bound, dt_out)
+        ok, worst, idx = OT.check(got, ref, bound, dt_out)
         assert ok, f"call {call}: ratio {worst} at {idx}"
+        assert np.array_equal(got, same64), f"call {call} differs from tiles_gemm_batched"
 
 
 def test_noalloc_rejects_bad_arguments_before_launch():
@@ -83,3 +85,34 @@ def test_noalloc_rejects_bad_arguments_before_launch():
     d.a_dtype = d.b_dtype = _abi.F16
     d.c_dtype = _abi.F32
     assert lib.tiles_gemm_noalloc(C.byref(d), None, None, 1) == _abi.ERR_MISALIGNED
+    # A K-split last round would need more scratch than the static array.
+    d.c = 0x30000
+    d.m = d.n = d.k = d.lda = d.ldb = d.ldc = 4096
+    stages = {(c.bn, c.cta_group): c.stages for c in T.gemm_variants()}[(256, 2)]
+    ks = T.make_config(256, 256, 64, stages, 192, "tcgen05", 2, 2, tail="ksplit")
+    assert lib.tiles_gemm_noalloc(C.byref(d), C.byref(ks), None, 1) == _abi.ERR_TOO_LARGE
+
+
+def test_noalloc_reports_a_timeout_once_then_clears_it():
+    # A bounded wait that runs out in one no-alloc call (a planted fault:
+    # the first CTA group skips one pipeline stage, 50 ms wait limit) is
+    # recorded in the library's static scratch; the next call with wait != 0
+    # reports it once and clears it, and the call after that is clean and
+    # correct.
+    lib = T.load()
+    bsz, m, n, k = 2, 512, 384, 1024
+    a_np = S.random_matrix(17, (bsz, m, k), S.F16, "normal")
+    b_np = S.random_matrix(18, (bsz, k, n), S.F16, "normal")
+    a, b = to_cuda(a_np, S.F16), to_cuda(b_np, S.F16)
+    handle = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    out = empty_out((bsz, m, n), S.F32)
+    d = desc_for(a, b, out, S.F16, S.F32)
+    assert lib.tiles_selftest_drop_stage(3, 50_000_000) == 0
+    assert lib.tiles_gemm_noalloc(C.byref(d), None, handle, 0) == 0
+    assert lib.tiles_gemm_noalloc(C.byref(d), None, handle, 1) == _abi.ERR_TIMEOUT
+    out2 = empty_out((bsz, m, n), S.F32)
+    d2 = desc_for(a, b, out2, S.F16, S.F32)
+    assert lib.tiles_gemm_noalloc(C.byref(d2), None, handle, 1) == 0
+    a64, b64 = S.widen(a_np, S.F16), S.widen(b_np, S.F16)
+    ok, worst, idx = OT.check(to_f64(out2), OG.gemm(a64, b64), OG.gemm_bound(a64, b64), S.F32)
+    assert ok, f"ratio {worst} at {idx}"

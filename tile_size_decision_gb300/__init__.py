@@ -18,11 +18,13 @@ from ._abi import TilesError, check as _check
 __all__ = [
     "TilesError", "load", "version", "device_preset", "device_query", "evaluate",
     "finish_parallelism", "c0_bytes", "plan", "htile_rows", "workspace_bytes", "workspace",
+    "gemm_variants", "gemm_variant_info",
     "gemm", "gemm_batched", "gemm_schedule", "gemm_workspace", "gemm_noalloc", "gemm_autotune",
     "gemm_host", "conv2d_host",
     "tuned_lookup", "tuned_save", "tuned_load", "tuned_clear", "conv2d_htiled", "conv2d_tiled",
     "conv_workspace",
-    "conv_out_shape", "check", "selftest_wait_timeout", "make_config",
+    "conv_out_shape", "conv_out_hw", "check", "selftest_wait_timeout", "selftest_drop_stage",
+    "make_config",
 ]
 
 
@@ -104,6 +106,25 @@ def plan(m: int, n: int, k: int, b: int = 1, in_dtype: str = "f16", out_dtype: s
     out = (_abi.Verdict * max(cap, 1))()
     _check(lib.tiles_plan(C.byref(device), C.byref(p), out, cap, C.byref(nf)), "tiles_plan")
     return list(out[:cap]), nf.value
+
+
+def gemm_variants() -> list:
+    """The compiled GEMM kernel variants as configurations (no GPU needed)."""
+    lib = load()
+    out = []
+    for i in range(lib.tiles_gemm_variant_count()):
+        c = _abi.Config()
+        _check(lib.tiles_gemm_variant(i, C.byref(c)), "tiles_gemm_variant")
+        out.append(c)
+    return out
+
+
+def gemm_variant_info(index: int) -> _abi.VariantInfo:
+    """What the CUDA runtime reports for compiled variant `index` on the
+    current device: registers, shared memory, resident blocks and groups."""
+    info = _abi.VariantInfo()
+    _check(load().tiles_gemm_variant_info(index, C.byref(info)), "tiles_gemm_variant_info")
+    return info
 
 
 def htile_rows(H, kh, sh, pt, d, o0, o1) -> _abi.HTile:
@@ -302,9 +323,15 @@ def conv2d_host(x_host, w_host, y_host, x_dev, w_dev, y_dev, stride=(1, 1), pad=
 
 
 def conv_out_hw(h, w, kh, kw, stride, pad, dil):
-    oh = (h + 2 * pad[0] - (kh - 1) * dil[0] - 1) // stride[0] + 1
-    ow = (w + 2 * pad[1] - (kw - 1) * dil[1] - 1) // stride[1] + 1
-    return oh, ow
+    """Output height and width of a convolution (tiles_conv_out_hw)."""
+    d = _abi.ConvDesc()
+    d.n, d.c, d.h, d.w, d.c_out, d.kh, d.kw = 1, 1, h, w, 1, kh, kw
+    d.sh, d.sw = stride
+    d.ph, d.pw = pad
+    d.dh, d.dw = dil
+    oh, ow = C.c_int32(0), C.c_int32(0)
+    _check(load().tiles_conv_out_hw(C.byref(d), C.byref(oh), C.byref(ow)), "tiles_conv_out_hw")
+    return oh.value, ow.value
 
 
 def _conv_desc(x, w, stride, pad, dil, out, layout):
@@ -414,7 +441,8 @@ def gemm_workspace(a, b, out, cfg=None):
     d = _gemm_desc(*_batched3(a, b, out), batched=True)
     n = int(load().tiles_gemm_workspace_bytes(C.byref(d), _cfg_ptr(cfg)))
     if n == 0:
-        raise TilesError(load().tiles_status_string(-1) and -1, "tiles_gemm_workspace_bytes")
+        # The call returns 0 on invalid arguments; tiles_last_error says why.
+        raise TilesError(_abi.ERR_INVALID_ARG, "tiles_gemm_workspace_bytes")
     return torch.zeros(n, dtype=torch.uint8, device=a.device)
 
 
@@ -440,3 +468,9 @@ def selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
     _check(load().tiles_selftest_wait_timeout(workspace.data_ptr(), limit_ns,
                                               _stream_handle(stream)),
            "tiles_selftest_wait_timeout")
+
+
+def selftest_drop_stage(stage: int, limit_ns: int) -> None:
+    """Arm a planted fault for this thread's next GEMM or TMA convolution
+    launch (tiles_selftest_drop_stage); stage < 0 disarms."""
+    _check(load().tiles_selftest_drop_stage(stage, limit_ns), "tiles_selftest_drop_stage")

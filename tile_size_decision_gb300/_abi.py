@@ -45,8 +45,9 @@ class Device(C.Structure):
         "smem_per_sm", "smem_per_block_max", "regs_per_sm", "max_threads_per_sm",
         "max_threads_per_block", "max_blocks_per_sm", "regs_per_thread_max",
         "reg_granularity_per_warp", "warp_size", "sm_count", "tmem_cols", "mma_flops_per_clk",
-        "fill_bytes_per_clk", "kernel_regs_per_thread", "cta_pairs")] + \
-        [("reserved", C.c_int32 * 3)]
+        "fill_bytes_per_clk", "kernel_regs_per_thread", "cta_pairs", "partial_bytes_per_clk",
+        "handoff_clocks")] + \
+        [("reserved", C.c_int32 * 1)]
 
 
 class Config(C.Structure):
@@ -111,6 +112,13 @@ class Schedule(C.Structure):
                 ("tail_mode", C.c_int32), ("ksplit", C.c_int32), ("workspace_bytes", C.c_int64)]
 
 
+class VariantInfo(C.Structure):
+    _fields_ = [("cfg", Config)] + [(n, C.c_int32) for n in (
+        "regs_per_thread", "local_bytes_per_thread", "static_smem_bytes", "dynamic_smem_bytes",
+        "max_dynamic_smem_bytes", "blocks_per_sm", "resident_groups")] + \
+        [("reserved", C.c_int32 * 5)]
+
+
 class TuneResult(C.Structure):
     _fields_ = [("cfg", Config), ("status", C.c_int32), ("tail_mode", C.c_int32),
                 ("ksplit", C.c_int32), ("us", C.c_float)]
@@ -150,6 +158,9 @@ SIGNATURES = {
     "tiles_gemm_schedule": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_size_t,
                                       C.POINTER(Schedule)]),
     "tiles_gemm_workspace_bytes": (C.c_size_t, [C.POINTER(GemmDesc), C.POINTER(Config)]),
+    "tiles_gemm_variant_count": (C.c_int, []),
+    "tiles_gemm_variant": (C.c_int, [C.c_int, C.POINTER(Config)]),
+    "tiles_gemm_variant_info": (C.c_int, [C.c_int, C.POINTER(VariantInfo)]),
     "tiles_conv2d_htiled": (C.c_int, [C.POINTER(ConvDesc), C.c_int, C.POINTER(Config),
                                       C.c_void_p, C.c_size_t, C.c_void_p]),
     "tiles_gemm_noalloc": (C.c_int, [C.POINTER(GemmDesc), C.POINTER(Config), C.c_void_p,
@@ -162,6 +173,8 @@ SIGNATURES = {
     "tiles_conv2d_tiled": (C.c_int, [C.POINTER(ConvDesc), C.c_int, C.c_int, C.c_int,
                                      C.POINTER(Config), C.c_void_p, C.c_size_t, C.c_void_p]),
     "tiles_conv_workspace_bytes": (C.c_size_t, [C.POINTER(ConvDesc), C.c_int]),
+    "tiles_conv_out_hw": (C.c_int, [C.POINTER(ConvDesc), C.POINTER(C.c_int32),
+                                    C.POINTER(C.c_int32)]),
     "tiles_gemm_autotune": (C.c_int, [C.POINTER(GemmDesc), C.c_int, C.c_int, C.c_void_p,
                                       C.c_size_t, C.c_void_p, C.POINTER(TuneResult), C.c_int,
                                       C.POINTER(C.c_int), C.POINTER(Config)]),
@@ -172,6 +185,7 @@ SIGNATURES = {
     "tiles_tuned_clear": (C.c_int, []),
     "tiles_check": (C.c_int, [C.c_void_p, C.c_void_p]),
     "tiles_selftest_wait_timeout": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
+    "tiles_selftest_drop_stage": (C.c_int, [C.c_int, C.c_int64]),
 }
 
 _lib = None

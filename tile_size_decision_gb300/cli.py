@@ -36,7 +36,16 @@ INSTRS = sorted(_abi.INSTR_CODES)
 PAGE_DEFAULTS = dict(m=4096, n=4096, k=4096, instr="wgmma", sm_count=132, smem_kb=228,
                      block_m=128, block_n=128, block_k=32, stages=3, threads=256, topk=15)
 GB300_DEFAULTS = dict(m=4096, n=4096, k=4096, instr="tcgen05", block_m=256, block_n=256,
-                      block_k=64, stages=7, threads=192, topk=15)
+                      block_k=64, threads=192, topk=15)
+
+
+def compiled_stages(bm: int, bn: int, cta_group: int) -> int:
+    """The pipeline depth of the compiled kernel with this tile (GB300 mode's
+    default --stages); 2 for a tile no kernel was compiled for."""
+    for c in T.gemm_variants():
+        if (c.bm, c.bn, c.cta_group) == (bm, bn, cta_group):
+            return c.stages
+    return 2
 
 
 def parse(argv=None):
@@ -74,6 +83,8 @@ def parse(argv=None):
             setattr(a, key, val)
     if a.cta_group is None:
         a.cta_group = 0 if a.mode == "pages" else (2 if a.block_m == 256 else 1)
+    if a.stages is None:
+        a.stages = compiled_stages(a.block_m, a.block_n, a.cta_group)
     return a
 
 

@@ -30,6 +30,8 @@ thread_local std::string g_last_error;
 
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr size_t kWorkspaceBytes = 256;
+static_assert(kWorkspaceBytes == static_cast<size_t>(kConvMinWorkspaceBytes),
+              "one workspace minimum for every kernel call");
 
 int bytes_of(int dtype) {
     switch (dtype) {
@@ -181,6 +183,34 @@ int max_groups(int ordinal, int bn, int cg, int sm_count) {
     if (cg == 2 && bn == 128) g = gemm_variant_max_groups<128, 2>(sm_count);
     cache[key] = g;
     return g;
+}
+
+int variant_attributes(int bn, int cg, int sm_count, VariantAttributes* out) {
+    if (cg == 1) {
+        switch (bn) {
+            case 64: return gemm_variant_attributes<64, 1>(sm_count, out);
+            case 128: return gemm_variant_attributes<128, 1>(sm_count, out);
+            case 192: return gemm_variant_attributes<192, 1>(sm_count, out);
+            case 256: return gemm_variant_attributes<256, 1>(sm_count, out);
+            default: break;
+        }
+    } else if (cg == 2) {
+        switch (bn) {
+            case 128: return gemm_variant_attributes<128, 2>(sm_count, out);
+            case 256: return gemm_variant_attributes<256, 2>(sm_count, out);
+            default: break;
+        }
+    }
+    return static_cast<int>(cudaErrorInvalidValue);
+}
+
+// The configuration of compiled variant i.
+tiles_config variant_config(int i) {
+    const KernelVariant& kv = kGemmVariants[i];
+    tiles_config c{};
+    c.bm = kv.bm; c.bn = kv.bn; c.bk = 64; c.stages = kv.stages; c.threads = kGemmThreads;
+    c.instr = TILES_INSTR_TCGEN05; c.acc_bufs = 2; c.cta_group = kv.cta_group;
+    return c;
 }
 
 int launch_variant(int bn, int cg, const CUtensorMap& ta, const CUtensorMap& tb,
@@ -364,6 +394,11 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
     GemmPlan gp;
     int s = gemm_prepare(d, user_cfg, batched, ws ? ws_bytes : 0, &gp);
     if (s != TILES_OK) return s;
+    // The workspace carries the kernel's timeout report: without one an
+    // expired wait would go unreported.
+    if (!ws || ws_bytes < kWorkspaceBytes)
+        return fail(TILES_ERR_INVALID_ARG, "a workspace of at least %zu bytes is required",
+                    kWorkspaceBytes);
     const tiles_config& cfg = gp.cfg;
     const int64_t batch = d->batch;
     const int64_t sa = batch > 1 ? d->stride_a : d->m * d->lda;
@@ -404,8 +439,11 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
     args.tma_store = tma_c ? 1 : 0;
     args.idesc = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, cfg.bm, cfg.bn);
     args.idesc_half = ptx::idesc_f16_f32acc(d->a_dtype == TILES_BF16, true, cfg.bm, cfg.bn / 2);
-    args.err = (ws && ws_bytes >= sizeof(int32_t)) ? static_cast<int32_t*>(ws) : nullptr;
+    args.err = static_cast<int32_t*>(ws);
     args.wait_limit_ns = kDefaultWaitLimitNs;
+    const PlantedFault planted = take_planted_fault();
+    args.drop_stage = planted.stage;
+    if (planted.stage >= 0) args.wait_limit_ns = planted.limit_ns;
     int e = launch_variant(cfg.bn, cfg.cta_group, ta, tb, tc, args, (int)gp.groups,
                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
@@ -415,6 +453,16 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
 }
 
 }  // namespace
+
+namespace {
+thread_local PlantedFault g_planted{-1, 0};
+}  // namespace
+
+PlantedFault take_planted_fault() {
+    const PlantedFault f = g_planted;
+    g_planted = PlantedFault{-1, 0};
+    return f;
+}
 
 int fail(int status, const char* fmt, ...) {
     char buf[512];
@@ -466,15 +514,23 @@ void* g_noalloc_addr[kMaxDevices] = {};
 
 // The device address of the scratch array on the current device.  In host
 // code the array's name is only a host-side stand-in, so the address is
-// asked of the runtime once per device (with that device current) and kept.
-int noalloc_scratch(void** out) {
+// asked of the runtime with the device current.  A call outside stream
+// capture asks again (after a device reset the module, and the array, load
+// anew at another address); a call during capture uses the address the last
+// call outside capture found on this device.
+int noalloc_scratch(cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices)
         return fail(TILES_ERR_INVALID_ARG, "device ordinal %d beyond %d", dev, kMaxDevices);
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) {
+        cudaGetLastError();
+        capture = cudaStreamCaptureStatusActive;     // unknown: keep the known address
+    }
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    if (!g_noalloc_addr[dev] || capture == cudaStreamCaptureStatusNone) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, tiles_noalloc_scratch);
         if (e != cudaSuccess || !p)
@@ -544,9 +600,68 @@ int tiles_device_query(int ordinal, tiles_device* out) {
     if (major == 10) {
         int current = 0;
         cudaGetDevice(&current);
-        if (current == ordinal) d.cta_pairs = max_groups(ordinal, 256, 2, d.sm_count);
+        if (current == ordinal) {
+            d.cta_pairs = max_groups(ordinal, 256, 2, d.sm_count);
+            // The kernels' register figure as the runtime reports it: the
+            // largest count of any compiled variant, rounded up to the
+            // per-warp allocation granule as the page's C2 rounds.
+            int regs = 0;
+            for (int i = 0; i < kNumGemmVariants; ++i) {
+                VariantAttributes va{};
+                if (variant_attributes(kGemmVariants[i].bn, kGemmVariants[i].cta_group, d.sm_count,
+                                       &va) == cudaSuccess)
+                    regs = std::max(regs, va.regs);
+                else
+                    cudaGetLastError();
+            }
+            if (regs > 0 && d.warp_size > 0 && d.reg_granularity_per_warp > 0) {
+                const int per_warp = (regs * d.warp_size + d.reg_granularity_per_warp - 1) /
+                                     d.reg_granularity_per_warp * d.reg_granularity_per_warp;
+                d.kernel_regs_per_thread = per_warp / d.warp_size;
+            }
+        }
     }
     *out = d;
+    return TILES_OK;
+}
+
+int tiles_gemm_variant_count(void) { return kNumGemmVariants; }
+
+int tiles_gemm_variant(int index, tiles_config* out) {
+    if (!out || index < 0 || index >= kNumGemmVariants)
+        return fail(TILES_ERR_INVALID_ARG, "variant index %d outside [0, %d)", index,
+                    kNumGemmVariants);
+    *out = variant_config(index);
+    return TILES_OK;
+}
+
+int tiles_gemm_variant_info(int index, tiles_variant_info* out) {
+    if (!out || index < 0 || index >= kNumGemmVariants)
+        return fail(TILES_ERR_INVALID_ARG, "variant index %d outside [0, %d)", index,
+                    kNumGemmVariants);
+    int ordinal = 0;
+    cudaError_t e = cudaGetDevice(&ordinal);
+    if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ordinal);
+    if (e != cudaSuccess)
+        return fail(TILES_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    std::memset(out, 0, sizeof(*out));
+    out->cfg = variant_config(index);
+    VariantAttributes va{};
+    const int r = variant_attributes(out->cfg.bn, out->cfg.cta_group, sms, &va);
+    if (r != cudaSuccess) {
+        cudaGetLastError();
+        return fail(TILES_ERR_CUDA, "variant %d: %s", index,
+                    cudaGetErrorString(static_cast<cudaError_t>(r)));
+    }
+    out->regs_per_thread = va.regs;
+    out->local_bytes_per_thread = va.local_bytes;
+    out->static_smem_bytes = va.static_smem;
+    out->dynamic_smem_bytes = va.dynamic_smem;
+    out->max_dynamic_smem_bytes = va.max_dynamic_smem;
+    out->blocks_per_sm = va.blocks_per_sm;
+    out->resident_groups = va.groups;
     return TILES_OK;
 }
 
@@ -839,6 +954,17 @@ int tiles_selftest_wait_timeout(void* ws, int64_t limit_ns, void* stream) {
     return TILES_OK;
 }
 
+int tiles_selftest_drop_stage(int stage, int64_t limit_ns) {
+    if (stage < 0) {
+        take_planted_fault();
+        return TILES_OK;
+    }
+    if (limit_ns <= 0 || limit_ns > 10000000000ll)
+        return fail(TILES_ERR_INVALID_ARG, "limit_ns must be in (0, 1e10]");
+    g_planted = PlantedFault{stage, static_cast<uint64_t>(limit_ns)};
+    return TILES_OK;
+}
+
 int tiles_conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg,
                         void* ws, size_t ws_bytes, void* stream) {
     return conv2d_htiled(desc, tile_oh, cfg, ws, ws_bytes, stream);
@@ -849,17 +975,37 @@ int tiles_conv2d_tiled(const tiles_conv_desc* desc, int tile_oh, int tile_ow, in
     return conv2d_tiled(desc, tile_oh, tile_ow, tile_n, cfg, ws, ws_bytes, stream);
 }
 
+int tiles_conv_out_hw(const tiles_conv_desc* desc, int32_t* oh, int32_t* ow) {
+    if (!oh || !ow) return fail(TILES_ERR_INVALID_ARG, "null output");
+    int64_t h = 0, w = 0;
+    const int s = conv_out_hw(desc, &h, &w);
+    if (s != TILES_OK) return s;
+    if (h > INT32_MAX || w > INT32_MAX) return fail(TILES_ERR_TOO_LARGE, "output too large");
+    *oh = static_cast<int32_t>(h);
+    *ow = static_cast<int32_t>(w);
+    return TILES_OK;
+}
+
 size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh) {
     return static_cast<size_t>(conv_workspace_bytes(desc, tile_oh));
 }
 
 int tiles_gemm_noalloc(const tiles_gemm_desc* desc, const tiles_config* cfg, void* stream,
                        int wait) {
-    if (tiles_workspace_bytes() > kNoAllocScratchBytes)
-        return fail(TILES_ERR_TOO_LARGE, "the GEMM needs %zu bytes of scratch; the static array "
-                    "holds %zu", tiles_workspace_bytes(), kNoAllocScratchBytes);
+    static_assert(kWorkspaceBytes <= kNoAllocScratchBytes,
+                  "the static scratch holds the kernels' error word");
+    // Every schedule but a K-split last round needs the error word alone; a
+    // configuration that forces a K split needs room for its partial tiles.
+    if (cfg && cfg->tail == TILES_TAIL_KSPLIT) {
+        int st = TILES_OK;
+        const int64_t need = gemm_ws_bytes(desc, cfg, &st);
+        if (st != TILES_OK) return st;
+        if (need > static_cast<int64_t>(kNoAllocScratchBytes))
+            return fail(TILES_ERR_TOO_LARGE, "a K-split last round needs %lld bytes of scratch; "
+                        "the static array holds %zu", (long long)need, kNoAllocScratchBytes);
+    }
     void* scratch = nullptr;
-    int s = noalloc_scratch(&scratch);
+    int s = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);
     if (s != TILES_OK) return s;
     s = gemm_common(desc, cfg, scratch, kNoAllocScratchBytes, stream, true);
     if (s != TILES_OK || !wait) return s;

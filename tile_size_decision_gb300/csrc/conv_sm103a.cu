@@ -298,6 +298,23 @@ PFN_cuTensorMapEncodeTiled_v12000 conv_encode_fn() {
 
 }  // namespace
 
+int conv_out_hw(const tiles_conv_desc* d, int64_t* oh, int64_t* ow) {
+    if (!d) return fail(TILES_ERR_INVALID_ARG, "null descriptor");
+    if (d->h < 1 || d->w < 1 || d->kh < 1 || d->kw < 1 || d->sh < 1 || d->sw < 1 || d->dh < 1 ||
+        d->dw < 1 || d->ph < 0 || d->pw < 0)
+        return fail(TILES_ERR_INVALID_ARG, "sizes, strides and dilations must be >= 1, pads >= 0");
+    // Output extent of a padded, dilated, strided window sweep: the windows
+    // (k-1)*d+1 wide that fit in h + 2p, one every s.
+    const int64_t span_h = static_cast<int64_t>(d->kh - 1) * d->dh + 1;
+    const int64_t span_w = static_cast<int64_t>(d->kw - 1) * d->dw + 1;
+    const int64_t in_h = static_cast<int64_t>(d->h) + 2 * d->ph;
+    const int64_t in_w = static_cast<int64_t>(d->w) + 2 * d->pw;
+    if (in_h < span_h || in_w < span_w) return fail(TILES_ERR_INVALID_ARG, "empty output");
+    *oh = (in_h - span_h) / d->sh + 1;
+    *ow = (in_w - span_w) / d->sw + 1;
+    return TILES_OK;
+}
+
 int conv2d_tiled(const tiles_conv_desc* d, int tile_oh, int tile_ow, int tile_n,
                  const tiles_config* cfg, void* ws, size_t ws_bytes, void* stream) {
     if (!d) return fail(TILES_ERR_INVALID_ARG, "null descriptor");
@@ -315,11 +332,9 @@ int conv2d_tiled(const tiles_conv_desc* d, int tile_oh, int tile_ow, int tile_n,
     if ((reinterpret_cast<uintptr_t>(d->x) & 1u) || (reinterpret_cast<uintptr_t>(d->y) & (ob - 1)) ||
         (reinterpret_cast<uintptr_t>(d->wt) & 1u))
         return fail(TILES_ERR_MISALIGNED, "x, w and y must be element aligned");
-    const int64_t oh = (static_cast<int64_t>(d->h) + 2 * d->ph - static_cast<int64_t>(d->kh - 1) * d->dh - 1) / d->sh + 1;
-    const int64_t ow = (static_cast<int64_t>(d->w) + 2 * d->pw - static_cast<int64_t>(d->kw - 1) * d->dw - 1) / d->sw + 1;
-    if (d->h + 2 * d->ph < (d->kh - 1) * d->dh + 1 || d->w + 2 * d->pw < (d->kw - 1) * d->dw + 1 ||
-        oh < 1 || ow < 1)
-        return fail(TILES_ERR_INVALID_ARG, "empty output");
+    int64_t oh = 0, ow = 0;
+    const int hw = conv_out_hw(d, &oh, &ow);
+    if (hw != TILES_OK) return hw;
     // tile_ow / tile_n <= 0: the whole width / batch in one tile.
     if (tile_ow <= 0 || tile_ow > ow) tile_ow = static_cast<int>(std::min<int64_t>(ow, INT32_MAX));
     if (tile_n <= 0 || tile_n > d->n) tile_n = d->n;
@@ -330,6 +345,11 @@ int conv2d_tiled(const tiles_conv_desc* d, int tile_oh, int tile_ow, int tile_n,
         return fail(TILES_ERR_TOO_LARGE, "tile_ow must be below 32768");
     if (k > (1 << 24) || tile_cols > (1 << 30) || static_cast<int64_t>(d->n) * d->c * d->h * d->w > (1ll << 40))
         return fail(TILES_ERR_TOO_LARGE, "convolution too large");
+    // The workspace carries the kernels' timeout report: without one an
+    // expired wait would go unreported.
+    if (!ws || ws_bytes < kConvMinWorkspaceBytes)
+        return fail(TILES_ERR_INVALID_ARG, "a workspace of at least %d bytes is required",
+                    kConvMinWorkspaceBytes);
 
     // Producer: the TMA im2col when it applies and the workspace holds its
     // prepared operands (or when forced), else the thread gather.
@@ -444,9 +464,8 @@ int64_t conv_workspace_bytes(const tiles_conv_desc* d, int tile_oh) {
     if (!d || tile_oh < 1 || d->kh < 1 || d->kw < 1 || d->sh < 1 || d->sw < 1 || d->dh < 1 ||
         d->dw < 1 || d->n < 1 || d->c < 1 || d->h < 1 || d->w < 1 || d->c_out < 1)
         return 0;
-    const int64_t oh = (static_cast<int64_t>(d->h) + 2 * d->ph - static_cast<int64_t>(d->kh - 1) * d->dh - 1) / d->sh + 1;
-    const int64_t ow = (static_cast<int64_t>(d->w) + 2 * d->pw - static_cast<int64_t>(d->kw - 1) * d->dw - 1) / d->sw + 1;
-    if (oh < 1 || ow < 1) return 0;
+    int64_t oh = 0, ow = 0;
+    if (conv_out_hw(d, &oh, &ow) != TILES_OK) return 0;
     ConvTmaGeometry g;
     return conv_tma_geometry(d, oh, ow, tile_oh, static_cast<int>(std::min<int64_t>(ow, INT32_MAX)), &g)
                ? g.ws_bytes : 256;

@@ -17,8 +17,12 @@
 // neighbouring pixels of one NCHW output plane: coalesced stores.
 //
 // The weights are reordered once per call to [c_out][r][s][C padded to 64]
-// (the K-major B operand in the same K order), and an NCHW input is first
-// transposed to NHWC; both go to the caller's workspace.
+// (the K-major operand in the same K order) in the caller's workspace,
+// except a 3x3 filter over 64 channels bound for tensor memory, which the
+// kernel builds from its OIHW rows.  An NCHW input is read in place by the
+// direct rows form (its warps transpose each stage's TMA box of input rows
+// into the operand); the other forms read NHWC rows, so for them an NCHW
+// input is first transposed to NHWC in the workspace.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -55,6 +59,7 @@ struct ConvTmaArgs {
     uint32_t idesc;
     int32_t* err;
     uint64_t wait_limit_ns;
+    int32_t drop_stage;                   // test hook: CTA 0 skips this input load (-1: none)
     // Weights in tensor memory (conv_wtmem_kernel): the reordered weights,
     // their row length kh*kw*Cp, the pixels of a tile (MMA N), the first
     // TMEM column of the weights (after the accumulators) and the shared-
@@ -700,9 +705,13 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                     // The transposers read the box's column origin after
                     // waiting on the slot's barrier (the arrive releases it).
                     bar->raw_col0[rs] = st.col0;
-                    ptx::mbar_arrive_expect_tx(rfull, raw_tx);
-                    tma_load_4d(base + args.raw_off + rs * args.raw_b, &tmX, rfull, st.col0 & ~7,
-                                st.ih, st.c0, st.img);
+                    // A planted fault (test hook) skips one box: its slot
+                    // never fills and the transposers' bounded wait expires.
+                    if (!(blockIdx.x == 0 && issued == args.drop_stage)) {
+                        ptx::mbar_arrive_expect_tx(rfull, raw_tx);
+                        tma_load_4d(base + args.raw_off + rs * args.raw_b, &tmX, rfull,
+                                    st.col0 & ~7, st.ih, st.c0, st.img);
+                    }
                     ++issued;
                     if (++rs == static_cast<uint32_t>(args.raw_stages)) { rs = 0; rphase ^= 1u; }
                     if (++kb == args.k_stages) { kb = 0; u += ur.step; }
@@ -748,6 +757,12 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                         break;
                     }
                     uint8_t* st = ring + stage * stage_bytes;
+                    if (blockIdx.x == 0 && issued == args.drop_stage) {
+                        // A planted fault (test hook): this stage never fills.
+                        ++issued;
+                        if (++stage == static_cast<uint32_t>(stages)) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     ptx::mbar_arrive_expect_tx(&bar->full[stage], args.tx_bytes);
                     if constexpr (ROWS) {
                         // Kernel row r, 64 channels: every stride phase of
@@ -1818,6 +1833,11 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
     a.out_dtype = d->out_dtype;
     a.err = static_cast<int32_t*>(ws);
     a.wait_limit_ns = 2000000000ull;
+    // A fault planted by the test hook goes to the first launch (of the TMEM
+    // forms, which take it) alone.
+    const PlantedFault planted = take_planted_fault();
+    a.drop_stage = planted.stage;
+    if (planted.stage >= 0) a.wait_limit_ns = planted.limit_ns;
     a.wr = wr;
     a.kp = static_cast<int32_t>(d->kh * d->kw * g.cp);
     const bool y16 = (reinterpret_cast<uintptr_t>(d->y) & 15u) == 0;
@@ -2041,6 +2061,8 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
                 if (e == cudaSuccess) e = cudaGetLastError();
                 if (e != cudaSuccess)
                     return fail(TILES_ERR_CUDA, "conv launch: %s", cudaGetErrorString(e));
+                a.drop_stage = -1;
+                a.wait_limit_ns = 2000000000ull;
             }
         }
     }

@@ -61,6 +61,37 @@ int gemm_variant_max_groups<BN, CG>(int sm_count) {
 }
 
 template <>
+int gemm_variant_attributes<BN, CG>(int sm_count, VariantAttributes* out) {
+    cudaError_t e = set_smem_attribute();
+    if (e != cudaSuccess) return static_cast<int>(e);
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, gemm_tcgen05_kernel<BN, STAGES, CG>);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    out->regs = fa.numRegs;
+    out->local_bytes = static_cast<int>(fa.localSizeBytes);
+    out->static_smem = static_cast<int>(fa.sharedSizeBytes);
+    out->dynamic_smem = Layout::SMEM_BYTES;
+    out->max_dynamic_smem = fa.maxDynamicSharedSizeBytes;
+    int blocks = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemm_tcgen05_kernel<BN, STAGES, CG>,
+                                                      kGemmThreads, Layout::SMEM_BYTES);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    out->blocks_per_sm = blocks;
+    if (CG == 1) {
+        out->groups = blocks * sm_count;
+        return static_cast<int>(cudaSuccess);
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_launch(&cfg, attr, sm_count / CG, nullptr);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, gemm_tcgen05_kernel<BN, STAGES, CG>, &cfg);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    out->groups = clusters;
+    return static_cast<int>(cudaSuccess);
+}
+
+template <>
 int launch_gemm_variant<BN, CG>(const CUtensorMap& ta, const CUtensorMap& tb,
                                 const CUtensorMap& tc, const GemmArgs& args, int groups,
                                 cudaStream_t stream) {

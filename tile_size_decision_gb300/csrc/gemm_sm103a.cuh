@@ -84,8 +84,9 @@ struct GemmArgs {
     int32_t tma_store;         // 1: C leaves through TMA stores of staged boxes
     uint32_t idesc;            // tcgen05 instruction descriptor, N = BN
     uint32_t idesc_half;       // the same with N = BN / 2
-    int32_t* err;              // workspace error word, may be null
+    int32_t* err;              // workspace error word
     uint64_t wait_limit_ns;
+    int32_t drop_stage;        // test hook: the first group skips this stage's loads (-1: none)
 };
 
 struct PipeBarriers {
@@ -386,7 +387,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     uint8_t* a_dst = smA + stage * L::A_BYTES;
                     uint8_t* b_dst = smB + stage * L::B_BYTES;
-                    if (ptx::elect_one_sync()) {
+                    // A planted fault (test hook): both CTAs of the first
+                    // group skip the same stage, so its full barrier never
+                    // completes and the MMA issuer's bounded wait expires.
+                    const bool planted = group == 0 && issued == args.drop_stage;
+                    if (!planted && ptx::elect_one_sync()) {
                         if (leader) ptx::mbar_arrive_expect_tx(&bar->full[stage], tx);
                         if constexpr (CG == 1) {
                             ptx::tma_load_3d(a_dst, &tmA, &bar->full[stage], kb * L::BK, row0, uc.b);
@@ -704,6 +709,22 @@ int launch_gemm_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 // Persistent CTA groups that fit on the device at once for a variant.
 template <int BN, int CG>
 int gemm_variant_max_groups(int sm_count);
+
+// What the CUDA runtime reports for one compiled variant on the current
+// device (defined per (BN, CG) in gemm_sm103a.cu).
+struct VariantAttributes {
+    int regs;               // registers per thread
+    int local_bytes;        // local memory per thread (spills)
+    int static_smem;        // static shared memory per block
+    int dynamic_smem;       // dynamic shared memory a launch requests
+    int max_dynamic_smem;   // the opted-in dynamic shared-memory limit
+    int blocks_per_sm;      // resident blocks per SM at that shared memory
+    int groups;             // resident CTA groups (clusters for CTA pairs)
+};
+
+// Fills *out; returns a cudaError_t value.
+template <int BN, int CG>
+int gemm_variant_attributes(int sm_count, VariantAttributes* out);
 
 // Stages compiled for each (BN, CG) (the planner's kGemmVariants agree).
 template <int BN, int CG> struct GemmStages;

@@ -1,13 +1,15 @@
 // Tile-size planner: constraints C0-C4, the sweep and the H-tile rows.
 //
-// Page mode follows the page "04-tile-size-decision/tile_decision.py"
-// (evaluate: C3 -> C1 -> C2 -> occupancy; finish_parallelism: C4;
-// dram_traffic: C0; sweep: enumerate, filter, rank) and its README (C0 with
-// the batch term b).  GB300 mode applies the same constraint order to the
-// sm_103a kernels of this library: C3 becomes the tcgen05 kind::f16 shape
-// and the kernels' tile layout, C2 becomes the tensor-memory (TMEM) column
-// budget of the accumulators, C4 counts waves of persistent CTA groups, and
-// the ranking puts a wave-quantised time estimate before C0.
+// The constraints are those of the page "04-tile-size-decision" (README,
+// "目的" and the four checks it names; the script tile_decision.py fixes the
+// numbers): C3 the MMA instruction shape, C1 on-chip capacity, C2 register
+// pressure, the resident blocks they leave, C4 waves and last-wave fill, C0
+// cache-less DRAM traffic.  Page mode reproduces the page's sweep and ranking
+// bit for bit.  GB300 mode applies the same constraints to the sm_103a
+// kernels of this library: C3 becomes the tcgen05 kind::f16 shape and the
+// kernels' tile layout, C2 becomes the tensor-memory (TMEM) column budget of
+// the accumulators, C4 counts rounds of persistent CTA groups, and the
+// ranking puts a wave-quantised time estimate before C0.
 //
 // Host-only C++; no CUDA here.
 
@@ -15,6 +17,7 @@
 
 #include <algorithm>
 #include <cfenv>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -25,68 +28,79 @@ namespace {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// (M multiple, N multiple, K multiple, thread multiple) of the page's
-// instruction-shape table: mma m16n8k16 (warp), wgmma m64nNk16 (warpgroup),
-// scalar.
-struct InstrMultiples { int m, n, k, t; };
+// The page's instruction-shape table: an MMA family fixes the multiples of
+// the tile's M, N and K edges and of the block's thread count (mma
+// m16n8k16 is issued per warp, wgmma m64nNk16 per warpgroup, scalar code
+// per thread).
+struct ShapeRule { int edge[3]; int threads; };
 
-bool page_multiples(int instr, InstrMultiples* out) {
+bool shape_rule(int instr, ShapeRule* out) {
     switch (instr) {
-        case TILES_INSTR_MMA:   *out = {16, 8, 16, 32}; return true;
-        case TILES_INSTR_WGMMA: *out = {64, 8, 16, 128}; return true;
-        case TILES_INSTR_SIMT:  *out = {1, 1, 1, 32}; return true;
+        case TILES_INSTR_MMA:   *out = {{16, 8, 16}, 32}; return true;
+        case TILES_INSTR_WGMMA: *out = {{64, 8, 16}, 128}; return true;
+        case TILES_INSTR_SIMT:  *out = {{1, 1, 1}, 32}; return true;
         default: return false;
     }
 }
 
-// Occupancy shared by both modes: least of the per-resource block counts,
-// capped by the hardware limit; the binding resource is the first reaching
-// that least value in the order regs, smem, threads (then TMEM in GB300 mode).
-void occupancy(const tiles_device& dev, tiles_verdict* v, bool with_tmem) {
-    v->blocks_by_regs = dev.regs_per_sm / std::max(v->regs_per_block, 1);
-    v->blocks_by_smem = (int32_t)(dev.smem_per_sm / std::max<int64_t>(v->smem_total, 1));
-    v->blocks_by_threads = dev.max_threads_per_sm / std::max(v->cfg.threads, 1);
-    int least = std::min(v->blocks_by_regs, std::min(v->blocks_by_smem, v->blocks_by_threads));
-    if (with_tmem) least = std::min(least, v->blocks_by_tmem);
-    v->blocks_per_sm = std::max(std::min(least, dev.max_blocks_per_sm), 0);
-    v->binding = TILES_BIND_NONE;
+// Residency: for every per-SM resource, how many blocks of this demand the
+// SM can hold; the scarcest resource binds.  The list order settles ties
+// (registers, shared memory, threads, then tensor memory in GB300 mode), and
+// the SM's block limit caps the count without ever being named as binding.
+void settle_residency(const tiles_device& dev, tiles_verdict* v, bool tensor_memory) {
+    struct Resource { int32_t* blocks; int64_t supply, demand; int32_t tag; };
+    const Resource table[] = {
+        {&v->blocks_by_regs, dev.regs_per_sm, v->regs_per_block, TILES_BIND_REGS},
+        {&v->blocks_by_smem, dev.smem_per_sm, v->smem_total, TILES_BIND_SMEM},
+        {&v->blocks_by_threads, dev.max_threads_per_sm, v->cfg.threads, TILES_BIND_THREADS},
+        {&v->blocks_by_tmem, dev.tmem_cols, v->tmem_cols_alloc, TILES_BIND_TMEM},
+    };
+    const int used = tensor_memory ? 4 : 3;
+    int64_t scarcest = INT64_MAX;
+    int32_t tag = TILES_BIND_NONE;
+    for (int i = 0; i < used; ++i) {
+        const int64_t fit = table[i].supply / std::max<int64_t>(table[i].demand, 1);
+        *table[i].blocks = static_cast<int32_t>(fit);
+        if (fit < scarcest) { scarcest = fit; tag = table[i].tag; }
+    }
+    v->blocks_per_sm = static_cast<int32_t>(
+        std::max<int64_t>(std::min<int64_t>(scarcest, dev.max_blocks_per_sm), 0));
     if (v->blocks_per_sm == 0) {
         v->failures |= TILES_FAIL_OCC;
-        return;
+        v->binding = TILES_BIND_NONE;
+    } else {
+        v->binding = tag;
     }
-    if (v->blocks_by_regs == least) v->binding = TILES_BIND_REGS;
-    else if (v->blocks_by_smem == least) v->binding = TILES_BIND_SMEM;
-    else if (v->blocks_by_threads == least) v->binding = TILES_BIND_THREADS;
-    else v->binding = TILES_BIND_TMEM;
 }
 
+// Page mode, one configuration.
 void evaluate_page(const tiles_device& dev, const tiles_config& cfg, int elem_bytes,
                    int accum_bytes, tiles_verdict* v) {
-    InstrMultiples im;
-    page_multiples(cfg.instr, &im);
-    // C3: instruction shape, checked first.
-    int c3 = 0;
-    if (cfg.bm % im.m) ++c3;
-    if (cfg.bn % im.n) ++c3;
-    if (cfg.bk % im.k) ++c3;
-    if (cfg.threads % im.t) ++c3;
-    if (cfg.threads > dev.max_threads_per_block) ++c3;
-    v->c3_violations = c3;
-    if (c3) v->failures |= TILES_FAIL_C3;
-    // C1: A and B slices of one stage, times the pipeline depth.
-    v->smem_per_stage = ((int64_t)cfg.bm * cfg.bk + (int64_t)cfg.bk * cfg.bn) * elem_bytes;
+    ShapeRule rule;
+    shape_rule(cfg.instr, &rule);
+    // C3: each tile edge and the thread count is a whole multiple of the
+    // family's shape, and the block stays within the per-block thread limit;
+    // every broken condition counts once.
+    const int edges[3] = {cfg.bm, cfg.bn, cfg.bk};
+    int broken = cfg.threads % rule.threads != 0;
+    for (int i = 0; i < 3; ++i) broken += edges[i] % rule.edge[i] != 0;
+    broken += cfg.threads > dev.max_threads_per_block;
+    v->c3_violations = broken;
+    if (broken) v->failures |= TILES_FAIL_C3;
+    // C1: a stage holds the A slice (bm x bk) and the B slice (bk x bn); the
+    // pipeline holds `stages` of them, within one block's shared memory.
+    v->smem_per_stage = (int64_t)(cfg.bm + cfg.bn) * cfg.bk * elem_bytes;
     v->smem_total = v->smem_per_stage * cfg.stages;
     if (v->smem_total > dev.smem_per_block_max) v->failures |= TILES_FAIL_C1;
-    // C2: accumulators per thread in 32-bit registers, rounded to the
-    // per-warp allocation granule.
+    // C2: the bm x bn accumulator tile spread over the block's threads, in
+    // 32-bit registers; a warp's registers come in whole allocation granules.
     v->accum_per_thread = (int32_t)ceil_div((int64_t)cfg.bm * cfg.bn, cfg.threads);
-    int64_t words = (int64_t)v->accum_per_thread * accum_bytes / 4;
-    int64_t per_warp = ceil_div(words * dev.warp_size, dev.reg_granularity_per_warp) *
-                       dev.reg_granularity_per_warp;
-    v->regs_per_thread = (int32_t)(per_warp / dev.warp_size);
+    const int64_t lane_words = (int64_t)v->accum_per_thread * accum_bytes / 4;
+    const int64_t granules = ceil_div(lane_words * dev.warp_size, dev.reg_granularity_per_warp);
+    v->regs_per_thread = (int32_t)(granules * dev.reg_granularity_per_warp / dev.warp_size);
     if (v->regs_per_thread > dev.regs_per_thread_max) v->failures |= TILES_FAIL_C2;
     v->regs_per_block = v->regs_per_thread * cfg.threads;
-    occupancy(dev, v, false);
+    settle_residency(dev, v, false);
 }
 
 }  // namespace
@@ -94,7 +108,7 @@ void evaluate_page(const tiles_device& dev, const tiles_config& cfg, int elem_by
 // GB300 kernel variants compiled into this library (bm, bn, cta_group,
 // stages), in enumeration order.  bk is one 128-byte swizzle atom of the
 // input type; the stage count is the deepest pipeline that fits 227 KB next
-// to the epilogue's staging boxes.
+// to the epilogue's staging boxes (at most kMaxStages).
 const KernelVariant kGemmVariants[] = {
     {128, 64, 1, 8}, {128, 128, 1, 6}, {128, 192, 1, 5}, {128, 256, 1, 4},
     {256, 128, 2, 8}, {256, 256, 2, 6},
@@ -103,7 +117,8 @@ const int kNumGemmVariants = sizeof(kGemmVariants) / sizeof(kGemmVariants[0]);
 
 int64_t gb300_smem_bytes(const tiles_config& cfg, int in_bytes, int64_t* per_stage) {
     const int cg = std::max(cfg.cta_group, 1);
-    int64_t stage = ((int64_t)(cfg.bm / cg) * cfg.bk + (int64_t)cfg.bk * (cfg.bn / cg)) * in_bytes;
+    // Each CTA of a group stages its own bm/cg rows of A and bn/cg columns of B.
+    int64_t stage = (int64_t)(cfg.bm / cg + cfg.bn / cg) * cfg.bk * in_bytes;
     if (per_stage) *per_stage = stage;
     return stage * cfg.stages + kSmemEpilogueBytes + kSmemBarrierBytes + kSmemAlignSlack;
 }
@@ -117,23 +132,27 @@ static int pow2_at_least(int x) {
 void evaluate_gb300(const tiles_device& dev, const tiles_config& cfg, int in_bytes,
                     tiles_verdict* v) {
     const int cg = cfg.cta_group;
+    const bool cg_ok = cg == 1 || cg == 2;
+    const int cgs = cg_ok ? cg : 1;
     // C3: tcgen05.mma kind::f16 takes M = 128 rows per CTA (cta_group::1:
     // M 128; ::2: M 256 over the pair), N a multiple of 16 in [16, 256], K 16
     // per instruction.  The kernels add their tile layout: a K block is one
     // 128-byte swizzle atom, B arrives in 64-column atoms per CTA, threads
     // are the 6 warps of the warp-specialised block.
-    int c3 = 0;
-    if (cg != 1 && cg != 2) ++c3;
-    const int cgs = (cg == 1 || cg == 2) ? cg : 1;
-    if (cfg.bm != 128 * cgs) ++c3;
-    if (cfg.bn % 16 || cfg.bn < 16 || cfg.bn > 256) ++c3;
-    if (cfg.bk % 16 || cfg.bk * in_bytes != 128) ++c3;
-    if ((cfg.bn / cgs) % 64) ++c3;
-    if (cfg.threads != kGemmThreads) ++c3;
-    if (cfg.acc_bufs < 1 || cfg.acc_bufs > 2) ++c3;
-    if (cfg.stages < 1 || cfg.stages > kMaxStages) ++c3;
-    v->c3_violations = c3;
-    if (c3) v->failures |= TILES_FAIL_C3;
+    const bool conditions[] = {
+        cg_ok,
+        cfg.bm == 128 * cgs,
+        cfg.bn % 16 == 0 && cfg.bn >= 16 && cfg.bn <= 256,
+        cfg.bk % 16 == 0 && cfg.bk * in_bytes == 128,
+        (cfg.bn / cgs) % 64 == 0,
+        cfg.threads == kGemmThreads,
+        cfg.acc_bufs >= 1 && cfg.acc_bufs <= 2,
+        cfg.stages >= 1 && cfg.stages <= kMaxStages,
+    };
+    int broken = 0;
+    for (bool ok : conditions) broken += !ok;
+    v->c3_violations = broken;
+    if (broken) v->failures |= TILES_FAIL_C3;
     // C1: pipeline stages plus the epilogue's staging boxes, the barriers
     // and the 1 KB alignment slack of the swizzled operand tiles, within the
     // opt-in per-block limit.
@@ -143,14 +162,14 @@ void evaluate_gb300(const tiles_device& dev, const tiles_config& cfg, int in_byt
     if (v->smem_total > dev.smem_per_block_max) v->failures |= TILES_FAIL_C1;
     // C2: the fp32 accumulators live in TMEM, 128 lanes x bn columns per
     // buffer per CTA; the allocation is a power of two of at least 32.
-    int cols = std::max(cfg.acc_bufs, 0) * cfg.bn;
+    const int cols = std::max(cfg.acc_bufs, 0) * cfg.bn;
     v->tmem_cols_alloc = pow2_at_least(std::max(cols, 1));
     if (v->tmem_cols_alloc > dev.tmem_cols) v->failures |= TILES_FAIL_C2;
+    // The kernels' own register figure (not an accumulator count).
     v->accum_per_thread = 0;
     v->regs_per_thread = dev.kernel_regs_per_thread;
     v->regs_per_block = dev.kernel_regs_per_thread * cfg.threads;
-    v->blocks_by_tmem = dev.tmem_cols / std::max(v->tmem_cols_alloc, 1);
-    occupancy(dev, v, true);
+    settle_residency(dev, v, true);
 }
 
 int evaluate(const tiles_device& dev, const tiles_config& cfg, int elem_bytes, int accum_bytes,
@@ -161,8 +180,8 @@ int evaluate(const tiles_device& dev, const tiles_config& cfg, int elem_bytes, i
         evaluate_gb300(dev, cfg, elem_bytes, v);
         return TILES_OK;
     }
-    InstrMultiples im;
-    if (!page_multiples(cfg.instr, &im)) return TILES_ERR_INVALID_ARG;
+    ShapeRule rule;
+    if (!shape_rule(cfg.instr, &rule)) return TILES_ERR_INVALID_ARG;
     evaluate_page(dev, cfg, elem_bytes, accum_bytes, v);
     return TILES_OK;
 }
@@ -170,16 +189,16 @@ int evaluate(const tiles_device& dev, const tiles_config& cfg, int elem_bytes, i
 void finish_parallelism(const tiles_device& dev, int64_t b, int64_t m, int64_t n,
                         tiles_verdict* v) {
     const tiles_config& cfg = v->cfg;
+    // C4: one block per output tile; the tiles run in waves of the blocks
+    // resident at once (never fewer than one, even when none fits).
     v->grid = b * ceil_div(m, cfg.bm) * ceil_div(n, cfg.bn);
-    int64_t resident;
-    if (cfg.instr == TILES_INSTR_TCGEN05) {
-        resident = gb300_resident_groups(dev, *v);
-    } else {
-        resident = std::max<int64_t>((int64_t)v->blocks_per_sm * dev.sm_count, 1);
-    }
+    const int64_t resident =
+        cfg.instr == TILES_INSTR_TCGEN05
+            ? gb300_resident_groups(dev, *v)
+            : std::max<int64_t>((int64_t)v->blocks_per_sm * dev.sm_count, 1);
     v->waves = ceil_div(v->grid, resident);
-    int64_t rem = v->grid % resident;
-    v->last_wave_fill = rem ? (double)rem / (double)resident : 1.0;
+    const int64_t last = v->grid % resident;
+    v->last_wave_fill = last ? (double)last / (double)resident : 1.0;
     v->warnings = 0;
     if (v->waves > 1 && v->last_wave_fill < 0.5) v->warnings |= TILES_WARN_TAIL;
     if (v->grid < dev.sm_count) v->warnings |= TILES_WARN_IDLE;
@@ -187,13 +206,14 @@ void finish_parallelism(const tiles_device& dev, int64_t b, int64_t m, int64_t n
 
 double c0_bytes(int64_t b, int64_t m, int64_t n, int64_t k, int bm, int bn, int in_bytes,
                 int out_bytes) {
-    // Left to right in double, as the page's expression: the integer product
-    // converts once, then multiplies (1/bn + 1/bm); the output term adds.
-    // The products are formed exactly in 128 bits, like Python's integers.
-    const __int128 rd = (__int128)in_bytes * b * m * n * k;
-    const __int128 wr = (__int128)out_bytes * b * m * n;
-    double reads = (double)rd * (1.0 / bn + 1.0 / bm);
-    return reads + (double)wr;
+    // Every tile streams a bm x K panel of A and a K x bn panel of B, so A is
+    // read N/bn times and B M/bm times; C is written once.  The sum is
+    // formed left to right in double, as the page writes it: the integer
+    // product (exact in 128 bits, like Python's integers) converts once and
+    // multiplies (1/bn + 1/bm); the output term adds.
+    const __int128 operand = (__int128)in_bytes * b * m * n * k;
+    const __int128 output = (__int128)out_bytes * b * m * n;
+    return (double)operand * (1.0 / bn + 1.0 / bm) + (double)output;
 }
 
 // Round half to even, as Python's round() on a float.
@@ -232,12 +252,12 @@ int64_t gb300_unit_clocks(const tiles_device& dev, const tiles_config& cfg, int6
 int64_t gb300_reduce_clocks(const tiles_device& dev, const tiles_config& cfg) {
     // One fp32 partial tile per CTA written by a leading part and read back
     // by the last part, plus the hand-off's fixed latency.  The partials
-    // move at kPartialBytesPerClk, not at the operand fill rate: they are
-    // written while every SM stores at once into an L2 full of dirty lines.
-    (void)dev;
+    // move at the device's partial rate, not at the operand fill rate: they
+    // are written while every SM stores at once into an L2 full of dirty
+    // lines.
     const int cg = std::max(cfg.cta_group, 1);
-    return 2 * ceil_div((int64_t)(cfg.bm / cg) * cfg.bn * 4, kPartialBytesPerClk) +
-           kTailHandoffClocks;
+    return 2 * ceil_div((int64_t)(cfg.bm / cg) * cfg.bn * 4, std::max(dev.partial_bytes_per_clk, 1)) +
+           dev.handoff_clocks;
 }
 
 TailChoice gb300_tail_choice(const tiles_device& dev, const tiles_config& cfg, int64_t tiles,
@@ -296,57 +316,81 @@ static int bytes_of(int dtype) {
     }
 }
 
-int plan(const tiles_device& dev, const tiles_problem& p, std::vector<tiles_verdict>* out) {
-    const int in_b = bytes_of(p.in_dtype), out_b = bytes_of(p.out_dtype);
-    if (!in_b || !out_b) return TILES_ERR_UNSUPPORTED_DTYPE;
-    struct Ranked { tiles_verdict v; int64_t c0r; int64_t order; };
-    std::vector<Ranked> kept;
-    int64_t order = 0;
-    if (p.mode == TILES_MODE_PAGES) {
-        InstrMultiples im;
-        if (!page_multiples(p.instr, &im)) return TILES_ERR_INVALID_ARG;
-        static const int BM[] = {16, 32, 64, 128, 256}, BK[] = {16, 32, 64, 128};
-        static const int ST[] = {2, 3, 4}, TH[] = {128, 256, 512};
-        for (int bm : BM) for (int bn : BM) for (int bk : BK) {
-            if (bk > p.k) continue;
-            for (int st : ST) for (int th : TH) {
-                if (th % im.t) continue;
-                tiles_config c{};
-                c.bm = bm; c.bn = bn; c.bk = bk; c.stages = st; c.threads = th; c.instr = p.instr;
-                tiles_verdict v;
-                evaluate(dev, c, in_b, 4, &v);
-                if (v.failures) continue;
-                finish_parallelism(dev, p.b, p.m, p.n, &v);
-                v.c0_bytes = c0_bytes(p.b, p.m, p.n, p.k, bm, bn, in_b, out_b);
-                kept.push_back({v, round_even(v.c0_bytes), order++});
-            }
-        }
-        std::stable_sort(kept.begin(), kept.end(), [](const Ranked& a, const Ranked& b) {
-            if (a.c0r != b.c0r) return a.c0r < b.c0r;
-            if (a.v.blocks_per_sm != b.v.blocks_per_sm) return a.v.blocks_per_sm > b.v.blocks_per_sm;
-            return a.v.smem_total < b.v.smem_total;
-        });
-    } else if (p.mode == TILES_MODE_GB300) {
-        if (in_b != 2) return TILES_ERR_UNSUPPORTED_DTYPE;
-        for (int i = 0; i < kNumGemmVariants; ++i) {
-            const KernelVariant& kv = kGemmVariants[i];
+namespace {
+
+// A feasible verdict with its rank key: the rounded C0 and its place in the
+// enumeration (ties keep that order).
+struct Ranked { tiles_verdict v; int64_t c0r; };
+
+// Page mode: the candidate grid of the page's sweep (bm, bn over 16..256,
+// bk over 16..128 but not beyond K, 2-4 stages, 128/256/512 threads, the
+// innermost varying fastest), feasible ones only.
+void sweep_page(const tiles_device& dev, const tiles_problem& p, int in_b, int out_b,
+                const ShapeRule& rule, std::vector<Ranked>* kept) {
+    static const int kEdges[] = {16, 32, 64, 128, 256};
+    static const int kDepths[] = {16, 32, 64, 128};
+    static const int kStages[] = {2, 3, 4};
+    static const int kThreads[] = {128, 256, 512};
+    for (int bm : kEdges) for (int bn : kEdges) for (int bk : kDepths) {
+        if (bk > p.k) continue;
+        for (int st : kStages) for (int th : kThreads) {
+            if (th % rule.threads) continue;
             tiles_config c{};
-            c.bm = kv.bm; c.bn = kv.bn; c.bk = 128 / in_b; c.threads = kGemmThreads;
-            c.instr = TILES_INSTR_TCGEN05; c.acc_bufs = 2; c.cta_group = kv.cta_group;
-            c.stages = kv.stages;
+            c.bm = bm; c.bn = bn; c.bk = bk; c.stages = st; c.threads = th; c.instr = p.instr;
             tiles_verdict v;
             evaluate(dev, c, in_b, 4, &v);
             if (v.failures) continue;
             finish_parallelism(dev, p.b, p.m, p.n, &v);
-            v.c0_bytes = c0_bytes(p.b, p.m, p.n, p.k, c.bm, c.bn, in_b, out_b);
-            v.est_clocks = gb300_est_clocks(dev, &v, p.k);
-            kept.push_back({v, round_even(v.c0_bytes), order++});
+            v.c0_bytes = c0_bytes(p.b, p.m, p.n, p.k, bm, bn, in_b, out_b);
+            kept->push_back({v, round_even(v.c0_bytes)});
         }
-        std::stable_sort(kept.begin(), kept.end(), [](const Ranked& a, const Ranked& b) {
+    }
+}
+
+// GB300 mode: the compiled kernel variants, feasible ones only.
+void sweep_gb300(const tiles_device& dev, const tiles_problem& p, int in_b, int out_b,
+                 std::vector<Ranked>* kept) {
+    for (int i = 0; i < kNumGemmVariants; ++i) {
+        const KernelVariant& kv = kGemmVariants[i];
+        tiles_config c{};
+        c.bm = kv.bm; c.bn = kv.bn; c.bk = 128 / in_b; c.threads = kGemmThreads;
+        c.instr = TILES_INSTR_TCGEN05; c.acc_bufs = 2; c.cta_group = kv.cta_group;
+        c.stages = kv.stages;
+        tiles_verdict v;
+        evaluate(dev, c, in_b, 4, &v);
+        if (v.failures) continue;
+        finish_parallelism(dev, p.b, p.m, p.n, &v);
+        v.c0_bytes = c0_bytes(p.b, p.m, p.n, p.k, c.bm, c.bn, in_b, out_b);
+        v.est_clocks = gb300_est_clocks(dev, &v, p.k);
+        kept->push_back({v, round_even(v.c0_bytes)});
+    }
+}
+
+}  // namespace
+
+int plan(const tiles_device& dev, const tiles_problem& p, std::vector<tiles_verdict>* out) {
+    const int in_b = bytes_of(p.in_dtype), out_b = bytes_of(p.out_dtype);
+    if (!in_b || !out_b) return TILES_ERR_UNSUPPORTED_DTYPE;
+    std::vector<Ranked> kept;
+    // The page's design order: least traffic first, then more resident
+    // blocks, then less shared memory.  GB300 mode puts the time estimate
+    // in front.
+    auto traffic_first = [](const Ranked& a, const Ranked& b) {
+        if (a.c0r != b.c0r) return a.c0r < b.c0r;
+        if (a.v.blocks_per_sm != b.v.blocks_per_sm) return a.v.blocks_per_sm > b.v.blocks_per_sm;
+        return a.v.smem_total < b.v.smem_total;
+    };
+    if (p.mode == TILES_MODE_PAGES) {
+        ShapeRule rule;
+        if (!shape_rule(p.instr, &rule)) return TILES_ERR_INVALID_ARG;
+        sweep_page(dev, p, in_b, out_b, rule, &kept);
+        std::stable_sort(kept.begin(), kept.end(), traffic_first);
+    } else if (p.mode == TILES_MODE_GB300) {
+        if (in_b != 2) return TILES_ERR_UNSUPPORTED_DTYPE;
+        sweep_gb300(dev, p, in_b, out_b, &kept);
+        std::stable_sort(kept.begin(), kept.end(), [&](const Ranked& a, const Ranked& b) {
             if (a.v.est_clocks != b.v.est_clocks) return a.v.est_clocks < b.v.est_clocks;
-            if (a.c0r != b.c0r) return a.c0r < b.c0r;
-            if (a.v.blocks_per_sm != b.v.blocks_per_sm) return a.v.blocks_per_sm > b.v.blocks_per_sm;
-            return a.v.smem_total < b.v.smem_total;
+            return traffic_first(a, b);
         });
     } else {
         return TILES_ERR_INVALID_ARG;
@@ -377,6 +421,8 @@ void device_preset_gb300(tiles_device* d) {
     d->mma_flops_per_clk = 8192;
     d->fill_bytes_per_clk = kDefaultFillBytesPerClk;
     d->kernel_regs_per_thread = kGemmRegsPerThread;
+    d->partial_bytes_per_clk = kPartialBytesPerClk;
+    d->handoff_clocks = kTailHandoffClocks;
 }
 
 int htile_rows(int H, int kh, int sh, int pt, int d, int o0, int o1, tiles_htile* t) {

@@ -11,9 +11,10 @@ namespace tiles {
 // Threads of the warp-specialised GEMM block: warp 0 TMA producer, warp 1
 // MMA issuer and TMEM owner, warps 2-5 epilogue.
 constexpr int kGemmThreads = 192;
-// Registers per thread of the GEMM kernels as built (ptxas reports up to
-// 164, which the per-warp granule of 256 rounds to 168); the planner's
-// occupancy uses this figure.
+// Registers per thread of the GEMM kernels in the GB300 preset (the
+// device model used without a GPU).  On a GPU, tiles_device_query replaces
+// it with the largest register count the runtime reports for a compiled
+// variant, rounded up to the per-warp allocation granule.
 constexpr int kGemmRegsPerThread = 168;
 // Shared memory beyond the operand stages: mbarriers, the TMEM address slot,
 // an abort flag (kSmemBarrierBytes) and the slack that lets the operand
@@ -60,12 +61,14 @@ int64_t gb300_reduce_clocks(const tiles_device& dev, const tiles_config& cfg);
 struct TailChoice { int mode; int parts; int64_t clocks; };
 TailChoice gb300_tail_choice(const tiles_device& dev, const tiles_config& cfg, int64_t tiles,
                              int64_t resident, int64_t k_blocks, int in_bytes, int forced);
-// Fixed clocks of a K-part hand-off (flag release, acquire, copy latency).
+// GB300 preset values of the time model's K-split hand-off (the device
+// record's handoff_clocks and partial_bytes_per_clk): fixed clocks of one
+// hand-off (flag release, acquire, copy latency), and the bytes per clock
+// per SM at which a K part writes or reads its fp32 partial tile.  The rate
+// was measured on the 4096^3 GEMM after an L2-flushing write: a CTA's
+// 128 KB partial took ~5,300 clocks out (~25 B/clk) whether written as
+// 4-byte or 16-byte lane stores.
 constexpr int64_t kTailHandoffClocks = 2048;
-// Bytes per clock per SM at which a K part writes or reads its fp32
-// partial tile.  Measured on the 4096^3 GEMM after an L2-flushing write:
-// a CTA's 128 KB partial took ~5,300 clocks out (~25 B/clk) whether written
-// as 4-byte or 16-byte lane stores.
 constexpr int64_t kPartialBytesPerClk = 32;
 constexpr int kMaxTailParts = 8;
 void device_preset_h100(tiles_device* d);
@@ -75,6 +78,21 @@ int conv2d_tiled(const tiles_conv_desc* desc, int tile_oh, int tile_ow, int tile
                  const tiles_config* cfg, void* ws, size_t ws_bytes, void* stream);
 int conv2d_htiled(const tiles_conv_desc* desc, int tile_oh, const tiles_config* cfg, void* ws,
                   size_t ws_bytes, void* stream);
+// Output height and width of a convolution descriptor (INVALID_ARG when a
+// size is out of range or no window fits).
+int conv_out_hw(const tiles_conv_desc* d, int64_t* oh, int64_t* ow);
+
+// Smallest workspace a kernel call accepts: the 256-byte header whose first
+// word records a bounded wait's expiry (tiles_workspace_bytes).
+constexpr int kConvMinWorkspaceBytes = 256;
+
+// A fault planted for the bounded-wait tests (tiles_selftest_drop_stage):
+// the first CTA (group) of the next GEMM or convolution launch from this
+// thread skips the loads and the arrival of its `stage`-th pipeline stage,
+// and every wait of that launch gives up after limit_ns.  stage < 0: none.
+struct PlantedFault { int32_t stage; uint64_t limit_ns; };
+// Takes the calling thread's armed fault, leaving none armed.
+PlantedFault take_planted_fault();
 
 // Per-thread error text (tiles_last_error).
 int fail(int status, const char* fmt, ...);

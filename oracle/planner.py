@@ -1,38 +1,50 @@
 """Tile-size constraint procedure, page mode (oracle; test infrastructure only).
 
-Restates, step by step, the checks of the page
-"04-tile-size-decision/tile_decision.py" (sections: ``Device``, ``Config``,
-``Verdict`` records; ``INSTR_SHAPES``; ``evaluate``; ``finish_parallelism``;
-``dram_traffic``; ``sweep``; ``main``) and the README on the same site
-("目的" block: C0 = b*M*N*K*(1/block_N + 1/block_M) + b*M*N).
+Source: the page "04-tile-size-decision" (its README's "目的" block and the
+four checks it names, whose numbers the page's script tile_decision.py and
+its printed outputs fix).  A GEMM tile (bm x bn, K step bk, a pipeline of
+`stages`, a block of `threads`) is checked against
 
-Order of the checks, as on the page:
-  C3 instruction shape -> C1 on-chip capacity -> C2 register pressure ->
-  occupancy and the binding resource -> C4 waves and last-wave fill -> C0 DRAM
-  traffic -> sweep, filter, sort.
+  C3  the MMA instruction shape: the tile edges and the thread count are
+      whole multiples of the MMA family's shape, within the block limit;
+  C1  on-chip capacity: `stages` copies of the A and B slices fit one
+      block's shared memory;
+  C2  register pressure: the accumulator tile, spread over the threads and
+      rounded to the per-warp register granule, fits the per-thread limit;
+then the resident blocks per SM follow from the scarcest of registers,
+shared memory and threads, and
 
-Page quirks kept on purpose (each is observable in the page's printed output):
-  * C2 counts accumulators only and rounds to 256 registers per warp.
-  * blocks_by_smem divides by shared memory per SM (not per block).
-  * With 0 blocks per SM the resident count is clamped to 1, so waves = grid.
-  * The binding label is the first minimum in the order regs, smem, threads.
-  * The sort key is (round(C0), -blocks_per_sm, smem_total), stable over the
-    enumeration order bm, bn, bk, stages, threads.
+  C4  waves: the tiles run in waves of the resident blocks; a last wave
+      under half full is a tail warning, fewer tiles than SMs an idle one;
+  C0  DRAM traffic without caches: every tile streams its panels of A and B
+      once, C is written once:
+          C0 = in_bytes*b*M*N*K*(1/bn + 1/bm) + out_bytes*b*M*N
 
-Readings where the pages are silent:
-  * C0 with a batch b and separate input/output widths:
-        in_bytes*b*M*N*K*(1/bn + 1/bm) + out_bytes*b*M*N
-    evaluated left to right in IEEE float64; with b=1 and in=out=elem this is
-    the page's own expression.
-  * ceil(M/bm) is the exact integer ceiling; the page's float ceiling equals
-    it for every block size below 2**22.
+A sweep over the page's candidate grid keeps the feasible tiles and ranks
+them by least traffic, then most resident blocks, then least shared memory.
+
+The page's numbers carry some conventions that its printed outputs make
+observable, and that are kept here:
+  * C2 counts the accumulators alone (no other registers).
+  * Blocks by shared memory divide the per-SM capacity, not the per-block one.
+  * With no resident block the resident count is taken as 1, so waves = tiles.
+  * The binding resource is the first scarcest in the order regs, smem,
+    threads; the 32-block hardware cap never binds by name.
+  * Traffic ranks by Python's round() (half to even) of the float64 C0, and
+    ties keep the enumeration order (bm, bn, bk, stages, threads ascending).
+
+Readings where the page is silent: C0 takes a batch b and separate input and
+output widths (the README's formula has b; with b=1 and equal widths it is
+the script's own expression), evaluated left to right in IEEE float64; the
+tile counts use exact integer ceilings.
 """
 
 from __future__ import annotations
 
+import itertools
 from dataclasses import dataclass, field
 
-# Failure tags (the page writes them as message prefixes).
+# Failure tags (the page prints them as message prefixes).
 C1 = "C1"
 C2 = "C2"
 C3 = "C3"
@@ -42,9 +54,9 @@ OCC = "C1/C2"
 W_TAIL = "C4-tail"
 W_IDLE = "C4-idle"
 
-# (M multiple, N multiple, K multiple, thread multiple) per MMA family, from
-# the page's instruction-shape table (mma m16n8k16 warp-level, wgmma m64nNk16
-# warpgroup-level, scalar).
+# The page's instruction-shape table: the multiples of (M edge, N edge, K
+# step, threads) for warp-level mma m16n8k16, warpgroup-level wgmma
+# m64nNk16, and scalar code.
 INSTR_MULTIPLES = {
     "mma": (16, 8, 16, 32),
     "wgmma": (64, 8, 16, 128),
@@ -54,7 +66,7 @@ INSTR_MULTIPLES = {
 
 @dataclass(frozen=True)
 class DeviceModel:
-    """Hardware parameters of the page's ``Device`` record (H100/H200 defaults)."""
+    """The page's hardware parameters (H100/H200 defaults)."""
 
     smem_per_sm: int = 228 * 1024
     smem_per_block_max: int = 227 * 1024
@@ -69,8 +81,8 @@ class DeviceModel:
 
 
 def cli_device(sm_count: int = 132, smem_kb: int = 228) -> DeviceModel:
-    """The device the page's command line builds: per-block shared memory is
-    the per-SM figure minus 1 KB."""
+    """The device the page's command line describes: its --smem-kb is per SM,
+    and one block may use all of it but 1 KB."""
     return DeviceModel(sm_count=sm_count, smem_per_sm=smem_kb * 1024,
                        smem_per_block_max=smem_kb * 1024 - 1024)
 
@@ -114,85 +126,70 @@ def ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-def check_instruction_shape(v: Verdict, dev: DeviceModel) -> None:
-    """C3: every tile edge and the thread count are multiples of the MMA shape;
-    the block may not exceed the per-block thread limit."""
-    cfg = v.cfg
-    mm, nm, km, tm = INSTR_MULTIPLES[cfg.instr]
-    for value, mult in ((cfg.bm, mm), (cfg.bn, nm), (cfg.bk, km), (cfg.threads, tm)):
-        if value % mult:
-            v.failures.append(C3)
-    if cfg.threads > dev.max_threads_per_block:
-        v.failures.append(C3)
+def shape_violations(cfg: TileConfig, dev: DeviceModel) -> int:
+    """C3: how many of the shape conditions the configuration breaks (each
+    tile edge and the thread count a multiple of the MMA family's shape; no
+    more threads than a block may have)."""
+    multiples = INSTR_MULTIPLES[cfg.instr]
+    values = (cfg.bm, cfg.bn, cfg.bk, cfg.threads)
+    broken = sum(1 for value, mult in zip(values, multiples) if value % mult)
+    return broken + (cfg.threads > dev.max_threads_per_block)
 
 
-def check_capacity(v: Verdict, dev: DeviceModel, elem_bytes: int) -> None:
-    """C1: one stage holds a bm x bk slice of A and a bk x bn slice of B; the
-    pipeline keeps `stages` of them; the total must fit one block's smem."""
-    cfg = v.cfg
-    v.smem_per_stage = (cfg.bm * cfg.bk + cfg.bk * cfg.bn) * elem_bytes
-    v.smem_total = v.smem_per_stage * cfg.stages
-    if v.smem_total > dev.smem_per_block_max:
-        v.failures.append(C1)
-
-
-def check_registers(v: Verdict, dev: DeviceModel, accum_bytes: int) -> None:
-    """C2: the bm x bn accumulator spread over the block's threads, counted in
-    32-bit registers and rounded up to the per-warp allocation granule."""
-    cfg = v.cfg
-    v.accum_per_thread = ceil_div(cfg.bm * cfg.bn, cfg.threads)
-    words = v.accum_per_thread * accum_bytes // 4
-    per_warp = ceil_div(words * dev.warp_size, dev.reg_granularity_per_warp) \
+def accumulator_registers(cfg: TileConfig, dev: DeviceModel, accum_bytes: int):
+    """C2: (accumulators per thread, 32-bit registers per thread once a
+    warp's share is rounded up to whole allocation granules)."""
+    per_thread = ceil_div(cfg.bm * cfg.bn, cfg.threads)
+    lane_words = per_thread * accum_bytes // 4
+    warp_regs = ceil_div(lane_words * dev.warp_size, dev.reg_granularity_per_warp) \
         * dev.reg_granularity_per_warp
-    v.regs_per_thread = per_warp // dev.warp_size
-    if v.regs_per_thread > dev.regs_per_thread_max:
-        v.failures.append(C2)
-    v.regs_per_block = v.regs_per_thread * cfg.threads
+    return per_thread, warp_regs // dev.warp_size
 
 
-def occupancy(v: Verdict, dev: DeviceModel) -> None:
-    """Resident blocks per SM: the least of what registers, shared memory and
-    threads allow, capped by the hardware block limit.  The binding resource
-    is the first of regs, smem, threads that reaches that least value."""
-    cfg = v.cfg
-    v.blocks_by_regs = dev.regs_per_sm // max(v.regs_per_block, 1)
-    v.blocks_by_smem = dev.smem_per_sm // max(v.smem_total, 1)
-    v.blocks_by_threads = dev.max_threads_per_sm // max(cfg.threads, 1)
-    least = min(v.blocks_by_regs, v.blocks_by_smem, v.blocks_by_threads)
-    v.blocks_per_sm = max(min(least, dev.max_blocks_per_sm), 0)
-    if v.blocks_per_sm == 0:
-        v.failures.append(OCC)
-        return
-    for name, count in (("regs", v.blocks_by_regs), ("smem", v.blocks_by_smem),
-                        ("threads", v.blocks_by_threads)):
-        if count == least:
-            v.binding = name
-            break
+def residency(regs_per_block: int, smem_per_block: int, threads: int, dev: DeviceModel):
+    """Blocks one SM holds by each resource, the resident count (the scarcest,
+    capped by the block limit) and the binding resource ("" when none fits)."""
+    fits = {
+        "regs": dev.regs_per_sm // max(regs_per_block, 1),
+        "smem": dev.smem_per_sm // max(smem_per_block, 1),
+        "threads": dev.max_threads_per_sm // max(threads, 1),
+    }
+    scarcest = min(fits.values())
+    resident = max(min(scarcest, dev.max_blocks_per_sm), 0)
+    binding = next(name for name, n in fits.items() if n == scarcest) if resident else ""
+    return fits, resident, binding
 
 
 def evaluate(cfg: TileConfig, dev: DeviceModel, elem_bytes: int = 2,
              accum_bytes: int = 4) -> Verdict:
-    """C3, C1, C2 and occupancy for one configuration, in the page's order."""
+    """C3, C1 and C2 for one configuration, then its residency."""
     v = Verdict(cfg=cfg)
-    check_instruction_shape(v, dev)
-    check_capacity(v, dev, elem_bytes)
-    check_registers(v, dev, accum_bytes)
-    occupancy(v, dev)
+    v.failures += [C3] * shape_violations(cfg, dev)
+    # C1: a stage holds the A slice (bm x bk) and the B slice (bk x bn).
+    v.smem_per_stage = (cfg.bm + cfg.bn) * cfg.bk * elem_bytes
+    v.smem_total = v.smem_per_stage * cfg.stages
+    if v.smem_total > dev.smem_per_block_max:
+        v.failures.append(C1)
+    v.accum_per_thread, v.regs_per_thread = accumulator_registers(cfg, dev, accum_bytes)
+    if v.regs_per_thread > dev.regs_per_thread_max:
+        v.failures.append(C2)
+    v.regs_per_block = v.regs_per_thread * cfg.threads
+    fits, v.blocks_per_sm, v.binding = residency(v.regs_per_block, v.smem_total, cfg.threads, dev)
+    v.blocks_by_regs, v.blocks_by_smem, v.blocks_by_threads = \
+        fits["regs"], fits["smem"], fits["threads"]
+    if v.blocks_per_sm == 0:
+        v.failures.append(OCC)
     return v
 
 
 def finish_parallelism(v: Verdict, m: int, n: int, dev: DeviceModel, b: int = 1) -> Verdict:
-    """C4: output tiles, waves over the resident blocks, last-wave fill.
-
-    ``b`` multiplies the tile count (a batch of independent GEMMs); b=1 is the
-    page.  Fill is 1.0 when the tiles divide the resident count exactly.
-    """
-    cfg = v.cfg
-    v.grid = b * ceil_div(m, cfg.bm) * ceil_div(n, cfg.bn)
+    """C4: the output tiles (times the batch b) in waves of the resident
+    blocks; the fill of the last wave is 1.0 when the waves come out even."""
+    v.grid = b * ceil_div(m, v.cfg.bm) * ceil_div(n, v.cfg.bn)
     resident = max(v.blocks_per_sm * dev.sm_count, 1)
     v.waves = ceil_div(v.grid, resident)
-    rem = v.grid % resident
-    v.last_wave_fill = rem / resident if rem else 1.0
+    leftover = v.grid % resident
+    v.last_wave_fill = leftover / resident if leftover else 1.0
     if v.waves > 1 and v.last_wave_fill < 0.5:
         v.warnings.append(W_TAIL)
     if v.grid < dev.sm_count:
@@ -202,21 +199,29 @@ def finish_parallelism(v: Verdict, m: int, n: int, dev: DeviceModel, b: int = 1)
 
 def c0_bytes(m: int, n: int, k: int, bm: int, bn: int, in_bytes: int = 2,
              out_bytes: int | None = None, b: int = 1) -> float:
-    """C0: cache-less DRAM traffic of the tiled GEMM.
-
-    Every output tile streams a bm x K panel of A and a K x bn panel of B, so
-    A is read ceil-free N/bn times and B M/bm times; C is written once.
-    """
+    """C0: cache-less DRAM traffic of the tiled GEMM: A is streamed N/bn
+    times and B M/bm times (no ceilings), C written once."""
     if out_bytes is None:
         out_bytes = in_bytes
     return in_bytes * b * m * n * k * (1 / bn + 1 / bm) + out_bytes * b * m * n
 
 
+# The page's candidate grid.
 SWEEP_BM = (16, 32, 64, 128, 256)
 SWEEP_BN = (16, 32, 64, 128, 256)
 SWEEP_BK = (16, 32, 64, 128)
 SWEEP_STAGES = (2, 3, 4)
 SWEEP_THREADS = (128, 256, 512)
+
+
+def candidates(k: int, instr: str):
+    """Configurations of the page's grid in its enumeration order: K steps
+    beyond K and thread counts off the family's multiple are left out."""
+    tmult = INSTR_MULTIPLES[instr][3]
+    for bm, bn, bk, stages, threads in itertools.product(SWEEP_BM, SWEEP_BN, SWEEP_BK,
+                                                         SWEEP_STAGES, SWEEP_THREADS):
+        if bk <= k and threads % tmult == 0:
+            yield TileConfig(bm, bn, bk, stages, threads, instr)
 
 
 @dataclass
@@ -226,39 +231,25 @@ class SweepResult:
     best_fill: float        # the largest last-wave fill among them
 
 
+def rank_key(v: Verdict):
+    """Least traffic, then most resident blocks, then least shared memory."""
+    return (round(v.c0_bytes), -v.blocks_per_sm, v.smem_total)
+
+
 def sweep(m: int, n: int, k: int, dev: DeviceModel, instr: str = "wgmma", b: int = 1,
           in_bytes: int = 2, out_bytes: int | None = None) -> SweepResult:
-    """Enumerate the page's candidate grid, keep the feasible ones, rank them.
-
-    Ranking: least rounded C0 first, then more resident blocks, then less
-    shared memory; ties keep the enumeration order (bm, bn, bk, stages,
-    threads, each ascending).  Python's round() rounds half to even.
-    b, in_bytes and out_bytes extend C0 and C4 as the README's C0 does; the
-    defaults are the page's sweep.
-    """
-    tmult = INSTR_MULTIPLES[instr][3]
+    """The feasible configurations of the page's grid, ranked (a stable sort,
+    so ties keep the enumeration order)."""
     kept = []
-    for bm in SWEEP_BM:
-        for bn in SWEEP_BN:
-            for bk in SWEEP_BK:
-                if bk > k:
-                    continue
-                for stages in SWEEP_STAGES:
-                    for threads in SWEEP_THREADS:
-                        if threads % tmult:
-                            continue
-                        v = evaluate(TileConfig(bm, bn, bk, stages, threads, instr), dev,
-                                     elem_bytes=in_bytes)
-                        if not v.feasible:
-                            continue
-                        finish_parallelism(v, m, n, dev, b)
-                        v.c0_bytes = c0_bytes(m, n, k, bm, bn, in_bytes, out_bytes, b)
-                        kept.append(v)
-    kept.sort(key=lambda v: (round(v.c0_bytes), -v.blocks_per_sm, v.smem_total))
-    if kept:
-        best = round(kept[0].c0_bytes)
-        tied = sum(1 for v in kept if round(v.c0_bytes) == best)
-        fill = max(v.last_wave_fill for v in kept)
-    else:
-        tied, fill = 0, 0.0
-    return SweepResult(kept, tied, fill)
+    for cfg in candidates(k, instr):
+        v = evaluate(cfg, dev, elem_bytes=in_bytes)
+        if v.feasible:
+            finish_parallelism(v, m, n, dev, b)
+            v.c0_bytes = c0_bytes(m, n, k, cfg.bm, cfg.bn, in_bytes, out_bytes, b)
+            kept.append(v)
+    kept.sort(key=rank_key)
+    if not kept:
+        return SweepResult(kept, 0, 0.0)
+    best = round(kept[0].c0_bytes)
+    tied = sum(round(v.c0_bytes) == best for v in kept)
+    return SweepResult(kept, tied, max(v.last_wave_fill for v in kept))

@@ -3,9 +3,13 @@
 Three kinds of pin:
   * values the pages print (tests/golden/planner_pages.json, each cited);
   * closed forms from the tiling tutorial (capacity, registers, intensity);
-  * a differential run of the page's own script, read at test time from the
-    mounted pages (skipped where they are absent), over a grid of shapes,
-    devices and instruction families.  Nothing of the script is stored here.
+  * opt-in: a differential run of the page's own script over a grid of
+    shapes, devices and instruction families.  The page text is third-party
+    content from the open web, so the run happens only when the variable
+    TILES_PAGES_DIR names a directory holding the page text, and then in an
+    isolated interpreter (python -I -S: no site packages, no user paths, no
+    environment) in a scratch directory, with a time limit.  Nothing of the
+    script is stored here.
 """
 
 import json
@@ -20,7 +24,8 @@ from oracle import planner as P
 from oracle import gemm as G
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "planner_pages.json")
-PAGES_DIR = "/root/reference"   # read-only mount of the source pages
+# Directory of the source pages' text, for the opt-in differential run.
+PAGES_ENV = "TILES_PAGES_DIR"
 
 
 @pytest.fixture(scope="module")
@@ -162,13 +167,16 @@ def test_binding_order_prefers_regs_on_ties():
 # --------------------------------------------------------------------------- #
 
 def _pages_lines():
-    """Lines of the mounted page text that prints the planner script."""
-    if not os.path.isdir(PAGES_DIR):
-        pytest.skip("source pages not mounted")
-    for name in sorted(os.listdir(PAGES_DIR)):
+    """Lines of the page text that prints the planner script."""
+    pages = os.environ.get(PAGES_ENV, "")
+    if not pages:
+        pytest.skip(f"opt-in: set {PAGES_ENV} to the directory of the source pages' text")
+    if not os.path.isdir(pages):
+        pytest.skip(f"{PAGES_ENV}={pages!r} is not a directory")
+    for name in sorted(os.listdir(pages)):
         if not name.endswith(".md"):
             continue
-        with open(os.path.join(PAGES_DIR, name), encoding="utf-8") as f:
+        with open(os.path.join(pages, name), encoding="utf-8") as f:
             lines = f.read().split("\n")
         if any(l.startswith("#!/usr/bin/env python3") for l in lines):
             return lines
@@ -191,8 +199,11 @@ def page_script(tmp_path_factory):
 
 
 def run_script(path, *args):
-    out = subprocess.run([sys.executable, "-I", path, *map(str, args)], capture_output=True,
-                         text=True, timeout=120)
+    # Isolated interpreter, empty environment, the script's own scratch
+    # directory as the working directory, bounded time.
+    out = subprocess.run([sys.executable, "-I", "-S", path, *map(str, args)],
+                         capture_output=True, text=True, timeout=120, env={},
+                         cwd=os.path.dirname(path))
     assert out.returncode == 0, out.stderr
     return out.stdout
 

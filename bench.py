@@ -80,6 +80,8 @@ def parse():
                          "the other four workloads")
     ap.add_argument("--sustained-seconds", type=float, default=2.5,
                     help="length of the sustained back-to-back leg")
+    ap.add_argument("--workload-sustained-seconds", type=float, default=0.8,
+                    help="length of each further workload's back-to-back leg (its clock record)")
     ap.add_argument("--e2e-chunks", type=int, default=4, metavar="P",
                     help="pieces of the end-to-end call (uploads, kernels, downloads overlap)")
     ap.add_argument("--autotune", type=int, default=4, metavar="K",
@@ -568,11 +570,15 @@ def sustained_leg(job, stream, seconds, gpu_index, peaks, src):
     tflops = job.flops * n / (total_ms * 1e-3) / 1e12
     clk = sampler.summary(t0, t1)
     out = {"launches": n, "seconds": round(total_ms / 1e3, 3), "us_per_launch": round(us, 3),
-           "tflops": round(tflops, 2),
-           "frac_of_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
-           "frac_of_burst": round(tflops / peaks["bf16_tflops"], 4),
-           "peak_source": f"{src} bf16 sustained (a seconds-long loop under the power cap)",
-           "clocks": clk}
+           "tflops": round(tflops, 2), "clocks": clk}
+    if job.bound == "tensor":
+        out.update({"frac_of_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
+                    "frac_of_burst": round(tflops / peaks["bf16_tflops"], 4),
+                    "peak_source": f"{src} bf16 sustained (a seconds-long loop under the power cap)"})
+    else:
+        gbs = job.bytes * n / (total_ms * 1e-3) / 1e9
+        out.update({"gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                    "peak_source": f"{src} HBM copy bandwidth (back to back, L2 warm between launches)"})
     if clk["sm_mhz"]:
         # Time x clock: the cycles one launch takes at the clock it ran at.
         out["kcycles_per_launch"] = round(us * clk["sm_mhz"] / 1e3, 1)
@@ -606,6 +612,10 @@ def workload_entry(name, args, dev, tiles, torch, stream, flush, peaks, src, gpu
     warm, _ = timed_steps(job, stream, flush, n, warm=True)
     sampler.stop()
     tiles.check(job.ws, stream)
+    # A short back-to-back leg under load: its clock samples are the
+    # workload's clock record (the flushed steps last milliseconds).
+    busy = sustained_leg(job, stream, args.workload_sustained_seconds, gpu_index, peaks, src)
+    tiles.check(job.ws, stream)
     mean = float(np.mean(ms))
     entry.update({
         "value": round(job.flops / (mean * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -614,7 +624,9 @@ def workload_entry(name, args, dev, tiles, torch, stream, flush, peaks, src, gpu
             job.flops / (float(np.median(warm)) * 1e-3) / 1e12, 2)),
         "roofline": roofline(job, mean, peaks, src, name),
         "gpu_launches": n * job.launches,
-        "clocks": dict(sampler.summary(t0, t1), whole_leg=sampler.summary()),
+        "clocks": busy["clocks"],
+        "clocks_flushed_steps": dict(sampler.summary(t0, t1), whole_leg=sampler.summary()),
+        "sustained": {key: val for key, val in busy.items() if key != "clocks"},
     })
     if not args.no_cpu_baseline:
         tf, secs, _, desc = job.oracle(args.extra_cpu_seconds)

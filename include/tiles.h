@@ -113,7 +113,9 @@ typedef struct {
                                          fp32 partial tile (0 counts as 1) */
     int32_t handoff_clocks;           /* GB300 time model: fixed clocks of one K-part
                                          hand-off (flag release, acquire, latency) */
-    int32_t reserved[1];
+    int32_t pair_launch_clocks;       /* GB300 time model: the extra fixed clocks of a launch
+                                         of the CTA-pair kernels (cluster launch, the pair's
+                                         prologue and last epilogue) over one-CTA kernels */
 } tiles_device;
 
 /* One tile configuration (the page's Config record plus GB300 fields). */
@@ -182,7 +184,8 @@ typedef struct {
     double c0_bytes;             /* C0, float64 as on the page */
     int64_t est_clocks;          /* GB300 time model (0 in page mode): whole rounds of
                                     ceil(K/bk) K blocks of max(MMA, fill) clocks,
-                                    then the last round in its cheapest schedule */
+                                    then the last round in its cheapest schedule, plus
+                                    pair_launch_clocks for a CTA-pair kernel */
 } tiles_verdict;
 
 /* A planning request. */

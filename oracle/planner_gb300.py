@@ -12,9 +12,9 @@ confirm.  So the kernel-dependent numbers are inputs here, never literals:
     list; the pipeline depth of each is derived, not listed: the deepest
     stage count (at most MAX_STAGES) that passes C1;
   * the kernels' register figure, the co-resident CTA pairs, the operand
-    fill rate and the K-split hand-off rate and latency are fields of the
-    device record, which callers fill from the runtime (GPU tests) or from
-    the library's preset (host tests).
+    fill rate, the K-split hand-off rate and latency and the CTA pairs'
+    launch cost are fields of the device record, which callers fill from the
+    runtime (GPU tests) or from the library's preset (host tests).
 
 What pins them: GPU tests compare C1's total with the dynamic shared memory
 the runtime reports for each compiled kernel, the register figure with its
@@ -52,7 +52,8 @@ Rules
        reduce, reduce = 2 * ceil((bm/cg)*bn*4 / partial_bytes_per_clk) +
        handoff_clocks (a part's fp32 partial goes out and comes back).
        Ties keep that order and the fewer parts.  tail_split reports s, -1
-       for N-halves, 0 for whole tiles.
+       for N-halves, 0 for whole tiles.  A CTA-pair kernel adds
+       pair_launch_clocks, its extra fixed cost per launch.
   rank (est_clocks, round(C0), -blocks per SM, smem_total), stable over the
        variant order.
 """
@@ -80,6 +81,7 @@ class GB300Device:
     fill_bytes_per_clk: int
     partial_bytes_per_clk: int
     handoff_clocks: int
+    pair_launch_clocks: int
     cta_pairs: int = 0          # co-resident 2-CTA clusters; 0 = sm_count // 2
     smem_per_sm: int = 228 * 1024
     smem_per_block_max: int = 227 * 1024
@@ -277,7 +279,8 @@ def est_clocks(v: GB300Verdict, dev: GB300Device, k: int) -> int:
     mode, parts, clocks = tail_choice(v, dev, kblocks, resident)
     v.tail_split = parts if mode == "ksplit" else (-1 if mode == "nhalf" else 0)
     rest = v.grid % resident
-    return (v.grid // resident) * kblocks * unit + (clocks if rest else 0)
+    launch = dev.pair_launch_clocks if cfg.cta_group == 2 else 0
+    return (v.grid // resident) * kblocks * unit + (clocks if rest else 0) + launch
 
 
 def compiled_configs(tiles, dev: GB300Device, in_bytes: int = 2) -> list:

@@ -13,6 +13,7 @@ def oracle_device(dev) -> OG.GB300Device:
         fill_bytes_per_clk=dev.fill_bytes_per_clk,
         partial_bytes_per_clk=dev.partial_bytes_per_clk,
         handoff_clocks=dev.handoff_clocks,
+        pair_launch_clocks=dev.pair_launch_clocks,
         cta_pairs=dev.cta_pairs,
         smem_per_sm=dev.smem_per_sm,
         smem_per_block_max=dev.smem_per_block_max,

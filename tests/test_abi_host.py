@@ -253,6 +253,7 @@ def test_gb300_plan_matches_oracle(lib, case):
     ("fill_bytes_per_clk", (16, 48, 64, 128)),
     ("partial_bytes_per_clk", (0, 8, 32, 256)),
     ("handoff_clocks", (0, 512, 2048, 20000)),
+    ("pair_launch_clocks", (0, 4500, 40000, 200000)),
 ])
 def test_gb300_plan_follows_every_model_input(lib, field, values):
     # The kernel-dependent numbers are inputs of both planners: varying any
@@ -337,7 +338,8 @@ def simulated_makespan(v, dev, k):
     smaller of the units and the resident groups); a unit costs its K
     blocks times the clocks of one K block at its width, and the last K part
     of a split tile, once its own K blocks are done, waits for its leading
-    parts to be done and then adds one partial read-back per leading part."""
+    parts to be done and then adds one partial read-back per leading part.
+    A CTA-pair launch adds its fixed cost (pair_launch_clocks)."""
     cfg = v.cfg
     cg = cfg.cta_group
     kb = -(-k // cfg.bk)
@@ -369,7 +371,7 @@ def simulated_makespan(v, dev, k):
         clock[g] = finish
         if tile is not None:
             done[(tile, part)] = clock[g]
-    return max(clock)
+    return max(clock) + (dev.pair_launch_clocks if cg == 2 else 0)
 
 
 @pytest.mark.parametrize("sm,pairs", [(148, 0), (152, 76), (152, 74), (160, 0)])

@@ -136,10 +136,11 @@ def test_host_calls_order_after_earlier_work_on_the_stream():
     b_d = torch.empty((k, n), dtype=torch.float16, device="cuda")
     c_d = torch.empty((m, n), dtype=torch.float32, device="cuda")
     s = torch.cuda.Stream()
+    ws = T.workspace()
     with torch.cuda.stream(s):
         for t in (a_d, b_d, c_d):
             t.fill_(7.0)
-        T.gemm_host(a_h, b_h, c_h, a_d, b_d, c_d, stream=s, chunks=3)
+        T.gemm_host(a_h, b_h, c_h, a_d, b_d, c_d, workspace=ws, stream=s, chunks=3)
         after = c_d.clone()
     s.synchronize()
     a64, b64 = S.widen(a_np, S.F16), S.widen(b_np, S.F16)
@@ -167,7 +168,8 @@ def test_host_calls_from_threads_that_exit():
             b_d = torch.empty((k, n), dtype=torch.float16, device="cuda")
             c_d = torch.empty((m, n), dtype=torch.float32, device="cuda")
             s = torch.cuda.Stream()
-            T.gemm_host(a_h, b_h, c_h, a_d, b_d, c_d, stream=s, chunks=2 + idx)
+            ws = T.workspace()                # each call has its own workspace
+            T.gemm_host(a_h, b_h, c_h, a_d, b_d, c_d, workspace=ws, stream=s, chunks=2 + idx)
             s.synchronize()
             outs.append(c_h)
         except Exception as e:          # reported below, in the main thread

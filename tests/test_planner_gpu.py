@@ -15,11 +15,11 @@ and that the script measures nothing.  These tests make that confirmation:
     pairs);
   * the oracle's GB300 plan, fed the device record the runtime query fills,
     is the native plan bit for bit;
-  * ranking: on the three large GEMM workloads the planner's first choice
-    (with its own last-round schedule) runs within 3% of the fastest
-    candidate of the measured shortlist, and the time estimate orders the
-    shortlist's configurations as they measure wherever it separates them
-    by more than 15%.
+  * ranking: on the four GEMM workloads the planner's first choice (with its
+    own last-round schedule) runs within 3% of the fastest candidate of the
+    measured shortlist, and the time estimate orders the shortlist's
+    configurations as they measure wherever it separates them by more than
+    20% (the model's error band, from measured shortlists of 16 shapes).
 """
 
 import pytest
@@ -106,7 +106,7 @@ def operands(wl):
     return a, b, c
 
 
-@pytest.mark.parametrize("name", ["gemm_4096", "gemm_batched", "gemm_ragged"])
+@pytest.mark.parametrize("name", ["gemm_4096", "gemm_batched", "gemm_ragged", "gemm_512"])
 def test_planner_choice_against_the_measured_shortlist(dev, name):
     wl = S.WORKLOADS[name]
     a, b, c = operands(wl)
@@ -135,10 +135,11 @@ def test_planner_choice_against_the_measured_shortlist(dev, name):
                     (cfg.bm, cfg.bn, cfg.stages, cfg.cta_group) and r["tail_asked"] == 0)
 
     table = [(v.cfg.bm, v.cfg.bn, v.cfg.cta_group, v.est_clocks, own(v.cfg)["us"]) for v in top]
-    assert own(first)["us"] <= 1.03 * fastest, (table, fastest)
+    # 3%, or 0.3 us on launches of a few microseconds (their jitter).
+    assert own(first)["us"] <= max(1.03 * fastest, fastest + 0.3), (table, fastest)
     for i, (_, _, _, est_i, us_i) in enumerate(table):
         for _, _, _, est_j, us_j in table[i + 1:]:
-            if est_i < 0.85 * est_j:
+            if est_i < 0.8 * est_j:
                 assert us_i < us_j, table
-            if est_j < 0.85 * est_i:
+            if est_j < 0.8 * est_i:
                 assert us_j < us_i, table

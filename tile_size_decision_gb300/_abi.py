@@ -46,8 +46,7 @@ class Device(C.Structure):
         "max_threads_per_block", "max_blocks_per_sm", "regs_per_thread_max",
         "reg_granularity_per_warp", "warp_size", "sm_count", "tmem_cols", "mma_flops_per_clk",
         "fill_bytes_per_clk", "kernel_regs_per_thread", "cta_pairs", "partial_bytes_per_clk",
-        "handoff_clocks")] + \
-        [("reserved", C.c_int32 * 1)]
+        "handoff_clocks", "pair_launch_clocks")]
 
 
 class Config(C.Structure):

@@ -305,7 +305,8 @@ int64_t gb300_est_clocks(const tiles_device& dev, tiles_verdict* v, int64_t k) {
     const int64_t rest = v->grid % resident;
     const TailChoice tc = gb300_tail_choice(dev, cfg, v->grid, resident, kblocks, 2, TILES_TAIL_AUTO);
     v->tail_split = tc.mode == TILES_TAIL_KSPLIT ? tc.parts : tc.mode == TILES_TAIL_NHALF ? -1 : 0;
-    return (v->grid / resident) * kblocks * unit + (rest ? tc.clocks : 0);
+    const int64_t launch = cfg.cta_group == 2 ? dev.pair_launch_clocks : 0;
+    return (v->grid / resident) * kblocks * unit + (rest ? tc.clocks : 0) + launch;
 }
 
 static int bytes_of(int dtype) {
@@ -423,6 +424,7 @@ void device_preset_gb300(tiles_device* d) {
     d->kernel_regs_per_thread = kGemmRegsPerThread;
     d->partial_bytes_per_clk = kPartialBytesPerClk;
     d->handoff_clocks = kTailHandoffClocks;
+    d->pair_launch_clocks = kPairLaunchClocks;
 }
 
 int htile_rows(int H, int kh, int sh, int pt, int d, int o0, int o1, tiles_htile* t) {

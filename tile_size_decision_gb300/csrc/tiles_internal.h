@@ -70,6 +70,13 @@ TailChoice gb300_tail_choice(const tiles_device& dev, const tiles_config& cfg, i
 // 4-byte or 16-byte lane stores.
 constexpr int64_t kTailHandoffClocks = 2048;
 constexpr int64_t kPartialBytesPerClk = 32;
+// GB300 preset of the extra fixed clocks of a CTA-pair launch over a one-CTA
+// launch (the device record's pair_launch_clocks): the cluster launch, the
+// pair's prologue and its last epilogue.  Measured on 512^3 GEMMs, where
+// both run 8 fill-bound K blocks per unit: the 256x256 pair took 11.1 us
+// against 8.6 us for 128x128 tiles, the 256x128 pair 10.9 us against 8.7 us
+// for 128x64, about 2.3 us, ~4,500 clocks at the 1.93 GHz of those runs.
+constexpr int64_t kPairLaunchClocks = 4500;
 constexpr int kMaxTailParts = 8;
 void device_preset_h100(tiles_device* d);
 void device_preset_gb300(tiles_device* d);

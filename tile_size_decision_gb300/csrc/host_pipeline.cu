@@ -195,8 +195,8 @@ extern "C" int tiles_conv2d_host(const tiles_conv_desc* d, int tile_oh, const ti
         return fail(TILES_ERR_INVALID_ARG, "invalid convolution shape");
     const int64_t ei = bytes_of_dtype(d->in_dtype), eo = bytes_of_dtype(d->out_dtype);
     if (!ei || !eo) return fail(TILES_ERR_UNSUPPORTED_DTYPE, "unsupported dtype");
-    const int64_t oh = (static_cast<int64_t>(d->h) + 2 * d->ph - static_cast<int64_t>(d->kh - 1) * d->dh - 1) / d->sh + 1;
-    const int64_t ow = (static_cast<int64_t>(d->w) + 2 * d->pw - static_cast<int64_t>(d->kw - 1) * d->dw - 1) / d->sw + 1;
+    int64_t oh = 0, ow = 0;
+    if (const int hw = conv_out_hw(d, &oh, &ow); hw != TILES_OK) return hw;
     // One image of x (either layout) and of y is contiguous.
     const int64_t x_img = static_cast<int64_t>(d->c) * d->h * d->w * ei;
     const int64_t y_img = static_cast<int64_t>(d->c_out) * oh * ow * eo;

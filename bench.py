@@ -175,6 +175,24 @@ def recorded_traffic(workload: str):
         return None
 
 
+L2_NOTE = ("flushed between timed GPU steps (a 256 MB write, outside the kernel events); the "
+           "CPU oracle arm has no L2 to flush")
+
+
+def workload_config(wl, world=1):
+    """The workload as both arms describe it in their line's config: shapes,
+    dtypes, distribution, seed, the L2 treatment and the replicas."""
+    if isinstance(wl, S.ConvWorkload):
+        base = {"workload": wl.name, "n": wl.n, "c": wl.c, "h": wl.h, "w": wl.w,
+                "c_out": wl.c_out, "kh": wl.kh, "kw": wl.kw, "stride": [wl.sh, wl.sw],
+                "pad": [wl.ph, wl.pw], "dil": [wl.dh, wl.dw], "tile_oh": wl.tile_oh}
+    else:
+        base = {"workload": wl.name, "b": wl.b, "m": wl.m, "n": wl.n, "k": wl.k}
+    return dict(base, in_dtype=wl.in_dtype, out_dtype=wl.out_dtype, accumulate="f32",
+                distribution=wl.dist, seed=wl.seed, l2=L2_NOTE,
+                parallelism=f"replicas x{world}")
+
+
 # --------------------------------------------------------------------------- #
 # CPU oracle timing (the baseline and the reference arm)
 # --------------------------------------------------------------------------- #
@@ -379,10 +397,9 @@ def gemm_job(wl, dev, tiles, torch):
     j.bound = "tensor"
     j.bytes = wl.b * (wl.m * wl.k + wl.k * wl.n) * 2 + wl.b * wl.m * wl.n * S.DTYPE_BYTES[wl.out_dtype]
     sch = tiles.gemm_schedule(a_d, b_d, j.out, workspace=j.ws)
-    j.config = {
-        "workload": wl.name, "b": wl.b, "m": wl.m, "n": wl.n, "k": wl.k,
-        "in_dtype": wl.in_dtype, "out_dtype": wl.out_dtype, "accumulate": "f32",
-        "distribution": wl.dist, "seed": wl.seed,
+    j.config = workload_config(wl)
+    # How this library runs it (reported beside the config, under "plan").
+    j.plan = {
         "tile": {"bm": c.bm, "bn": c.bn, "bk": c.bk, "stages": c.stages,
                  "cta_group": c.cta_group, "grid_tiles": verdict.grid, "waves": verdict.waves,
                  "last_wave_fill": round(verdict.last_wave_fill, 4),
@@ -465,12 +482,10 @@ def conv_job(wl, dev, tiles, torch):
     rows = [tiles.htile_rows(wl.h, wl.kh, wl.sh, wl.ph, wl.dh, o0, min(o0 + wl.tile_oh, wl.oh))
             for o0 in range(0, wl.oh, wl.tile_oh)]
     halo_bytes = sum(min(r.in_end, wl.h) - r.in_start for r in rows) * wl.n * wl.c * wl.w * 2
-    j.config = {
-        "workload": wl.name, "n": wl.n, "c": wl.c, "h": wl.h, "w": wl.w, "c_out": wl.c_out,
-        "kh": wl.kh, "kw": wl.kw, "stride": [wl.sh, wl.sw], "pad": [wl.ph, wl.pw],
-        "dil": [wl.dh, wl.dw], "tile_oh": wl.tile_oh, "h_tiles": n_ht,
-        "in_dtype": wl.in_dtype, "out_dtype": wl.out_dtype, "accumulate": "f32",
-        "distribution": wl.dist, "seed": wl.seed,
+    j.config = workload_config(wl)
+    # How this library runs it (reported beside the config, under "plan").
+    j.plan = {
+        "h_tiles": n_ht,
         "gemm_per_tile": {"m": wl.c_out, "n": wl.tile_oh * wl.ow, "k": wl.c * wl.kh * wl.kw},
         "input_bytes_with_halo": halo_bytes,
         "producer": ("tma: the NCHW input read in place; per (kernel row, 64 channels) a TMA box "
@@ -597,9 +612,9 @@ def workload_entry(name, args, dev, tiles, torch, stream, flush, peaks, src, gpu
     at least 50 flushed steps and as many L2-warm ones, its roofline, and the
     oracle timed on a bounded sample of it."""
     job, wl = make_job(name, dev, tiles, torch)
-    entry = {"config": job.config}
+    entry = {"config": job.config, "plan": job.plan}
     if getattr(job, "autotune", None) and args.autotune > 0:
-        entry["config"]["autotune"] = job.autotune(args.autotune)
+        entry["plan"]["autotune"] = job.autotune(args.autotune)
     sampler = ClockSampler(gpu_index)
     sampler.start()
     time.sleep(0.3)
@@ -655,7 +670,7 @@ def run_ours(args, rank, world, local_rank):
     peaks, src = load_peaks()
 
     if getattr(job, "autotune", None) and args.autotune > 0:
-        job.config["autotune"] = job.autotune(args.autotune)
+        job.plan["autotune"] = job.autotune(args.autotune)
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -721,7 +736,8 @@ def run_ours(args, rank, world, local_rank):
 
     # What the line reports of the headline job (the job is released before
     # the other workloads run).
-    head = {"dtype": job.dtype, "config": job.config, "roofline": roofline(job, ms, peaks, src,
+    head = {"dtype": job.dtype, "config": job.config, "plan": job.plan,
+            "roofline": roofline(job, ms, peaks, src,
                                                                             args.workload),
             "h2d": int(sum(t.numel() * t.element_size() for t in job.host_in)),
             "d2h": int(job.host_out.numel() * job.host_out.element_size()),
@@ -776,9 +792,8 @@ def run_ours(args, rank, world, local_rank):
             "dtype": head["dtype"],
             "data": "synthetic",
             "impl": "ours",
-            "config": dict(head["config"],
-                           l2="flushed between timed steps (256 MB write, outside the kernel events)",
-                           parallelism=f"replicas x{world}"),
+            "config": dict(head["config"], parallelism=f"replicas x{world}"),
+            "plan": head["plan"],
             "roofline": head["roofline"],
             "e2e": {"value": round(e2e, 2), "unit": "TFLOP/s",
                     "call": "tiles_gemm_host" if args.workload.startswith("gemm") else "tiles_conv2d_host",
@@ -819,14 +834,10 @@ def run_reference(args, rank, world):
     if isinstance(wl, S.ConvWorkload):
         x, w = S.conv_inputs(wl)
         sample = lambda budget: oracle_conv_sample(wl, budget, x, w)  # noqa: E731
-        config = {"workload": wl.name, "n": wl.n, "c": wl.c, "h": wl.h, "w": wl.w,
-                  "c_out": wl.c_out, "kh": wl.kh, "kw": wl.kw, "tile_oh": wl.tile_oh,
-                  "in_dtype": wl.in_dtype, "out_dtype": wl.out_dtype}
     else:
         a, b = S.gemm_inputs(wl)
         sample = lambda budget: oracle_sample(wl, budget, a, b)  # noqa: E731
-        config = {"workload": wl.name, "b": wl.b, "m": wl.m, "n": wl.n, "k": wl.k,
-                  "in_dtype": wl.in_dtype, "out_dtype": wl.out_dtype}
+    config = workload_config(wl, world)
     per_step = max(2.0, min(10.0, 150.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
         sample(min(per_step, 2.0))

@@ -51,3 +51,14 @@ def test_clock_summary_keeps_only_the_samples_of_its_window():
     assert (s["samples"], s["sm_mhz"], s["sm_max_mhz"], s["reasons"]) == (2, 1850.0, 2070.0, [])
     assert bench.summarize_clocks(rows)["reasons"] == ["sw_thermal_slowdown"]
     assert bench.summarize_clocks(rows, t[4] + 1, t[4] + 2)["samples"] == 0
+
+
+def test_both_arms_describe_each_workload_alike():
+    # The reference arm and this library's arm build their line's config
+    # from the same description of the workload.
+    import synth_inputs as S
+    for name, wl in S.WORKLOADS.items():
+        c = bench.workload_config(wl, 2)
+        assert (c["workload"], c["seed"], c["accumulate"]) == (name, wl.seed, "f32")
+        assert c["parallelism"] == "replicas x2" and "tile" not in c
+        assert c == bench.workload_config(wl, 2)

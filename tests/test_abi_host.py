@@ -487,3 +487,28 @@ def test_plan_validation(lib):
 def test_binding_exports_every_listed_name():
     for name in T.__all__:
         assert hasattr(T, name), name
+
+
+def test_drop_stage_hook_validates_before_arming(lib):
+    # The planted-fault hook takes a limit in (0, 1e10] ns; a negative stage
+    # disarms whatever is armed.  No GPU is touched by arming.
+    assert lib.tiles_selftest_drop_stage(0, 0) == _abi.ERR_INVALID_ARG
+    assert lib.tiles_selftest_drop_stage(3, 10_000_000_001) == _abi.ERR_INVALID_ARG
+    assert lib.tiles_selftest_drop_stage(3, 50_000_000) == _abi.OK
+    assert lib.tiles_selftest_drop_stage(-1, 0) == _abi.OK
+
+
+def test_kernel_calls_refuse_a_missing_workspace_before_any_launch(lib):
+    # Descriptor checks come first; then the workspace check, still before
+    # any device work (a GEMM needs the device for its plan, so only the
+    # order of the checks is visible here: a bad descriptor is reported as
+    # such even with no workspace).
+    d = _desc(a=None)
+    assert lib.tiles_gemm(C.byref(d), None, None, 0, None) == _abi.ERR_INVALID_ARG
+    assert b"null matrix pointer" in lib.tiles_last_error()
+    cd = _abi.ConvDesc()
+    cd.n, cd.c, cd.h, cd.w, cd.c_out, cd.kh, cd.kw = 1, 8, 9, 9, 4, 3, 3
+    cd.sh = cd.sw = cd.dh = cd.dw = 1
+    cd.x, cd.wt, cd.y = 0x10000, 0x20000, 0x30000
+    assert lib.tiles_conv2d_htiled(C.byref(cd), 4, None, None, 0, None) == _abi.ERR_INVALID_ARG
+    assert b"workspace" in lib.tiles_last_error()

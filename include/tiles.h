@@ -269,8 +269,12 @@ const char* tiles_version(void);
 int tiles_device_preset(int preset, tiles_device* out);
 
 /* The GB300 preset with the runtime's values for CUDA device `ordinal`
- * (SM count, shared memory per SM and per block, registers, threads).
- * CUDA error if no such device. */
+ * (SM count, shared memory per SM and per block, registers, threads).  When
+ * `ordinal` is the current device it also takes the compiled kernels' facts
+ * from the runtime: kernel_regs_per_thread is the largest register count of
+ * a compiled variant rounded up to the per-warp granule, and cta_pairs the
+ * co-resident 2-CTA clusters of the 256-wide pair kernel.  CUDA error if no
+ * such device. */
 int tiles_device_query(int ordinal, tiles_device* out);
 
 /* ---- constraint procedure ---------------------------------------------- */

@@ -412,6 +412,30 @@ def test_extreme_aspect_ratios(ws, m, n, k, in_dt, out_dt):
     assert_close(to_f64(c), S.widen(a, in_dt), S.widen(b, in_dt), out_dt)
 
 
+@pytest.mark.parametrize("v", [(256, 2), (128, 1)], ids=["bn256_cg2", "bn128_cg1"])
+def test_grouped_tile_order_covers_every_tile(ws, v):
+    # A tall GEMM whose A panels (20 M blocks x K) exceed the scheduler's L2
+    # share, so the tiles go in groups of 8 M blocks: two full groups, a last
+    # group of 4 blocks ending in a ragged one, and a ragged N.  Every output
+    # is written (NaN canary) and rows sampled in every group match the
+    # oracle.
+    bn, cg = v
+    bm = 128 * cg
+    m, n = bm * 19 + 37, 2 * bn + 40
+    k = 4608 if cg == 2 else 9216
+    assert -(-m // bm) * bm * k * 2 > (43 << 20)
+    a = S.random_matrix(97, (m, k), S.F16, "normal")
+    b = S.random_matrix(98, (k, n), S.F16, "normal")
+    c = empty_out((m, n), S.F32)
+    T.gemm(to_cuda(a, S.F16), to_cuda(b, S.F16), out=c, cfg=variant(v), workspace=ws)
+    T.check(ws)
+    got = to_f64(c)
+    assert not np.isnan(got).any()
+    rows = np.r_[0:8, 8 * bm - 4:8 * bm + 4, 16 * bm - 4:16 * bm + 4, m - 40:m]
+    a64, b64 = S.widen(a[rows], S.F16), S.widen(b, S.F16)
+    assert_close(got[rows], a64, b64, S.F32)
+
+
 def test_many_tiny_batch_items(ws):
     batch, m, n, k = 1000, 16, 24, 32
     a = S.random_matrix(95, (batch, m, k), S.F16)

@@ -29,6 +29,11 @@ namespace {
 thread_local std::string g_last_error;
 
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s per wait
+// Grouped tile order: A panels of up to kTileGroupBytes (a third of the
+// 129 MB L2) keep plain M-fastest order; beyond it tiles go in groups of
+// kTileGroupM M blocks (8 + 76/8 panels in flight for 76 CTA pairs).
+constexpr int64_t kTileGroupBytes = 43ll << 20;
+constexpr int32_t kTileGroupM = 8;
 constexpr size_t kWorkspaceBytes = 256;
 static_assert(kWorkspaceBytes == static_cast<size_t>(kConvMinWorkspaceBytes),
               "one workspace minimum for every kernel call");
@@ -417,6 +422,14 @@ int gemm_common(const tiles_gemm_desc* d, const tiles_config* user_cfg, void* ws
     args.m = (int32_t)d->m; args.n = (int32_t)d->n; args.k = (int32_t)d->k;
     args.batch = (int32_t)batch;
     args.m_blocks = (int32_t)((d->m + cfg.bm - 1) / cfg.bm);
+    // Grouped tile order (the persistent scheduler's rasterisation): when the
+    // A panels of every M block of an item would not stay in L2 while the
+    // concurrent CTAs sweep N, the tiles go in groups of kTileGroupM M blocks.
+    // A window of resident groups then covers kTileGroupM M blocks by about
+    // resident / kTileGroupM N blocks of panels.
+    const int64_t a_panels = static_cast<int64_t>(args.m_blocks) * cfg.bm * d->k * 2;
+    args.group_m = a_panels <= kTileGroupBytes ? args.m_blocks
+                                               : std::min<int32_t>(args.m_blocks, kTileGroupM);
     args.n_blocks = (int32_t)((d->n + cfg.bn - 1) / cfg.bn);
     args.k_blocks = (int32_t)((d->k + cfg.bk - 1) / cfg.bk);
     args.tiles = (int32_t)gp.tiles;

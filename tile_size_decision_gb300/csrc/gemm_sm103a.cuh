@@ -65,6 +65,7 @@ struct GemmArgs {
     int32_t m, n, k, batch;
     int32_t m_blocks, n_blocks, k_blocks;
     int32_t tiles;             // batch * m_blocks * n_blocks
+    int32_t group_m;           // tile order: groups of group_m M blocks (1 .. m_blocks)
     // Work units: units [0, full_units) are whole tiles.  The tiles after
     // them (the last, partly filled round) run by tail_mode:
     //   kTailNone   as whole tiles (units = tiles);
@@ -133,13 +134,22 @@ struct GemmLayout {
 
 struct TileCoord { int b, mi, ni; };
 
-__device__ __forceinline__ TileCoord decode_tile(int t, int m_blocks, int n_blocks) {
+__device__ __forceinline__ TileCoord decode_tile(int t, int m_blocks, int n_blocks, int group_m) {
+    // Within a batch item the tiles go in groups of group_m M blocks: M
+    // fastest inside a group (concurrent CTAs share B panels), then N, then
+    // the next group (the groups keep the A panels of concurrent CTAs few
+    // enough to stay in L2).  group_m == m_blocks is plain M-fastest order.
     const int per_batch = m_blocks * n_blocks;
     TileCoord c;
     c.b = t / per_batch;
     const int r = t - c.b * per_batch;
-    c.mi = r % m_blocks;        // M fastest: concurrent CTAs share B panels
-    c.ni = r / m_blocks;
+    const int span = group_m * n_blocks;
+    const int g = r / span;
+    const int first = g * group_m;
+    const int rows = min(group_m, m_blocks - first);
+    const int q = r - g * span;
+    c.mi = first + q % rows;
+    c.ni = q / rows;
     return c;
 }
 
@@ -175,7 +185,7 @@ __device__ __forceinline__ UnitCoord decode_unit(int u, const GemmArgs& a) {
             kb1 = (part + 1) * a.k_blocks / a.ksplit;
         }
     }
-    const TileCoord tc = decode_tile(t, a.m_blocks, a.n_blocks);
+    const TileCoord tc = decode_tile(t, a.m_blocks, a.n_blocks, a.group_m);
     return UnitCoord{tc.b, tc.mi, tc.ni * BN + off, width, kb0, kb1, part, tail};
 }
 

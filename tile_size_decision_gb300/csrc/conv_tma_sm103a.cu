@@ -678,9 +678,15 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                 const int kb0 = args.raw_filter ? p * kRawFilterBoxes : p * args.w_slots;
                 const int nkb = args.raw_filter ? kRawFilterBoxes : min(args.w_slots, args.k_blocks - kb0);
                 ptx::mbar_arrive_expect_tx(&bar->wfull, static_cast<uint32_t>(nkb * kWtWeightBlockBytes));
-                for (int i = 0; i < nkb; ++i)
+                // Every CTA reads the same blocks at start-up; each begins at
+                // a different one (blockIdx.x mod nkb) so that the L2 lines
+                // in demand at any moment are spread over the whole filter.
+                const int rot = static_cast<int>(blockIdx.x % static_cast<unsigned>(nkb));
+                for (int j = 0; j < nkb; ++j) {
+                    const int i = j + rot < nkb ? j + rot : j + rot - nkb;
                     ptx::tma_load_3d(base + args.w_off + i * kWtWeightBlockBytes, &tmW, &bar->wfull,
                                      (kb0 + i) * 64, 0, 0);
+                }
             };
             if constexpr (DIRECT) {
                 // ---------------- TMA producer: each stage's raw NCHW box ----------------
@@ -1914,6 +1920,14 @@ int conv2d_tma(const tiles_conv_desc* d, const tiles_config* cfg, int tile_oh, i
         a.stg_pitch = tma_store ? owc * yb : wp.stg_pitch;
         a.bar_off = a.stg_off + wp.stg_bytes;
         a.w_slots = wp.w_slots;
+        if (use_direct && raw_filter) {
+            // Every raw slot below the 9 filter boxes' start-up space loads
+            // beside them.
+            while (a.raw_early + 1 < a.raw_stages &&
+                   a.bar_off - (a.raw_early + 1) * a.raw_b >= kRawFilterBoxes * kWtWeightBlockBytes)
+                ++a.raw_early;
+            a.w_off = a.raw_early * a.raw_b;
+        }
         smem = wp.smem;
         e = use_direct ? set_smem_attr(reinterpret_cast<const void*>(conv_wtmem_kernel<2>),
                                        &g_smem_direct, smem)

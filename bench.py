@@ -7,11 +7,15 @@
 A step is one pass of the hot path over one batch of synthetic input: the
 planned configuration (memoised after the first call) and one launch of the
 persistent GEMM kernel through the C ABI.  Inputs are seeded (synth_inputs),
-resident in HBM before the timed region; L2 (129 MB) is flushed between
-timed steps by writing a 256 MB buffer, outside the per-step CUDA events.
+resident in HBM before the timed region.  The K timed steps run back to back
+between one pair of CUDA events, cycling through R copies of the operands:
+between two uses of one copy the other R - 1 copies, at least twice the
+129 MB L2, pass through it, so no step finds its inputs in L2 and none needs
+a flush (inputs larger than L2).  Per-step figures with L2 flushed between
+steps (a 256 MB write outside per-step events) are reported beside it.
 
 One JSON line is printed by rank 0.  ``value`` is whole-job TFLOP/s (2*b*M*N*K
-per step per rank over the max-over-ranks mean kernel time); ``e2e`` is the
+per step per rank over the max-over-ranks time per step); ``e2e`` is the
 same metric through the same call with pinned host buffers and the H2D/D2H
 copies inside the timed region; ``roofline`` relates the kernel to the
 measured bf16 tensor peak; ``cpu_baseline`` times the float64 oracle on the
@@ -22,15 +26,16 @@ has no exchange step).
 
 The default single-GPU run of the 4096^3 headline adds, after the headline's
 timed steps:
-  timing     the step timed at least 50 times with L2 flushed and 50 times
-             L2-warm (mean, median, minimum);
+  timing     the step timed on its own at least 50 times with L2 flushed and
+             50 times L2-warm (mean, median, minimum);
   sustained  about 2.5 s of back-to-back launches between one pair of
              events, with the SM clock sampled inside that window: TFLOP/s
              against the measured sustained bf16 peak, and the cycles per
              launch at the clock it ran at;
   workloads  the other four seeded workloads (gemm_512, gemm_batched,
              gemm_ragged, conv_htiled), each measured like the headline
-             (at least 50 flushed and 50 warm steps) with its roofline, its
+             (at least 50 rotating steps, then 50 flushed and 50 warm ones
+             on their own) with its roofline, its
              recorded DRAM traffic, its clock record and the oracle timed on
              a bounded sample of it.
 """
@@ -58,6 +63,7 @@ import numpy as np  # noqa: E402
 import synth_inputs as S  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -175,8 +181,17 @@ def recorded_traffic(workload: str):
         return None
 
 
-L2_NOTE = ("flushed between timed GPU steps (a 256 MB write, outside the kernel events); the "
-           "CPU oracle arm has no L2 to flush")
+L2_NOTE = ("inputs larger than L2: the timed GPU steps run back to back over R copies of the "
+           "operands, and the R - 1 other copies touched between two uses of one copy hold at "
+           "least twice the 129 MB L2 (no flush); the per-step figures under 'flushed' write a "
+           "256 MB buffer between steps instead; the CPU oracle arm has no L2")
+
+
+def rotation_sets(set_bytes: int) -> int:
+    """Copies of a workload's operands (inputs and output) that the timed
+    steps cycle through: enough that the other copies touched between two
+    uses of one hold at least twice the L2."""
+    return max(2, -(-2 * L2_BYTES // max(int(set_bytes), 1)) + 1)
 
 
 def workload_config(wl, world=1):
@@ -355,8 +370,9 @@ def summarize_clocks(rows, t0=None, t1=None):
 
 class Job:
     """One workload prepared on a device: pinned host inputs, resident device
-    inputs, the output, the step (one call through the C ABI) and the
-    figures the JSON line reports."""
+    inputs and output (copy 0 of the rotation, beside copies 1 .. R-1), the
+    step (one call through the C ABI on copy i % R) and the figures the JSON
+    line reports."""
 
 
 def gemm_job(wl, dev, tiles, torch):
@@ -377,12 +393,16 @@ def gemm_job(wl, dev, tiles, torch):
                                c.cta_group, tail="ksplit")
     j.ws = max(tiles.gemm_workspace(a_d, b_d, j.out), tiles.gemm_workspace(a_d, b_d, j.out, ksplit),
                key=lambda t: t.numel())
+    j.set_bytes = sum(t.numel() * t.element_size() for t in (a_d, b_d, j.out))
+    j.sets = [(a_d, b_d, j.out)] + [(a_d.clone(), b_d.clone(), torch.empty_like(j.out))
+                                    for _ in range(rotation_sets(j.set_bytes) - 1)]
 
-    def step(ws, stream):
+    def step(i, stream):
+        a, b, out = j.sets[i % len(j.sets)]
         if wl.b > 1:
-            tiles.gemm_batched(a_d, b_d, out=j.out, workspace=j.ws, stream=stream)
+            tiles.gemm_batched(a, b, out=out, workspace=j.ws, stream=stream)
         else:
-            tiles.gemm(a_d, b_d, out=j.out, workspace=j.ws, stream=stream)
+            tiles.gemm(a, b, out=out, workspace=j.ws, stream=stream)
 
     j.step = step
 
@@ -434,10 +454,11 @@ def gemm_job(wl, dev, tiles, torch):
                      round(r["us"], 2)] for r in rows if r["status"] == 0]}
 
     j.autotune = autotune
-    c_lib = torch.empty_like(j.out)
+    c_lib = [torch.empty_like(j.out) for _ in j.sets]
 
-    def library_step():
-        torch.matmul(a_d, b_d, out=c_lib)
+    def library_step(i):
+        a, b, _ = j.sets[i % len(j.sets)]
+        torch.matmul(a, b, out=c_lib[i % len(j.sets)])
 
     j.library_step = library_step if j.out.dtype == a_d.dtype else None
     return j
@@ -455,10 +476,14 @@ def conv_job(wl, dev, tiles, torch):
     # A workspace sized for the TMA im2col producer (the default path).
     j.ws = tiles.conv_workspace(x_d, w_d, (wl.sh, wl.sw), (wl.ph, wl.pw), (wl.dh, wl.dw),
                                 wl.tile_oh)
+    j.set_bytes = sum(t.numel() * t.element_size() for t in (x_d, w_d, j.out))
+    j.sets = [(x_d, w_d, j.out)] + [(x_d.clone(), w_d.clone(), torch.empty_like(j.out))
+                                    for _ in range(rotation_sets(j.set_bytes) - 1)]
 
-    def step(ws, stream):
-        tiles.conv2d_htiled(x_d, w_d, (wl.sh, wl.sw), (wl.ph, wl.pw), (wl.dh, wl.dw), wl.tile_oh,
-                            out=j.out, workspace=j.ws, stream=stream)
+    def step(i, stream):
+        x, w, out = j.sets[i % len(j.sets)]
+        tiles.conv2d_htiled(x, w, (wl.sh, wl.sw), (wl.ph, wl.pw), (wl.dh, wl.dw), wl.tile_oh,
+                            out=out, workspace=j.ws, stream=stream)
 
     j.step = step
 
@@ -509,11 +534,31 @@ def host_tensor(x, dt, torch):
     return t.pin_memory()
 
 
+def timed_rotating(job, stream, steps, start=0):
+    """Milliseconds per step of `steps` back-to-back steps over the job's
+    operand copies (step i uses copy i % R, from i = start), between one pair
+    of CUDA events on `stream`, and the host-clock window (time.time()) they
+    ran in."""
+    import torch
+
+    s_ev = torch.cuda.Event(enable_timing=True)
+    e_ev = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    s_ev.record(stream)
+    for i in range(start, start + steps):
+        job.step(i, stream)
+    e_ev.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    return s_ev.elapsed_time(e_ev) / steps, (t0, t1)
+
+
 def timed_steps(job, stream, flush, steps, warm=False):
-    """Milliseconds of each of `steps` steps, each bracketed by CUDA events
-    on `stream`; before each step L2 is flushed (a 256 MB write outside the
-    events) unless `warm`.  Also returns the host-clock window (time.time())
-    that the steps ran in."""
+    """Milliseconds of each of `steps` steps on operand copy 0, each
+    bracketed by CUDA events on `stream`; before each step L2 is flushed (a
+    256 MB write outside the events) unless `warm`.  Also returns the
+    host-clock window (time.time()) that the steps ran in."""
     import torch
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -524,7 +569,7 @@ def timed_steps(job, stream, flush, steps, warm=False):
         if not warm:
             flush.zero_()
         starts[i].record(stream)
-        job.step(None, stream)
+        job.step(0, stream)
         ends[i].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
@@ -559,13 +604,14 @@ def ms_stats(ms):
 
 
 def sustained_leg(job, stream, seconds, gpu_index, peaks, src):
-    """Back-to-back launches of the step (no flush) between one pair of CUDA
-    events for about `seconds`, with the clocks sampled inside that window:
-    the throughput under the power cap and the clock-normalised time."""
+    """Back-to-back launches of the step over the rotating operand copies
+    (no flush) between one pair of CUDA events for about `seconds`, with the
+    clocks sampled inside that window: the throughput under the power cap
+    and the clock-normalised time."""
     import torch
 
-    probe, _ = timed_steps(job, stream, None, 20, warm=True)
-    n = max(50, int(seconds * 1e3 / max(float(np.median(probe)), 1e-3)))
+    probe, _ = timed_rotating(job, stream, 20)
+    n = max(50, int(seconds * 1e3 / max(probe, 1e-3)))
     sampler = ClockSampler(gpu_index)
     sampler.start()
     time.sleep(0.3)
@@ -574,8 +620,8 @@ def sustained_leg(job, stream, seconds, gpu_index, peaks, src):
     torch.cuda.synchronize()
     t0 = time.time()
     s_ev.record(stream)
-    for _ in range(n):
-        job.step(None, stream)
+    for i in range(n):
+        job.step(i, stream)
     e_ev.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
@@ -593,7 +639,8 @@ def sustained_leg(job, stream, seconds, gpu_index, peaks, src):
     else:
         gbs = job.bytes * n / (total_ms * 1e-3) / 1e9
         out.update({"gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                    "peak_source": f"{src} HBM copy bandwidth (back to back, L2 warm between launches)"})
+                    "peak_source": f"{src} HBM copy bandwidth (back to back over the rotating "
+                                   "operand copies)"})
     if clk["sm_mhz"]:
         # Time x clock: the cycles one launch takes at the clock it ran at.
         out["kcycles_per_launch"] = round(us * clk["sm_mhz"] / 1e3, 1)
@@ -609,8 +656,9 @@ def make_job(name, dev, tiles, torch):
 
 def workload_entry(name, args, dev, tiles, torch, stream, flush, peaks, src, gpu_index):
     """One non-headline workload measured like the headline: warm-up, then
-    at least 50 flushed steps and as many L2-warm ones, its roofline, and the
-    oracle timed on a bounded sample of it."""
+    at least 50 back-to-back steps over its rotating operand copies (its
+    value and roofline), 50 flushed and 50 L2-warm steps on their own, and
+    the oracle timed on a bounded sample of it."""
     job, wl = make_job(name, dev, tiles, torch)
     entry = {"config": job.config, "plan": job.plan}
     if getattr(job, "autotune", None) and args.autotune > 0:
@@ -618,12 +666,12 @@ def workload_entry(name, args, dev, tiles, torch, stream, flush, peaks, src, gpu
     sampler = ClockSampler(gpu_index)
     sampler.start()
     time.sleep(0.3)
-    for _ in range(args.warmup):
-        flush.zero_()
-        job.step(None, stream)
+    for i in range(args.warmup):
+        job.step(i, stream)
     tiles.check(job.ws, stream)
     n = max(args.steps, 50)
-    ms, (t0, t1) = timed_steps(job, stream, flush, n)
+    mean, (t0, t1) = timed_rotating(job, stream, n, start=args.warmup)
+    ms, _ = timed_steps(job, stream, flush, n)
     warm, _ = timed_steps(job, stream, flush, n, warm=True)
     sampler.stop()
     tiles.check(job.ws, stream)
@@ -631,16 +679,17 @@ def workload_entry(name, args, dev, tiles, torch, stream, flush, peaks, src, gpu
     # workload's clock record (the flushed steps last milliseconds).
     busy = sustained_leg(job, stream, args.workload_sustained_seconds, gpu_index, peaks, src)
     tiles.check(job.ws, stream)
-    mean = float(np.mean(ms))
     entry.update({
         "value": round(job.flops / (mean * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-        "ms_per_step": round(mean, 5), "flushed": ms_stats(ms),
+        "ms_per_step": round(mean, 5), "steps": n, "operand_copies": len(job.sets),
+        "flushed": dict(ms_stats(ms), tflops_median=round(
+            job.flops / (float(np.median(ms)) * 1e-3) / 1e12, 2)),
         "l2_warm": dict(ms_stats(warm), tflops_median=round(
             job.flops / (float(np.median(warm)) * 1e-3) / 1e12, 2)),
         "roofline": roofline(job, mean, peaks, src, name),
         "gpu_launches": n * job.launches,
         "clocks": busy["clocks"],
-        "clocks_flushed_steps": dict(sampler.summary(t0, t1), whole_leg=sampler.summary()),
+        "clocks_timed_steps": dict(sampler.summary(t0, t1), whole_leg=sampler.summary()),
         "sustained": {key: val for key, val in busy.items() if key != "clocks"},
     })
     if not args.no_cpu_baseline:
@@ -675,22 +724,21 @@ def run_ours(args, rank, world, local_rank):
     sampler.start()
     time.sleep(0.3)
     # The warm-up steps run right before the timed ones, after the sampler's
-    # start-up pause, so that the timed steps start from a busy GPU.
-    for _ in range(args.warmup):
-        flush.zero_()
-        job.step(None, stream)
+    # start-up pause, so that the timed steps start from a busy GPU; the
+    # rotation continues from them.
+    for i in range(args.warmup):
+        job.step(i, stream)
     tiles.check(job.ws, stream)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    kernel_ms, (t0, t1) = timed_steps(job, stream, flush, args.steps)
+    ms, (t0, t1) = timed_rotating(job, stream, args.steps, start=args.warmup)
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - t_wall
     sampler.stop()
     tiles.check(job.ws, stream)
-    ms = float(np.mean(kernel_ms))
     # The headline's clock record: every sample from the warm-up to the end
     # of the timed steps (the timed region itself lasts milliseconds; the
     # sustained leg below samples a seconds-long window under load).
@@ -714,25 +762,25 @@ def run_ours(args, rank, world, local_rank):
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, world, dev)
 
     # Context only (not on this library's path): cuBLAS through torch.matmul
-    # on the same operands, timed the same way.
+    # on the same operand copies, timed the same way.
     context = None
     if getattr(job, "library_step", None) is not None:
-        lib_ms = []
-        for i in range(args.warmup + args.steps):
-            flush.zero_()
-            s_ev = torch.cuda.Event(enable_timing=True)
-            e_ev = torch.cuda.Event(enable_timing=True)
-            s_ev.record(stream)
-            job.library_step()
-            e_ev.record(stream)
-            torch.cuda.synchronize()
-            if i >= args.warmup:
-                lib_ms.append(s_ev.elapsed_time(e_ev))
-        lib_mean = float(np.mean(lib_ms))
+        for i in range(args.warmup):
+            job.library_step(i)
+        torch.cuda.synchronize()
+        s_ev = torch.cuda.Event(enable_timing=True)
+        e_ev = torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)
+        for i in range(args.warmup, args.warmup + args.steps):
+            job.library_step(i)
+        e_ev.record(stream)
+        torch.cuda.synchronize()
+        lib_mean = s_ev.elapsed_time(e_ev) / args.steps
         context = {"cublas_torch_matmul": {
             "ms_per_step": round(lib_mean, 5),
             "tflops": round(job.flops / (lib_mean * 1e-3) / 1e12, 2),
-            "note": "torch.matmul on the same device tensors; context, not a baseline"}}
+            "note": "torch.matmul on the same device operand copies, timed the same way; "
+                    "context, not a baseline"}}
 
     # What the line reports of the headline job (the job is released before
     # the other workloads run).
@@ -741,7 +789,7 @@ def run_ours(args, rank, world, local_rank):
                                                                             args.workload),
             "h2d": int(sum(t.numel() * t.element_size() for t in job.host_in)),
             "d2h": int(job.host_out.numel() * job.host_out.element_size()),
-            "launches": job.launches}
+            "launches": job.launches, "copies": len(job.sets)}
 
     # The same step timed at least 50 times, L2 flushed and L2 warm, and a
     # sustained, clock-sampled leg of back-to-back launches.
@@ -804,8 +852,7 @@ def run_ours(args, rank, world, local_rank):
             "gpu_launches": args.steps * head["launches"],
             "clocks": clocks,
             "wall_s_timed_region": round(wall, 4),
-            "kernel_ms_min": round(min(kernel_ms), 5),
-            "kernel_ms_median": round(float(np.median(kernel_ms)), 5),
+            "operand_copies": head["copies"],
             "cpu_baseline": cpu,
         }
         if timing is not None:

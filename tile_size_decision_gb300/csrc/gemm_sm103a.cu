@@ -98,8 +98,14 @@ int launch_gemm_variant<BN, CG>(const CUtensorMap& ta, const CUtensorMap& tb,
     cudaError_t e = set_smem_attribute();
     if (e != cudaSuccess) return static_cast<int>(e);
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     fill_launch(&cfg, attr, groups, stream);
+    // Programmatic serialization: the blocks may start their set-up while
+    // the previous kernel on the stream drains; they wait for it in-kernel
+    // before touching global memory.
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
     e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<BN, STAGES, CG>, ta, tb, tc, args);
     if (e != cudaSuccess) return static_cast<int>(e);
     return static_cast<int>(cudaGetLastError());

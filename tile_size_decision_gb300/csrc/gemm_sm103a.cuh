@@ -369,6 +369,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::tc_fence_before();
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
+    // The previous kernel on the stream may still be draining (programmatic
+    // serialization): nothing global is read or written before it has
+    // completed.  Every block of this grid is resident from here on, so the
+    // next kernel on the stream may start its own set-up on SMs as they free.
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort = &bar->abort;

@@ -1165,9 +1165,10 @@ __global__ void __launch_bounds__(FORM == 2 ? kWtDirectThreads : kWtThreads, 1)
                 }
             }
         }
-        // The last TMA store completes before the block (and its shared
-        // memory) goes away.
-        if (args.tma_store && et == 0) ptx::bulk_wait_all();
+        // The last TMA store has read the staging tile before the block
+        // (and its shared memory) goes away; its writes to y complete with
+        // the grid, before anything that waits for it reads y.
+        if (args.tma_store && et == 0) ptx::bulk_wait_read_all();
     } else if constexpr (DIRECT) {
         // ---------------- transposer warps (FORM 2) ----------------
         // A raw box is 64 channel rows of xw input columns (row pitch 2 xw

@@ -701,8 +701,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
-        // C is written, and the staging boxes are free, once the stores end.
-        if (lane == 0) ptx::bulk_wait_all();
+        // The staging boxes are free once the stores have read them; their
+        // writes to C complete with the grid, before anything that waits
+        // for it (a later kernel, or griddepcontrol.wait) reads C.
+        if (lane == 0) ptx::bulk_wait_read_all();
         __syncwarp();
     }
 

@@ -140,24 +140,47 @@ def workspace_bytes() -> int:
 # ---- kernels (need torch and a GPU) --------------------------------------------
 
 
+_TORCH = None
+_DTYPE_CODES = None
+_RAW_STREAM = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _TORCH
+    if _TORCH is None:
+        import torch
+        _TORCH = torch
+    return _TORCH
 
 
 def _dtype_code(t) -> int:
-    torch = _torch()
-    m = {torch.float16: _abi.F16, torch.bfloat16: _abi.BF16, torch.float32: _abi.F32}
-    if t.dtype not in m:
+    global _DTYPE_CODES
+    if _DTYPE_CODES is None:
+        torch = _torch()
+        _DTYPE_CODES = {torch.float16: _abi.F16, torch.bfloat16: _abi.BF16,
+                        torch.float32: _abi.F32}
+    code = _DTYPE_CODES.get(t.dtype)
+    if code is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
-    return m[t.dtype]
+    return code
 
 
 def _stream_handle(stream):
-    torch = _torch()
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return C.c_void_p(stream.cuda_stream)
+    """The CUDA stream handle of `stream`, or of the current device's current
+    stream.  The latter is read through torch's raw-stream query where it
+    exists (torch.cuda.current_stream() builds a Python object per call)."""
+    global _RAW_STREAM
+    if stream is not None:
+        return C.c_void_p(stream.cuda_stream)
+    if _RAW_STREAM is None:
+        tc = _torch()._C
+        if hasattr(tc, "_cuda_getCurrentRawStream") and hasattr(tc, "_cuda_getDevice"):
+            get, dev = tc._cuda_getCurrentRawStream, tc._cuda_getDevice
+            _RAW_STREAM = lambda: get(dev())
+        else:
+            cur = _torch().cuda.current_stream
+            _RAW_STREAM = lambda: cur().cuda_stream
+    return C.c_void_p(_RAW_STREAM())
 
 
 def workspace(device=None):
@@ -179,21 +202,23 @@ def _check_operand(t, name):
 
 
 def _gemm_desc(a, b, out, batched: bool) -> _abi.GemmDesc:
-    for t, nm in ((a, "a"), (b, "b"), (out, "out")):
-        _check_operand(t, nm)
+    sa, sb, sc = a.stride(), b.stride(), out.stride()
+    if not (a.is_cuda and b.is_cuda and out.is_cuda) or sa[-1] != 1 or sb[-1] != 1 or sc[-1] != 1:
+        for t, nm in ((a, "a"), (b, "b"), (out, "out")):
+            _check_operand(t, nm)
+    ha, hb, hc = a.shape, b.shape, out.shape
+    m, k, n = ha[-2], ha[-1], hb[-1]
+    if hb[-2] != k or hc[-2] != m or hc[-1] != n:
+        raise ValueError(f"shape mismatch: {tuple(ha)} x {tuple(hb)} -> {tuple(hc)}")
     d = _abi.GemmDesc()
-    d.m, d.k = a.shape[-2], a.shape[-1]
-    d.n = b.shape[-1]
-    if b.shape[-2] != d.k or out.shape[-2] != d.m or out.shape[-1] != d.n:
-        raise ValueError(f"shape mismatch: {tuple(a.shape)} x {tuple(b.shape)} -> "
-                         f"{tuple(out.shape)}")
-    d.batch = a.shape[0] if batched else 1
+    d.m, d.n, d.k = m, n, k
+    d.batch = ha[0] if batched else 1
     d.a, d.b, d.c = a.data_ptr(), b.data_ptr(), out.data_ptr()
-    d.lda, d.ldb, d.ldc = a.stride(-2), b.stride(-2), out.stride(-2)
+    d.lda, d.ldb, d.ldc = sa[-2], sb[-2], sc[-2]
     if batched:
-        if b.shape[0] != d.batch or out.shape[0] != d.batch:
+        if hb[0] != d.batch or hc[0] != d.batch:
             raise ValueError("batch sizes differ")
-        d.stride_a, d.stride_b, d.stride_c = a.stride(0), b.stride(0), out.stride(0)
+        d.stride_a, d.stride_b, d.stride_c = sa[0], sb[0], sc[0]
     d.a_dtype, d.b_dtype, d.c_dtype = _dtype_code(a), _dtype_code(b), _dtype_code(out)
     return d
 
@@ -322,8 +347,16 @@ def conv2d_host(x_host, w_host, y_host, x_dev, w_dev, y_dev, stride=(1, 1), pad=
     return y_host
 
 
+_OUT_HW = {}
+
+
 def conv_out_hw(h, w, kh, kw, stride, pad, dil):
-    """Output height and width of a convolution (tiles_conv_out_hw)."""
+    """Output height and width of a convolution (tiles_conv_out_hw; the
+    library's answer is kept per geometry, so repeated calls skip it)."""
+    key = (h, w, kh, kw, tuple(stride), tuple(pad), tuple(dil))
+    hit = _OUT_HW.get(key)
+    if hit is not None:
+        return hit
     d = _abi.ConvDesc()
     d.n, d.c, d.h, d.w, d.c_out, d.kh, d.kw = 1, 1, h, w, 1, kh, kw
     d.sh, d.sw = stride
@@ -331,6 +364,8 @@ def conv_out_hw(h, w, kh, kw, stride, pad, dil):
     d.dh, d.dw = dil
     oh, ow = C.c_int32(0), C.c_int32(0)
     _check(load().tiles_conv_out_hw(C.byref(d), C.byref(oh), C.byref(ow)), "tiles_conv_out_hw")
+    if len(_OUT_HW) < 4096:
+        _OUT_HW[key] = (oh.value, ow.value)
     return oh.value, ow.value
 
 

@@ -62,3 +62,54 @@ def test_both_arms_describe_each_workload_alike():
         assert (c["workload"], c["seed"], c["accumulate"]) == (name, wl.seed, "f32")
         assert c["parallelism"] == "replicas x2" and "tile" not in c
         assert c == bench.workload_config(wl, 2)
+
+
+def test_rotation_keeps_each_steps_inputs_out_of_l2():
+    # Between two uses of one operand copy the other copies pass through L2:
+    # at least twice its capacity, whatever the size of one copy.
+    import synth_inputs as S
+    for set_bytes in (1, 2 << 20, 77_217_792, 100_663_296, 125_536_000, 129 << 20,
+                      268_435_456, 1 << 34):
+        r = bench.rotation_sets(set_bytes)
+        assert r >= 2
+        assert (r - 1) * set_bytes >= 2 * bench.L2_BYTES or r == 2 and set_bytes >= 2 * bench.L2_BYTES
+        # No more copies than that needs.
+        assert r == 2 or (r - 2) * set_bytes < 2 * bench.L2_BYTES
+    # The seeded workloads' copies, as the bench counts them.
+    gemm = S.WORKLOADS["gemm_4096"]
+    one = gemm.b * (gemm.m * gemm.k + gemm.k * gemm.n) * 2 + gemm.b * gemm.m * gemm.n * 2
+    assert bench.rotation_sets(one) == 4
+
+
+class _FakeJob:
+    def __init__(self):
+        self.calls = []
+        self.sets = [0, 1, 2]
+
+    def step(self, i, stream):
+        self.calls.append(i % len(self.sets))
+
+
+def test_timed_steps_continue_the_rotation_from_the_warm_up(monkeypatch):
+    # timed_rotating runs steps start .. start + K - 1, so that the first
+    # timed step uses the copy after the warm-up's last one.
+    import types
+    events = []
+
+    class Ev:
+        def __init__(self, enable_timing=False):
+            self.t = None
+
+        def record(self, stream=None):
+            self.t = len(events)
+            events.append(self)
+
+        def elapsed_time(self, other):
+            return 6.0
+
+    fake_torch = types.SimpleNamespace(cuda=types.SimpleNamespace(Event=Ev, synchronize=lambda: None))
+    monkeypatch.setitem(__import__("sys").modules, "torch", fake_torch)
+    job = _FakeJob()
+    ms, (t0, t1) = bench.timed_rotating(job, None, 4, start=5)
+    assert job.calls == [2, 0, 1, 2]
+    assert ms == 1.5 and t1 >= t0

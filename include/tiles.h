@@ -302,8 +302,7 @@ double tiles_c0_bytes(int64_t b, int64_t m, int64_t n, int64_t k, int bm, int bn
  * enumerates bm,bn in {16..256}, bk in {16..128} (<= K), stages 2..4,
  * threads 128/256/512 and ranks by (round(C0), -blocks_per_sm, smem_total);
  * GB300 mode enumerates the compiled sm_103a kernel variants and ranks by
- * (est_clocks, a split last round after an unsplit one, round(C0),
- * -blocks_per_sm, smem_total).  Ties keep the
+ * (est_clocks, round(C0), -blocks_per_sm, smem_total).  Ties keep the
  * enumeration order.  Writes min(capacity, n) verdicts to out (out may be
  * NULL when capacity is 0) and always writes *n_feasible. */
 int tiles_plan(const tiles_device* dev, const tiles_problem* prob, tiles_verdict* out,

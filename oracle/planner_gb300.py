@@ -54,11 +54,8 @@ Rules
        Ties keep that order and the fewer parts.  tail_split reports s, -1
        for N-halves, 0 for whole tiles.  A CTA-pair kernel adds
        pair_launch_clocks, its extra fixed cost per launch.
-  rank (est_clocks, a split last round after an unsplit one, round(C0),
-       -blocks per SM, smem_total), stable over the variant order.  (Equal
-       estimates with and without a split last round mean equal K loops; the
-       split units carry what the estimate does not count: each reloads its
-       tile's A panel and finishes a partly used accumulator.)
+  rank (est_clocks, round(C0), -blocks per SM, smem_total), stable over the
+       variant order.
 """
 
 from __future__ import annotations
@@ -306,6 +303,5 @@ def plan(b: int, m: int, n: int, k: int, dev: GB300Device, tiles, in_bytes: int 
         v.c0_bytes = page.c0_bytes(m, n, k, cfg.bm, cfg.bn, in_bytes, out_bytes, b)
         v.est_clocks = est_clocks(v, dev, k)
         kept.append(v)
-    kept.sort(key=lambda v: (v.est_clocks, v.tail_split != 0, round(v.c0_bytes),
-                             -v.blocks_per_sm, v.smem_total))
+    kept.sort(key=lambda v: (v.est_clocks, round(v.c0_bytes), -v.blocks_per_sm, v.smem_total))
     return kept

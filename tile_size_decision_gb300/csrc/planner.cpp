@@ -389,13 +389,8 @@ int plan(const tiles_device& dev, const tiles_problem& p, std::vector<tiles_verd
     } else if (p.mode == TILES_MODE_GB300) {
         if (in_b != 2) return TILES_ERR_UNSUPPORTED_DTYPE;
         sweep_gb300(dev, p, in_b, out_b, &kept);
-        // Equal estimates: an unsplit last round before a split one (the
-        // split units reload their tiles' A panels and finish partly used
-        // accumulators, which the estimate does not count), then traffic.
         std::stable_sort(kept.begin(), kept.end(), [&](const Ranked& a, const Ranked& b) {
             if (a.v.est_clocks != b.v.est_clocks) return a.v.est_clocks < b.v.est_clocks;
-            const bool sa = a.v.tail_split != 0, sb = b.v.tail_split != 0;
-            if (sa != sb) return !sa;
             return traffic_first(a, b);
         });
     } else {

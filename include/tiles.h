@@ -511,15 +511,18 @@ typedef struct {
     int32_t status;          /* TILES_OK, or why the candidate could not run (us is then 0) */
     int32_t tail_mode;       /* the schedule the launches used: 0 none needed, 1 N-halves, 2 K split */
     int32_t ksplit;          /* K parts of a split last round (1 otherwise) */
-    float us;                /* median launch time over the timed repetitions, microseconds */
+    float us;                /* time per launch, microseconds: the faster of two passes of
+                                reps launches back to back, each pass's time over reps */
 } tiles_tune_result;
 
 /* Time the planner's top_k configurations (GB300 mode, in rank order) for
  * this GEMM, each with every last-round schedule it admits (the planner's
  * own choice first, then whole tiles, N-halves, a K split when the
  * workspace holds its partials; ties keep the earlier): one untimed
- * launch, then reps launches bracketed by CUDA events on `stream`, of which
- * the median counts.  The fastest becomes the tuned configuration of the
+ * launch, then two passes of reps launches back to back, each between one
+ * pair of CUDA events on `stream`; the faster pass's time over reps counts
+ * (launches overlap their neighbours' set-up, so a launch has no time of
+ * its own between events).  The fastest becomes the tuned configuration of the
  * problem (batch, m, n, k, dtypes, SM count), which tiles_gemm and
  * tiles_gemm_batched use when called with cfg == NULL; *best receives it.
  *

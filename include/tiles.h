@@ -487,12 +487,10 @@ size_t tiles_conv_workspace_bytes(const tiles_conv_desc* desc, int tile_oh);
  * routine.  The GEMM needs exactly that much (its timeout error word): the
  * last round of tiles never splits along K here (it runs as whole tiles or
  * N-halves), and a cfg that forces a K split, whose partial tiles would need
- * more, is rejected with TILES_ERR_TOO_LARGE.  A call made outside stream
- * capture looks up the array's device address (cudaGetSymbolAddress) with
- * the current device (so that it follows a device reset, after which the
- * array loads at a new address); a call during stream capture uses the
- * address the last call outside capture found on that device, so make one
- * call on each device before any capture.  All calls share the array: a
+ * more, is rejected with TILES_ERR_TOO_LARGE.  Every call looks up the
+ * array's device address (cudaGetSymbolAddress) on the current device, so
+ * that it follows a device reset, after which the array loads at a new
+ * address.  All calls share the array: a
  * timeout recorded by a call stays until a call with wait != 0 reads and
  * clears it, and calls that overlap on the GPU race on it.
  * wait == 0: asynchronous on `stream`, returns the launch status.

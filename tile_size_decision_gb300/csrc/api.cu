@@ -521,36 +521,19 @@ namespace tiles {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = sizeof(tiles_noalloc_scratch);
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
-
 // The device address of the scratch array on the current device.  In host
 // code the array's name is only a host-side stand-in, so the address is
-// asked of the runtime with the device current.  A call outside stream
-// capture asks again (after a device reset the module, and the array, load
-// anew at another address); a call during capture uses the address the last
-// call outside capture found on this device.
-int noalloc_scratch(cudaStream_t stream, void** out) {
+// asked of the runtime, with the device current, on every call (after a
+// device reset the module, and the array, load anew at another address).
+int noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(TILES_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return fail(TILES_ERR_INVALID_ARG, "device ordinal %d beyond %d", dev, kMaxDevices);
-    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) {
-        cudaGetLastError();
-        capture = cudaStreamCaptureStatusActive;     // unknown: keep the known address
-    }
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev] || capture == cudaStreamCaptureStatusNone) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, tiles_noalloc_scratch);
-        if (e != cudaSuccess || !p)
-            return fail(TILES_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-        g_noalloc_addr[dev] = p;
-    }
-    *out = g_noalloc_addr[dev];
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, tiles_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+        return fail(TILES_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    *out = p;
     return TILES_OK;
 }
 
@@ -1021,7 +1004,7 @@ int tiles_gemm_noalloc(const tiles_gemm_desc* desc, const tiles_config* cfg, voi
                         "the static array holds %zu", (long long)need, kNoAllocScratchBytes);
     }
     void* scratch = nullptr;
-    int s = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);
+    int s = noalloc_scratch(&scratch);
     if (s != TILES_OK) return s;
     s = gemm_common(desc, cfg, scratch, kNoAllocScratchBytes, stream, true);
     if (s != TILES_OK || !wait) return s;

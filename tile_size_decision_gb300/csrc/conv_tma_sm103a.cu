@@ -1636,7 +1636,9 @@ bool rows_plan(const tiles_conv_desc* d, int64_t oh, int64_t ow, int tile_oh, in
             rp.wp.stg_pitch = pitch;
             rp.wp.stg_bytes = stg;
             // The filter's start-up passes use everything from raw slot 1
-            // on (the direct form's first raw box loads beside them).
+            // on (the direct form's first raw box loads beside them; a 3x3
+            // filter read from its OIHW rows starts as high as its 9 boxes
+            // allow, so that more raw boxes load beside it).
             rp.wp.w_slots = (ring_bytes + stg - (direct ? raw_b : 0)) / kWtWeightBlockBytes;
             rp.wp.smem = std::max(ring_bytes + stg + kSmemBarrierBytes + kSmemAlignSlack,
                                   116 * 1024);

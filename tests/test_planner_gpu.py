@@ -106,6 +106,35 @@ def operands(wl):
     return a, b, c
 
 
+def alternate_times(a, b, c, ws, batched, cfg_x, cfg_y, rounds=7, launches=20):
+    """Median microseconds per launch of two configurations, each timed as
+    `launches` back-to-back launches between one pair of events, the two
+    alternating for `rounds` rounds."""
+    def run(cfg):
+        if batched:
+            T.gemm_batched(a, b, out=c, cfg=cfg, workspace=ws)
+        else:
+            T.gemm(a, b, out=c, cfg=cfg, workspace=ws)
+
+    times = ([], [])
+    for cfg in (cfg_x, cfg_y):
+        run(cfg)
+    torch.cuda.synchronize()
+    for _ in range(rounds):
+        for i, cfg in enumerate((cfg_x, cfg_y)):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(launches):
+                run(cfg)
+            e.record()
+            torch.cuda.synchronize()
+            times[i].append(1000.0 * s.elapsed_time(e) / launches)
+    T.check(ws)
+    med = lambda v: sorted(v)[len(v) // 2]
+    return med(times[0]), med(times[1])
+
+
 @pytest.mark.parametrize("name", ["gemm_4096", "gemm_batched", "gemm_ragged", "gemm_512"])
 def test_planner_choice_against_the_measured_shortlist(dev, name):
     wl = S.WORKLOADS[name]
@@ -135,8 +164,18 @@ def test_planner_choice_against_the_measured_shortlist(dev, name):
                     (cfg.bm, cfg.bn, cfg.stages, cfg.cta_group) and r["tail_asked"] == 0)
 
     table = [(v.cfg.bm, v.cfg.bn, v.cfg.cta_group, v.est_clocks, own(v.cfg)["us"]) for v in top]
-    # 3%, or 0.3 us on launches of a few microseconds (their jitter).
-    assert own(first)["us"] <= max(1.03 * fastest, fastest + 0.3), (table, fastest)
+    # 3%, or 0.3 us on launches of a few microseconds (their jitter).  The
+    # shortlist times its candidates one after another, so a clock that
+    # drifts between them can misorder two close ones: a first choice
+    # outside the band is timed again against the fastest, alternately.
+    us_first = own(first)["us"]
+    if us_first > max(1.03 * fastest, fastest + 0.3):
+        best = min(ran, key=lambda r: r["us"])
+        cfg_best = T.make_config(best["bm"], best["bn"], first.bk, best["stages"], first.threads,
+                                 first.instr, first.acc_bufs, best["cta_group"],
+                                 tail=best["tail_asked"])
+        us_first, fastest = alternate_times(a, b, c, ws, wl.b > 1, first, cfg_best)
+    assert us_first <= max(1.03 * fastest, fastest + 0.3), (table, fastest, us_first)
     for i, (_, _, _, est_i, us_i) in enumerate(table):
         for _, _, _, est_j, us_j in table[i + 1:]:
             if est_i < 0.8 * est_j:

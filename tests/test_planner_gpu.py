@@ -17,7 +17,8 @@ and that the script measures nothing.  These tests make that confirmation:
     is the native plan bit for bit;
   * ranking: on the four GEMM workloads the planner's first choice (with its
     own last-round schedule) runs within 3% of the fastest candidate of the
-    measured shortlist, and the time estimate orders the shortlist's
+    measured shortlist (timed again, alternating with the fastest, when the
+    shortlist's one-after-another timings put it outside), and the time estimate orders the shortlist's
     configurations as they measure wherever it separates them by more than
     20% (the model's error band, from measured shortlists of 16 shapes).
 """

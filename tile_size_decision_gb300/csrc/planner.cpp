@@ -73,11 +73,9 @@ void settle_residency(const tiles_device& dev, tiles_verdict* v, bool tensor_mem
     }
 }
 
-// Page mode, one configuration.
-void evaluate_page(const tiles_device& dev, const tiles_config& cfg, int elem_bytes,
-                   int accum_bytes, tiles_verdict* v) {
-    ShapeRule rule;
-    shape_rule(cfg.instr, &rule);
+// Page mode, one configuration of the MMA family whose shape rule is `rule`.
+void evaluate_page(const tiles_device& dev, const tiles_config& cfg, const ShapeRule& rule,
+                   int elem_bytes, int accum_bytes, tiles_verdict* v) {
     // C3: each tile edge and the thread count is a whole multiple of the
     // family's shape, and the block stays within the per-block thread limit;
     // every broken condition counts once.
@@ -182,7 +180,7 @@ int evaluate(const tiles_device& dev, const tiles_config& cfg, int elem_bytes, i
     }
     ShapeRule rule;
     if (!shape_rule(cfg.instr, &rule)) return TILES_ERR_INVALID_ARG;
-    evaluate_page(dev, cfg, elem_bytes, accum_bytes, v);
+    evaluate_page(dev, cfg, rule, elem_bytes, accum_bytes, v);
     return TILES_OK;
 }
 
